@@ -1,0 +1,280 @@
+"""Plain fp64 definition of the MoE layer forward, step by step.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): slow, single-purpose, obviously
+correct. Every array is numpy float64 / int64; library primitives (matmul, argsort,
+bincount, cumsum, exp) serve as steps, with no blocking, fusion or reordering beyond the
+definitions below.
+
+Sources, cited by page title and section:
+  [HF-EP]  Hugging Face Transformers docs, "Expert parallelism": sections
+           "DistributedConfig", "Token dispatch", "How the sizes combine".
+  [UL-EP]  Ultralytics glossary, "Expert Parallelism": sections "How tokens move between
+           GPUs" (the four steps and the routing example) and "Load balancing and
+           capacity".
+
+Readings taken where the pages are silent (each listed in the design notes):
+  * the router score is the raw linear logit; the k largest are chosen, ties going to
+    the lower expert id; the routing weights are a softmax over the k chosen logits;
+  * each expert is a SwiGLU FFN  y = Wd (silu(Wg x) * (Wu x)), no biases;
+  * capacity C = ceil(cf * N * k / E) per expert over the whole call; the first C pairs
+    of an expert in token order are kept, the rest contribute zero, with no
+    renormalisation of the surviving weights;
+  * the mask-and-sum mode sums partition partial outputs in partition order.
+
+Parity status: routing and load counts are pinned by the worked example's printed loads;
+dispatch, expert math and combine are pinned by an independent dense brute force, a
+library SwiGLU-MLP special case and a library softmax special case (see tests/).
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---------------------------------------------------------------- step 1: routing
+def router_logits(x, w_router, b_router=None):
+    """[UL-EP] "How tokens move between GPUs", step 1 and its routing example: the
+    router is a linear layer (weight [E, H] in nn.Linear's out x in layout, optional
+    bias [E]) that scores every token against every expert.
+    logits[t, e] = b[e] + sum_h x[t, h] * w_router[e, h]."""
+    logits = _f64(x) @ _f64(w_router).T
+    if b_router is not None:
+        logits = logits + _f64(b_router)[None, :]
+    return logits
+
+
+def top_k_experts(logits, k):
+    """[UL-EP] step 1: keep the k best-scoring experts of each token (the example takes
+    top-k of the raw logits). Returned in descending score order; equal scores are
+    ordered by lower expert id (the pages do not fix a tie rule; this is ours).
+    A stable ascending sort of -logits realises exactly that order."""
+    order = np.argsort(-_f64(logits), axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
+
+
+def routing_weights(logits, idx):
+    """[UL-EP] step 4 weights expert outputs "by the router scores"; [HF-EP] "Token
+    dispatch" combines "with the routing weights". Reading: softmax over the k chosen
+    logits, w[t, j] = exp(l[t, idx[t, j]] - m_t) / sum_j' exp(l[t, idx[t, j']] - m_t),
+    m_t the largest chosen logit."""
+    chosen = np.take_along_axis(_f64(logits), idx, axis=1)
+    m = chosen.max(axis=1, keepdims=True)
+    e = np.exp(chosen - m)
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def route(x, w_router, b_router, k):
+    """Step 1 end to end: (logits, topk_idx [N,k] int64, topk_w [N,k] float64)."""
+    logits = router_logits(x, w_router, b_router)
+    idx = top_k_experts(logits, k)
+    return logits, idx, routing_weights(logits, idx)
+
+
+# ---------------------------------------------------------------- step 2: dispatch
+def expert_partition(expert, num_experts, ep_size):
+    """[HF-EP] "How the sizes combine": ep_size splits the expert list into ep_size
+    contiguous blocks of num_experts/ep_size; [UL-EP] routing example: owner =
+    expert // (num_experts // num_gpus)."""
+    if num_experts % ep_size:
+        raise ValueError("ep_size must divide the number of experts")
+    return np.asarray(expert) // (num_experts // ep_size)
+
+
+def load_counts(idx, num_experts, ep_size):
+    """[UL-EP] routing example: bincount of the chosen expert ids (per-expert load) and
+    of their owners (per-partition load)."""
+    flat = np.asarray(idx).reshape(-1)
+    per_expert = np.bincount(flat, minlength=num_experts).astype(np.int64)
+    per_part = np.bincount(expert_partition(flat, num_experts, ep_size),
+                           minlength=ep_size).astype(np.int64)
+    return per_expert, per_part
+
+
+def expert_capacity(capacity_factor, num_tokens, k, num_experts):
+    """[UL-EP] "Load balancing and capacity": each expert takes at most capacity_factor
+    times its equal share of the batch's assignments (e.g. 1.25). Reading:
+    C = ceil(cf * N * k / E), evaluated in exact rational arithmetic on the float32
+    value of cf (the library's argument type). None (no limit) when cf <= 0 or None."""
+    if capacity_factor is None:
+        return None
+    cf = Fraction(float(np.float32(capacity_factor)))
+    if cf <= 0:
+        return None
+    return math.ceil(cf * num_tokens * k / num_experts)
+
+
+def dispatch_layout(idx, num_experts, ep_size, capacity=None):
+    """[HF-EP] "Token dispatch": every (token, expert) pair is sent to the partition that
+    owns the expert; [UL-EP] step 2. On one device the send buffer is grouped by expert,
+    so each partition's rows are contiguous (experts are split contiguously).
+
+    Pair p = t*k + j. Its rank is the number of earlier pairs (lower token index) routed
+    to the same expert. With a capacity C, a pair is kept iff rank < C ([UL-EP] "Load
+    balancing and capacity": overflow pairs skip that expert; reading: the first C in
+    token order are kept).
+
+    Returns dict of int64 arrays:
+      routed_counts [E]    pairs routed to each expert before capacity
+      counts        [E]    pairs kept
+      expert_offsets[E+1]  exclusive prefix sum of counts (send-row start per expert)
+      part_offsets  [P+1]  send-row start per partition = expert_offsets[p*E/P]
+      slot_pos      [N*k]  send row of pair p, -1 when dropped
+      perm          [A']   pair id held by send row r (inverse of slot_pos on kept pairs)
+    """
+    idx = np.asarray(idx)
+    N, k = idx.shape
+    E = num_experts
+    flat = idx.reshape(-1).astype(np.int64)
+    routed = np.bincount(flat, minlength=E).astype(np.int64)
+    # pairs grouped by expert; the stable sort keeps pair (= token) order inside a group
+    by_expert = np.argsort(flat, kind="stable")
+    group_start = np.concatenate([[0], np.cumsum(routed)[:-1]])
+    rank = np.empty(N * k, dtype=np.int64)
+    rank[by_expert] = np.arange(N * k) - group_start[flat[by_expert]]
+    keep = np.ones(N * k, dtype=bool) if capacity is None else rank < capacity
+    counts = np.bincount(flat[keep], minlength=E).astype(np.int64)
+    expert_offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    slot_pos = np.where(keep, expert_offsets[flat] + rank, -1).astype(np.int64)
+    perm = np.empty(int(expert_offsets[-1]), dtype=np.int64)
+    perm[slot_pos[keep]] = np.nonzero(keep)[0]
+    part_offsets = expert_offsets[np.arange(ep_size + 1) * (E // ep_size)]
+    return dict(routed_counts=routed, counts=counts, expert_offsets=expert_offsets,
+                part_offsets=part_offsets, slot_pos=slot_pos, perm=perm)
+
+
+def permute(x, perm, k):
+    """[UL-EP] step 2 (the all-to-all that carries each token's hidden state to its
+    experts' owner), on one device: send row r holds the hidden state of token
+    perm[r] // k."""
+    return _f64(x)[np.asarray(perm, dtype=np.int64) // k]
+
+
+# ---------------------------------------------------------------- step 3: experts
+def silu(z):
+    """silu(z) = z * sigmoid(z) = z / (1 + exp(-z))."""
+    z = _f64(z)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def swiglu_expert(rows, w_gate, w_up, w_down):
+    """One expert's feed-forward network on its received rows ([UL-EP] step 3). The
+    pages never define the expert network; reading: SwiGLU without biases,
+    y = W_down (silu(W_gate x) * (W_up x)), weights in nn.Linear layout
+    (w_gate, w_up [I, H]; w_down [H, I])."""
+    rows = _f64(rows)
+    g = rows @ _f64(w_gate).T
+    u = rows @ _f64(w_up).T
+    return (silu(g) * u) @ _f64(w_down).T
+
+
+def expert_outputs(send, expert_offsets, w_gate, w_up, w_down,
+                   expert_begin=0, expert_end=None):
+    """[UL-EP] step 3 / [HF-EP] "Token dispatch": each partition runs its local experts
+    on what it received. Send rows of expert e are [expert_offsets[e],
+    expert_offsets[e+1]). Rows of experts outside [expert_begin, expert_end) stay 0."""
+    send = _f64(send)
+    E = len(expert_offsets) - 1
+    expert_end = E if expert_end is None else expert_end
+    y = np.zeros((send.shape[0], np.shape(w_down)[1]), dtype=np.float64)
+    for e in range(expert_begin, expert_end):
+        a, b = int(expert_offsets[e]), int(expert_offsets[e + 1])
+        if b > a:
+            y[a:b] = swiglu_expert(send[a:b], w_gate[e], w_up[e], w_down[e])
+    return y
+
+
+# ---------------------------------------------------------------- step 4: combine
+def combine_dispatch(y_send, slot_pos, topk_w, num_tokens, k):
+    """[UL-EP] step 4 / [HF-EP] "Token dispatch": expert outputs return to their token
+    and are summed weighted by the routing weights. out[t] = sum over kept slots j, in
+    slot order, of w[t, j] * y[slot_pos[t*k + j]]. A dropped pair adds nothing (the
+    token's residual path lives outside the layer)."""
+    y_send = _f64(y_send)
+    out = np.zeros((num_tokens, y_send.shape[1]), dtype=np.float64)
+    sp = np.asarray(slot_pos).reshape(num_tokens, k)
+    w = _f64(topk_w).reshape(num_tokens, k)
+    for j in range(k):
+        kept = sp[:, j] >= 0
+        out[kept] += w[kept, j, None] * y_send[sp[kept, j]]
+    return out
+
+
+def combine_mask_sum(y_send, slot_pos, topk_idx, topk_w, num_experts, ep_size):
+    """[HF-EP] "DistributedConfig" / plan rules "ep_router" + "moe_tp_experts": each
+    partition masks the experts it does not own, computes its local ones, and an
+    all-reduce sums the partitions' outputs. Here partial[p, t] = sum over kept slots j
+    of token t whose expert lives in partition p (slot order) of w[t,j] * y, and
+    out = partial[0] + partial[1] + ... in partition order. Returns (partials, out)."""
+    y_send = _f64(y_send)
+    idx = np.asarray(topk_idx)
+    N, k = idx.shape
+    sp = np.asarray(slot_pos).reshape(N, k)
+    w = _f64(topk_w).reshape(N, k)
+    owner = expert_partition(idx, num_experts, ep_size)
+    partials = np.zeros((ep_size, N, y_send.shape[1]), dtype=np.float64)
+    for p in range(ep_size):
+        for j in range(k):
+            sel = (sp[:, j] >= 0) & (owner[:, j] == p)
+            partials[p, sel] += w[sel, j, None] * y_send[sp[sel, j]]
+    out = np.zeros((N, y_send.shape[1]), dtype=np.float64)
+    for p in range(ep_size):
+        out += partials[p]
+    return partials, out
+
+
+# ---------------------------------------------------------------- the whole layer
+def layer_forward(x, w_router, b_router, w_gate, w_up, w_down, top_k, ep_size,
+                  capacity_factor=None, mode="dispatch"):
+    """Route -> dispatch -> local experts -> weighted combine, all in fp64.
+    Returns a dict with every intermediate (logits, topk_idx, topk_w, the dispatch
+    layout, send, y_send, out and, in mask mode, partials)."""
+    x = _f64(x)
+    N = x.shape[0]
+    E = np.shape(w_router)[0]
+    logits, idx, w = route(x, w_router, b_router, top_k)
+    C = expert_capacity(capacity_factor, N, top_k, E)
+    lay = dispatch_layout(idx, E, ep_size, C)
+    send = permute(x, lay["perm"], top_k)
+    y_send = expert_outputs(send, lay["expert_offsets"], w_gate, w_up, w_down)
+    res = dict(logits=logits, topk_idx=idx, topk_w=w, capacity=C, send=send,
+               y_send=y_send, **lay)
+    if mode == "dispatch":
+        res["out"] = combine_dispatch(y_send, lay["slot_pos"], w, N, top_k)
+    elif mode == "mask_sum":
+        res["partials"], res["out"] = combine_mask_sum(y_send, lay["slot_pos"], idx, w,
+                                                       E, ep_size)
+    else:
+        raise ValueError(mode)
+    return res
+
+
+def token_outputs(x_rows, idx_rows, w_rows, keep_rows, expert_weights):
+    """Layer output of a few tokens, one at a time (for sampled checks at full size).
+
+    x_rows [n, H]; idx_rows / w_rows / keep_rows [n, k] (keep from the full-batch
+    dispatch layout, since capacity depends on every token). expert_weights(e) returns
+    (w_gate[e], w_up[e], w_down[e]). out[i] = sum_j keep * w * FFN_idx(x_i), in j order.
+    """
+    x_rows = _f64(x_rows)
+    n, k = np.shape(idx_rows)
+    needed = sorted({int(e) for i in range(n) for j in range(k) if keep_rows[i][j]})
+    y = {}
+    for e in needed:
+        wg, wu, wd = expert_weights(e)
+        for i in range(n):
+            for j in range(k):
+                if keep_rows[i][j] and int(idx_rows[i][j]) == e:
+                    y[(i, j)] = swiglu_expert(x_rows[i:i + 1], wg, wu, wd)[0]
+    out = np.zeros((n, np.shape(x_rows)[1]), dtype=np.float64)
+    for i in range(n):
+        for j in range(k):
+            if keep_rows[i][j]:
+                out[i] += float(w_rows[i][j]) * y[(i, j)]
+    return out
