@@ -264,7 +264,8 @@ def token_outputs(x_rows, idx_rows, w_rows, keep_rows, expert_weights):
     """
     x_rows = _f64(x_rows)
     n, k = np.shape(idx_rows)
-    needed = sorted({int(e) for i in range(n) for j in range(k) if keep_rows[i][j]})
+    needed = sorted({int(idx_rows[i][j]) for i in range(n) for j in range(k)
+                     if keep_rows[i][j]})
     y = {}
     for e in needed:
         wg, wu, wd = expert_weights(e)

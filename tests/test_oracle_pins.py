@@ -323,6 +323,19 @@ def test_exact_variant_router_sums_fit_fp32(shape):
     assert bound < limit
 
 
+def test_token_outputs_equal_full_batch_layer():
+    """The per-token path used for sampled checks at full size gives the same rows as the
+    whole-batch path (with the batch's keep decisions)."""
+    x, wr, b, wg, wu, wd = tiny_inputs(31, 40, 8, 6, 5)
+    res = oracle.layer_forward(x, wr, b, wg, wu, wd, 2, 5, capacity_factor=0.6)
+    sample = np.array([0, 3, 17, 39])
+    keep = (res["slot_pos"].reshape(40, 2) >= 0)[sample]
+    assert not keep.all()
+    got = oracle.token_outputs(x[sample], res["topk_idx"][sample], res["topk_w"][sample], keep,
+                               lambda e: (wg[e], wu[e], wd[e]))
+    assert rel_err(got, res["out"][sample]) < 1e-13
+
+
 # ------------------------------------------------------------------ planted mistakes
 MUTANTS = {
     "tie_to_higher_id": ("top_k_experts",
