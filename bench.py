@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE layer forward (route -> dispatch -> grouped GEMM -> combine).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl b300|reference]
+
+Prints ONE JSON line (rank 0). A step is one full moe_layer_forward over one batch of
+synthetic, seeded inputs already resident in HBM. The default workload is the
+gpt-oss-120b-shaped layer (8192 tokens x hidden 2880, 128 experts, top-4, SwiGLU
+intermediate 2880, 8 logical EP partitions). Its 6.4 GB of expert weights are ~50x the
+L2, so no L2 flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs the same layer on its own batch (different
+seed): the expert-parallel partitions live inside one GPU, so ranks share no data and
+the scaling is weak, with no collective on the data path.
+
+--impl reference times the fp64 CPU oracle instead (rank 0 only), on a bounded sample
+of the same workload, extrapolated to the whole batch.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (route→dispatch→grouped GEMM→combine); % of roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic work
+def stage_work(shape, counts):
+    """Algorithmic bytes and flops of each stage, given the kept per-expert counts.
+    Only what the method must move or compute: every operand read once, every result
+    written once (weights of experts that received no token are not touched)."""
+    s = 2 if shape.dtype == "bf16" else 4
+    N, H, I, E, k = shape.N, shape.H, shape.I, shape.E, shape.top_k
+    A = int(np.sum(counts))                     # kept pairs
+    touched = int(np.count_nonzero(counts))
+    nseg = math.ceil(N / 64)
+    bias = 4 * E if (shape.bias or shape.zipf_s) else 0
+    return {
+        "route": dict(bytes=N * H * s + E * H * s + bias + N * k * 8 + nseg * E * 4,
+                      flops=2 * N * H * E),
+        "scan": dict(bytes=3 * nseg * E * 4 + 4 * E * 4, flops=0),
+        "assign": dict(bytes=N * k * 8 + A * 4 + nseg * E * 4, flops=0),
+        "permute": dict(bytes=N * H * s + A * H * s + N * k * 4, flops=0),
+        "gate_up": dict(bytes=touched * 2 * I * H * s + A * H * s + A * I * s,
+                        flops=4 * A * H * I),
+        "down": dict(bytes=touched * H * I * s + A * I * s + A * H * s + A * 8,
+                     flops=2 * A * H * I),
+        "combine": dict(bytes=A * H * s + N * H * s + N * k * 4, flops=0),
+    }
+
+
+def roofline_entry(work, ms, peaks, source, dtype):
+    t = ms / 1e3
+    hbm = peaks["hbm_gbs"]
+    tf = peaks["bf16_tflops"] if dtype == "bf16" else None
+    t_mem = work["bytes"] / (hbm * 1e9)
+    t_flop = work["flops"] / (tf * 1e12) if tf else 0.0
+    if tf and t_flop >= t_mem:
+        ach = work["flops"] / t / 1e12
+        return dict(bound="tensor", achieved=round(ach, 2), peak=tf, unit="TFLOP/s",
+                    frac=round(ach / tf, 4), peak_source=f"{source} bf16 burst",
+                    hbm_frac=round(work["bytes"] / t / 1e9 / hbm, 4))
+    ach = work["bytes"] / t / 1e9
+    out = dict(bound="hbm", achieved=round(ach, 1), peak=hbm, unit="GB/s",
+               frac=round(ach / hbm, 4), peak_source=f"{source} copy bandwidth")
+    if tf and work["flops"]:
+        out["tensor_frac"] = round(work["flops"] / t / 1e12 / tf, 4)
+    return out
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.2)
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        rows = []
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smmax=float(f[2]), power=float(f[3]),
+                                 hw=f[5], hwt=f[6], swt=f[7], swpc=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] > 0.5 * max(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swpc", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(r["sm"] for r in loaded),
+                    sm_max_mhz=max(r["smmax"] for r in rows), samples=len(loaded),
+                    power_w_max=max(r["power"] for r in rows), reasons=sorted(reasons))
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return 1
+
+
+def time_oracle(shape, x, w_router, b_router, expert_fn, n_sample_experts, seed=0):
+    """Times the fp64 oracle on the whole batch for routing, dispatch and combine, and on
+    the full segments of `n_sample_experts` experts for the SwiGLU experts; the expert
+    time is extrapolated to every kept pair. Returns (seconds for the batch, detail)."""
+    import oracle
+    N, k, E = shape.N, shape.top_k, shape.E
+    t0 = time.perf_counter()
+    logits, idx, w = oracle.route(x, w_router, b_router, k)
+    t1 = time.perf_counter()
+    C = oracle.expert_capacity(shape.capacity_factor, N, k, E)
+    lay = oracle.dispatch_layout(idx, E, shape.ep_size, C)
+    send = oracle.permute(x, lay["perm"], k)
+    t2 = time.perf_counter()
+    rng = np.random.default_rng(seed)
+    busy = np.nonzero(lay["counts"])[0]
+    pick = rng.choice(busy, size=min(n_sample_experts, busy.size), replace=False)
+    rows = 0
+    t_ffn = 0.0
+    for e in pick:
+        wg, wu, wd = expert_fn(int(e))
+        a, b = int(lay["expert_offsets"][e]), int(lay["expert_offsets"][e + 1])
+        ts = time.perf_counter()
+        oracle.swiglu_expert(send[a:b], wg, wu, wd)
+        t_ffn += time.perf_counter() - ts
+        rows += b - a
+    y_send = np.zeros((send.shape[0], shape.H))
+    t3 = time.perf_counter()
+    oracle.combine_dispatch(y_send, lay["slot_pos"], w, N, k)
+    t4 = time.perf_counter()
+    kept = int(lay["expert_offsets"][-1])
+    ffn_total = t_ffn * kept / max(rows, 1)
+    total = (t1 - t0) + (t2 - t1) + ffn_total + (t4 - t3)
+    detail = dict(route_s=t1 - t0, dispatch_s=t2 - t1, ffn_sample_s=t_ffn,
+                  ffn_extrapolated_s=ffn_total, combine_s=t4 - t3, sample_rows=rows,
+                  kept_pairs=kept, sampled_experts=len(pick))
+    return total, detail
+
+
+def host_inputs_for_oracle(shape, inp):
+    f = lambda t: None if t is None else t.detach().to("cpu", torch.float64).numpy()
+    return f(inp["x"]), f(inp["w_router"]), f(inp["b_router"])
+
+
+def cpu_baseline_from_device(shape, inp, n_sample_experts=4):
+    x, wr, b = host_inputs_for_oracle(shape, inp)
+
+    def expert_fn(e):
+        return tuple(inp[k][e].detach().to("cpu", torch.float64).numpy()
+                     for k in ("w_gate", "w_up", "w_down"))
+
+    total, detail = time_oracle(shape, x, wr, b, expert_fn, n_sample_experts)
+    return dict(value=round(shape.N / total, 2), unit="tokens/s", cores=blas_threads(),
+                kind="oracle",
+                sample=(f"fp64 oracle: route, dispatch and combine on all {shape.N} tokens; "
+                        f"SwiGLU experts timed on the full segments of "
+                        f"{detail['sampled_experts']} of {shape.E} experts "
+                        f"({detail['sample_rows']} of {detail['kept_pairs']} kept pairs), "
+                        f"extrapolated linearly in kept pairs"),
+                seconds=round(total, 3), detail={k: (round(v, 4) if isinstance(v, float) else v)
+                                                 for k, v in detail.items()})
+
+
+def run_reference(args, shape):
+    """--impl reference: the fp64 CPU oracle as it stands, one bounded sample per step."""
+    inp = workloads.layer_inputs(shape, seed=0, variant="perf", device="cpu",
+                                 with_experts=False)
+    x, wr, b = host_inputs_for_oracle(shape, inp)
+    cache = {}
+
+    def expert_fn(e):
+        if e not in cache:
+            cache.clear()
+            cache[e] = tuple(workloads.expert_weight(shape, k, e, 0, "cpu").double().numpy()
+                             for k in ("w_gate", "w_up", "w_down"))
+        return cache[e]
+
+    for i in range(args.warmup):
+        time_oracle(shape, x, wr, b, expert_fn, 1, seed=i)
+    totals = []
+    details = None
+    for i in range(args.steps):
+        t, details = time_oracle(shape, x, wr, b, expert_fn, 1, seed=100 + i)
+        totals.append(t)
+    sec = float(np.mean(totals))
+    value = shape.N / sec
+    cores = blas_threads()
+    sample = (f"per step: fp64 oracle route, dispatch and combine on all {shape.N} tokens, "
+              f"SwiGLU of 1 of {shape.E} experts on its full segment, extrapolated "
+              f"linearly in kept pairs")
+    line = dict(metric=METRIC, value=round(value, 3), unit="tokens/s", n_gpus=args.gpus,
+                steps=args.steps, warmup=args.warmup, ms_per_step=round(sec * 1e3, 3),
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic (seeded; same distributions as the GPU arm)",
+                config=workload_config(shape), impl="reference",
+                cpu_baseline=dict(value=round(value, 3), unit="tokens/s", cores=cores,
+                                  kind="oracle", sample=sample),
+                e2e=dict(value=round(value, 3), unit="tokens/s", h2d_bytes_per_step=0,
+                         d2h_bytes_per_step=0),
+                detail={k: (round(v, 4) if isinstance(v, float) else v)
+                        for k, v in details.items()})
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(shape):
+    return dict(workload=shape.name, tokens=shape.N, hidden=shape.H, intermediate=shape.I,
+                experts=shape.E, top_k=shape.top_k, ep_size=shape.ep_size,
+                capacity_factor=shape.capacity_factor, router_zipf_s=shape.zipf_s,
+                mode="dispatch", values="perf (continuous)",
+                l2="inputs larger than L2 (expert weights >> 126 MB); no flush")
+
+
+# ------------------------------------------------------------------ GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=workloads.GPTOSS.name, choices=sorted(workloads.BY_NAME))
+    ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--mode", default="dispatch", choices=["dispatch", "mask_sum"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    shape = workloads.BY_NAME[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, shape)
+        return
+
+    import expert_token_dispatch_gemm_b300 as moe
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    dev = torch.device("cuda", local)
+    inp = workloads.layer_inputs(shape, seed=rank, variant="perf", device=dev)
+    cfg = moe.config(shape.N, shape.H, shape.I, shape.E, shape.top_k, shape.ep_size,
+                     shape.capacity_factor, args.mode, shape.dtype,
+                     has_bias=inp["b_router"] is not None)
+    packed = moe.moe_pack_weights(cfg, inp["w_gate"], inp["w_up"])
+    ws = moe.alloc_workspace(cfg, dev)
+    out = torch.empty(shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
+    x, wr, b, wd = inp["x"], inp["w_router"], inp["b_router"], inp["w_down"]
+    stream = torch.cuda.current_stream()
+
+    # one run with diagnostics for the kept counts (algorithmic work of each stage)
+    counts_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
+    moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws, dict(counts=counts_t))
+    torch.cuda.synchronize()
+    counts = counts_t.cpu().numpy()
+    work = stage_work(shape, counts)
+
+    nst = moe.binding.MOE_NUM_STAGES
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+           for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)     # creates the handles before the library re-records them
+    for _ in range(args.warmup):
+        moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws, None, evs[0])
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws, None, evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = start.elapsed_time(end)
+    stage_ms = {}
+    for j, name in enumerate(moe.binding.STAGE_NAMES):
+        stage_ms[name] = float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1])
+                                         for i in range(args.steps)]))
+    flags = moe.moe_read_device_status(cfg, ws)
+    if flags:
+        raise RuntimeError(f"device status flags {flags} after the timed steps")
+
+    ms_step = ms_total / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * shape.N / (ms_step / 1e3)
+
+    # end to end through the C ABI: pinned host input -> device, forward, output -> host
+    e2e = None
+    if not args.no_e2e:
+        x_host = x.cpu().pin_memory()
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        x_dev = torch.empty_like(x)
+        for _ in range(3):
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.moe_layer_forward(cfg, x_dev, wr, b, packed, wd, out, ws)
+            out_host.copy_(out, non_blocking=True)
+        barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.moe_layer_forward(cfg, x_dev, wr, b, packed, wd, out, ws)
+            out_host.copy_(out, non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = s0.elapsed_time(s1) / args.steps
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        nbytes = x.numel() * x.element_size()
+        e2e = dict(value=round(world * shape.N / (e2e_ms / 1e3), 1), unit="tokens/s",
+                   ms_per_step=round(e2e_ms, 4), h2d_bytes_per_step=nbytes,
+                   d2h_bytes_per_step=out.numel() * out.element_size())
+
+    peaks, source = load_peaks()
+    dom = max(("gate_up", "down", "route", "permute", "combine"), key=lambda n: stage_ms[n])
+    roof = roofline_entry(work[dom], stage_ms[dom], peaks, source, shape.dtype)
+    roof = dict(kernel=dom, **roof, traffic=None)
+    per_stage = {n: dict(ms=round(stage_ms[n], 4),
+                         **{k: v for k, v in roofline_entry(work[n], max(stage_ms[n], 1e-6),
+                                                            peaks, source, shape.dtype).items()
+                            if k in ("bound", "achieved", "unit", "frac")})
+                 for n in moe.binding.STAGE_NAMES}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_from_device(shape, inp)
+
+    launches_per_step = 7 if args.mode == "dispatch" else 4 + 2 * shape.ep_size + 2
+    if rank == 0:
+        line = dict(metric=METRIC, value=round(value, 1), unit="tokens/s", n_gpus=world,
+                    steps=args.steps, warmup=args.warmup, ms_per_step=round(ms_step, 4),
+                    higher_is_better=True, scaling="weak", vs_baseline=None, dtype=shape.dtype,
+                    data="synthetic (seeded; x~N(0,1), router~U(+-1/sqrt(H)), experts~N(0,0.02))",
+                    config=dict(workload_config(shape), mode=args.mode,
+                                parallelism=f"replicas x{world} (one layer per GPU)"),
+                    roofline=roof, stages=per_stage, cpu_baseline=cpu, e2e=e2e,
+                    gpu_launches=launches_per_step * args.steps, clocks=clk.summary(),
+                    kept_pairs=int(counts.sum()), impl="b300")
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

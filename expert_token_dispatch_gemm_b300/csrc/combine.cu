@@ -1,0 +1,185 @@
+// Step 4 -- combine, both forward rules, and the one-time gate/up weight packing.
+//
+// Dispatch rule (Ultralytics glossary "Expert Parallelism", step 4; Hugging Face
+// "Expert parallelism" docs, "Token dispatch"): the expert outputs come back to their
+// token already weighted (the down-projection epilogue wrote w * y into the pair's slot)
+// and are summed in slot order.
+// Mask-and-sum rule (Hugging Face docs, "DistributedConfig": "ep_router" masks the
+// experts of other ranks, "moe_tp_experts" computes the local ones, an all-reduce sums
+// the rank outputs): every partition forms its partial output from the slots whose
+// expert it owns; the partials are then summed in partition order.
+// All three kernels are one warp per token with 16-byte vector accesses: HBM-bound.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+combine_kernel(const T *__restrict__ slots, const int32_t *__restrict__ slot_pos, int N, int k,
+               int H, T *__restrict__ out) {
+    using V = Vec16<T>;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= N) return;
+    const unsigned kept = __ballot_sync(0xffffffffu, lane < k && slot_pos[(size_t)t * k + lane] >= 0);
+    const int nvec = H / V::N;
+    const uint4 *src = reinterpret_cast<const uint4 *>(slots + (size_t)t * k * H);
+    uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)t * H);
+    for (int v = lane; v < nvec; v += 32) {
+        float acc[V::N];
+#pragma unroll
+        for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            if (!((kept >> j) & 1u)) continue;
+            float f[V::N];
+            V::to_float(__ldg(src + (size_t)j * nvec + v), f);
+#pragma unroll
+            for (int i = 0; i < V::N; ++i) acc[i] += f[i];
+        }
+        dst[v] = V::from_float(acc);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+mask_partials_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
+                     const int32_t *__restrict__ slot_pos, int N, int k, int H, int E, int P,
+                     float *__restrict__ partials) {
+    using V = Vec16<T>;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= N) return;
+    const int per_part = E / P;
+    int owner = -1;
+    if (lane < k && slot_pos[(size_t)t * k + lane] >= 0) {
+        const int e = idx[(size_t)t * k + lane];
+        owner = e / per_part;
+    }
+    const int nvec = H / V::N;
+    const uint4 *src = reinterpret_cast<const uint4 *>(slots + (size_t)t * k * H);
+    for (int p = 0; p < P; ++p) {
+        const unsigned mine = __ballot_sync(0xffffffffu, owner == p);
+        float4 *dst = reinterpret_cast<float4 *>(partials + ((size_t)p * N + t) * H);
+        for (int v = lane; v < nvec; v += 32) {
+            float acc[V::N];
+#pragma unroll
+            for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
+            for (int j = 0; j < k; ++j) {
+                if (!((mine >> j) & 1u)) continue;
+                float f[V::N];
+                V::to_float(__ldg(src + (size_t)j * nvec + v), f);
+#pragma unroll
+                for (int i = 0; i < V::N; ++i) acc[i] += f[i];
+            }
+#pragma unroll
+            for (int i = 0; i < V::N; i += 4)
+                dst[(size_t)v * (V::N / 4) + i / 4] = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+partition_sum_kernel(const float *__restrict__ partials, int N, int H, int P, T *__restrict__ out) {
+    using V = Vec16<T>;
+    const int64_t nvec = (int64_t)N * H / V::N;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+        float acc[V::N];
+#pragma unroll
+        for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
+        for (int p = 0; p < P; ++p) {
+            const float4 *src = reinterpret_cast<const float4 *>(partials + (size_t)p * N * H) + v * (V::N / 4);
+#pragma unroll
+            for (int i = 0; i < V::N; i += 4) {
+                const float4 f = __ldg(src + i / 4);
+                acc[i] += f.x;
+                acc[i + 1] += f.y;
+                acc[i + 2] += f.z;
+                acc[i + 3] += f.w;
+            }
+        }
+        reinterpret_cast<uint4 *>(out)[v] = V::from_float(acc);
+    }
+}
+
+// packed[e][r][:] for r in [0, 2*Ipad): block b = r / 256 holds gate rows 128b..128b+127
+// then up rows 128b..128b+127; rows at or beyond I are zero.
+template <typename T>
+__global__ void pack_gate_up_kernel(const T *__restrict__ wg, const T *__restrict__ wu, int E,
+                                    int I, int Ipad, int H, T *__restrict__ packed) {
+    using V = Vec16<T>;
+    const int nvec = H / V::N;
+    const int64_t total = (int64_t)E * 2 * Ipad * nvec;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int v = (int)(i % nvec);
+        const int64_t row = i / nvec;            // e * 2 * Ipad + r
+        const int r = (int)(row % (2 * Ipad));
+        const int e = (int)(row / (2 * Ipad));
+        const int blk = r / (2 * kGateUpBlock), within = r % (2 * kGateUpBlock);
+        const int src_row = blk * kGateUpBlock + within % kGateUpBlock;
+        const T *src = within < kGateUpBlock ? wg : wu;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (src_row < I)
+            val = reinterpret_cast<const uint4 *>(src + ((size_t)e * I + src_row) * H)[v];
+        reinterpret_cast<uint4 *>(packed)[i] = val;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const LayerDims &d, const void *out_slots, const int32_t *slot_pos,
+                           void *out, cudaStream_t s) {
+    const int grid = ceil_div(d.N, 8);
+    if (d.dtype == MOE_DTYPE_BF16)
+        combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            (const __nv_bfloat16 *)out_slots, slot_pos, d.N, d.k, d.H, (__nv_bfloat16 *)out);
+    else
+        combine_kernel<float><<<grid, 256, 0, s>>>((const float *)out_slots, slot_pos, d.N, d.k,
+                                                   d.H, (float *)out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mask_partials(const LayerDims &d, const void *out_slots,
+                                 const int32_t *topk_idx, const int32_t *slot_pos,
+                                 float *partials, cudaStream_t s) {
+    const int grid = ceil_div(d.N, 8);
+    if (d.dtype == MOE_DTYPE_BF16)
+        mask_partials_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            (const __nv_bfloat16 *)out_slots, topk_idx, slot_pos, d.N, d.k, d.H, d.E, d.P, partials);
+    else
+        mask_partials_kernel<float><<<grid, 256, 0, s>>>((const float *)out_slots, topk_idx,
+                                                         slot_pos, d.N, d.k, d.H, d.E, d.P,
+                                                         partials);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_partition_sum(const LayerDims &d, const float *partials, void *out,
+                                 cudaStream_t s) {
+    const int64_t nvec = (int64_t)d.N * d.H / (d.dtype == MOE_DTYPE_BF16 ? 8 : 4);
+    const int grid = (int)std::min<int64_t>(ceil_div64(nvec, 256), 148 * 16);
+    if (d.dtype == MOE_DTYPE_BF16)
+        partition_sum_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(partials, d.N, d.H, d.P,
+                                                                 (__nv_bfloat16 *)out);
+    else
+        partition_sum_kernel<float><<<grid, 256, 0, s>>>(partials, d.N, d.H, d.P, (float *)out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_gate_up(const LayerDims &d, const void *w_gate, const void *w_up,
+                                void *packed, cudaStream_t s) {
+    const int64_t nvec = (int64_t)d.E * 2 * d.Ipad * d.H / (d.dtype == MOE_DTYPE_BF16 ? 8 : 4);
+    const int grid = (int)std::min<int64_t>(ceil_div64(nvec, 256), 148 * 32);
+    if (d.dtype == MOE_DTYPE_BF16)
+        pack_gate_up_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            (const __nv_bfloat16 *)w_gate, (const __nv_bfloat16 *)w_up, d.E, d.I, d.Ipad, d.H,
+            (__nv_bfloat16 *)packed);
+    else
+        pack_gate_up_kernel<float><<<grid, 256, 0, s>>>((const float *)w_gate, (const float *)w_up,
+                                                        d.E, d.I, d.Ipad, d.H, (float *)packed);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,177 @@
+// Shared device helpers and internal launcher declarations of libmoe (sm_103a only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Tokens per histogram segment. The routing kernel and the standalone histogram kernel
+// both count expert ids per segment of this many tokens; the scan turns the per-segment
+// counts into the stable rank base of every segment.
+constexpr int kSegTokens = 64;
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 32;
+// Output rows per interleaved gate/up block of the packed weights.
+constexpr int kGateUpBlock = 128;
+
+// Rows per M tile of the grouped GEMMs (tensor-core path and fp32 path).
+constexpr int kTcBlockM = 128;
+constexpr int kSimtBlockM = 64;
+
+__host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// 16-byte vector of T: 8 bf16 or 4 fp32.
+template <typename T> struct Vec16;
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void to_float(const uint4 &v, float *f) {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 p = __bfloat1622float2(h[i]);
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+        }
+    }
+    __device__ __forceinline__ static uint4 from_float(const float *f) {
+        uint4 v;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        return v;
+    }
+};
+template <> struct Vec16<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void to_float(const uint4 &v, float *f) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static uint4 from_float(const float *f) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+};
+
+// ----------------------------------------------------------------------------------
+// Internal launchers (host side). Each returns the cudaError_t of its launch(es).
+// ----------------------------------------------------------------------------------
+struct LayerDims {
+    int N, H, I, Ipad, E, k, P;
+    int capacity;      // INT32_MAX when unlimited
+    int dtype;         // MOE_DTYPE_*
+};
+
+cudaError_t launch_route(const LayerDims &d, const void *x, const void *w_router,
+                         const float *b_router, int32_t *topk_idx, float *topk_w,
+                         int32_t *seg_hist /* [nseg, E] or nullptr */, cudaStream_t s);
+
+cudaError_t launch_histogram(const LayerDims &d, const int32_t *topk_idx, int32_t *seg_hist,
+                             int32_t *status, cudaStream_t s);
+cudaError_t launch_scan(const LayerDims &d, const int32_t *seg_hist, int32_t *seg_base,
+                        int32_t *routed_counts, int32_t *counts, int32_t *expert_offsets,
+                        int32_t *part_offsets, cudaStream_t s);
+cudaError_t launch_assign(const LayerDims &d, const int32_t *topk_idx, const int32_t *seg_base,
+                          const int32_t *expert_offsets, int32_t *slot_pos, int32_t *perm,
+                          int32_t *status, cudaStream_t s);
+cudaError_t launch_permute(const LayerDims &d, const void *x, const int32_t *slot_pos,
+                           void *send, cudaStream_t s);
+
+cudaError_t launch_pack_gate_up(const LayerDims &d, const void *w_gate, const void *w_up,
+                                void *packed, cudaStream_t s);
+
+// Tensor-core (bf16) grouped GEMMs. h has row stride Ipad.
+cudaError_t launch_tc_gate_up(const LayerDims &d, const void *send, const int32_t *expert_offsets,
+                              int e_begin, int e_end, const void *packed, void *h,
+                              int32_t *status, int num_sms, cudaStream_t s);
+cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *expert_offsets,
+                           int e_begin, int e_end, const void *w_down, const int32_t *perm,
+                           const float *topk_w, void *out_slots, int32_t *status, int num_sms,
+                           cudaStream_t s);
+
+// fp32 FFMA grouped FFN.
+cudaError_t launch_simt_gate_up(const LayerDims &d, const float *send,
+                                const int32_t *expert_offsets, int e_begin, int e_end,
+                                const float *packed, float *h, cudaStream_t s);
+cudaError_t launch_simt_down(const LayerDims &d, const float *h, const int32_t *expert_offsets,
+                             int e_begin, int e_end, const float *w_down, const int32_t *perm,
+                             const float *topk_w, float *out_slots, cudaStream_t s);
+
+cudaError_t launch_combine(const LayerDims &d, const void *out_slots, const int32_t *slot_pos,
+                           void *out, cudaStream_t s);
+cudaError_t launch_mask_partials(const LayerDims &d, const void *out_slots,
+                                 const int32_t *topk_idx, const int32_t *slot_pos,
+                                 float *partials, cudaStream_t s);
+cudaError_t launch_partition_sum(const LayerDims &d, const float *partials, void *out,
+                                 cudaStream_t s);
+
+}  // namespace moe
+
+namespace moe {
+
+// Grouped-GEMM tile scheduling over variable-length expert segments.
+// mtp[i] (i in [0, ne]) = number of BM-row tiles of experts e_begin .. e_begin+i-1 and
+// eo[i] = expert_offsets[e_begin + i]; one warp builds both in shared memory.
+__device__ inline void build_tile_tables(const int32_t *__restrict__ expert_offsets, int e_begin,
+                                         int ne, int bm, int *eo, int *mtp) {
+    const int lane = threadIdx.x & 31;
+    const int per = (ne + 31) / 32;
+    const int i0 = lane * per;
+    int local = 0;
+    for (int i = i0; i < i0 + per && i < ne; ++i) {
+        const int a = expert_offsets[e_begin + i], b = expert_offsets[e_begin + i + 1];
+        eo[i] = a;
+        local += (b - a + bm - 1) / bm;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int i = i0; i < i0 + per && i < ne; ++i) {
+        mtp[i] = run;
+        run += (expert_offsets[e_begin + i + 1] - expert_offsets[e_begin + i] + bm - 1) / bm;
+    }
+    if (lane == 31) {
+        mtp[ne] = incl;
+        eo[ne] = expert_offsets[e_begin + ne];
+    }
+}
+
+// Tile t -> (expert index i in [0, ne), m tile, n tile). Tiles of one expert are ordered
+// n-major with m fastest, so CTAs working at the same time share weight tiles in L2.
+__device__ inline void decode_tile(int t, const int *mtp, int ne, int n_tiles, int &i, int &m,
+                                   int &n) {
+    int lo = 0, hi = ne - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (mtp[mid] * n_tiles <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    i = lo;
+    const int mt = mtp[lo + 1] - mtp[lo];
+    const int local = t - mtp[lo] * n_tiles;
+    n = local / mt;
+    m = local - n * mt;
+}
+
+}  // namespace moe

@@ -1,0 +1,213 @@
+// Step 2 -- dispatch: the send layout grouped by expert, hence by partition (experts are
+// split contiguously: partition = expert / (E / ep_size)), and the copy of every kept
+// pair's hidden state into it. (Hugging Face "Expert parallelism" docs, section "Token
+// dispatch"; Ultralytics glossary "Expert Parallelism", step 2 and section "Load
+// balancing and capacity".)
+//
+// Pair p = t*k + j. Its rank within expert e is the number of earlier pairs (lower token
+// index) routed to e; with a capacity C the pair is kept iff rank < C, and its send row
+// is expert_offsets[e] + rank. The rank is computed without atomics on values:
+//   1. per segment of kSegTokens tokens, a histogram of expert ids (fused into routing
+//      for the whole layer, or histogram_kernel here);
+//   2. one CTA scans the [segments x E] histogram: exclusive per-expert segment bases,
+//      routed counts, kept counts, expert and partition offsets;
+//   3. one warp per segment walks its pairs in order 32 at a time; lanes holding the
+//      same expert find each other with __match_any_sync, so a pair's rank is its
+//      segment base plus the number of earlier pairs of that expert.
+// Every step is deterministic, so counts, offsets, perm and slot_pos are bit-exact.
+#include <limits.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kScanThreads = 1024;
+
+__global__ void histogram_kernel(const int32_t *__restrict__ idx, int N, int k, int E,
+                                 int32_t *__restrict__ seg_hist, int32_t *status) {
+    __shared__ int hs[kMaxExperts];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hs[e] = 0;
+    __syncthreads();
+    const int64_t p0 = (int64_t)blockIdx.x * kSegTokens * k;
+    const int64_t p1 = min(p0 + (int64_t)kSegTokens * k, (int64_t)N * k);
+    for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+        const int e = idx[p];
+        if (e >= 0 && e < E)
+            atomicAdd(&hs[e], 1);
+        else
+            atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) seg_hist[(size_t)blockIdx.x * E + e] = hs[e];
+}
+
+// Single CTA. Thread (e, c) = (tid % E, tid / E) owns a contiguous chunk of segments
+// for expert e; G = 1024 / E chunks per expert.
+__global__ void __launch_bounds__(kScanThreads)
+scan_kernel(const int32_t *__restrict__ seg_hist, int nseg, int E, int P, int capacity,
+            int32_t *__restrict__ seg_base, int32_t *__restrict__ routed_counts,
+            int32_t *__restrict__ counts, int32_t *__restrict__ expert_offsets,
+            int32_t *__restrict__ part_offsets) {
+    __shared__ int part[kScanThreads];        // [G][E] chunk sums, then exclusive bases
+    __shared__ int kept_s[kMaxExperts + 1];
+    const int tid = threadIdx.x;
+    const int G = kScanThreads / E;
+    const int e = tid % E, c = tid / E;
+    const bool active = c < G;
+    const int per = (nseg + G - 1) / G;
+    const int b0 = min(c * per, nseg), b1 = min(b0 + per, nseg);
+    if (active) {
+        int s = 0;
+        for (int b = b0; b < b1; ++b) s += seg_hist[(size_t)b * E + e];
+        part[c * E + e] = s;
+    }
+    __syncthreads();
+    if (tid < E) {   // exclusive scan over chunks of expert tid
+        int run = 0;
+        for (int cc = 0; cc < G; ++cc) {
+            const int v = part[cc * E + tid];
+            part[cc * E + tid] = run;
+            run += v;
+        }
+        routed_counts[tid] = run;
+        const int kept = run < capacity ? run : capacity;
+        counts[tid] = kept;
+        kept_s[tid] = kept;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int ee = 0; ee < E; ++ee) {
+            const int v = kept_s[ee];
+            kept_s[ee] = run;
+            expert_offsets[ee] = run;
+            run += v;
+        }
+        kept_s[E] = run;
+        expert_offsets[E] = run;
+    }
+    __syncthreads();
+    if (tid <= P) part_offsets[tid] = kept_s[tid * (E / P)];
+    if (active) {
+        int run = part[c * E + e];
+        for (int b = b0; b < b1; ++b) {
+            seg_base[(size_t)b * E + e] = run;
+            run += seg_hist[(size_t)b * E + e];
+        }
+    }
+}
+
+// One warp per segment; 8 warps per CTA.
+__global__ void __launch_bounds__(256)
+assign_kernel(const int32_t *__restrict__ idx, int N, int k, int E, int capacity,
+              const int32_t *__restrict__ seg_base, const int32_t *__restrict__ expert_offsets,
+              int32_t *__restrict__ slot_pos, int32_t *__restrict__ perm, int32_t *status) {
+    __shared__ int base_s[8][kMaxExperts];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int seg = blockIdx.x * 8 + warp;
+    const int nseg = (N + kSegTokens - 1) / kSegTokens;
+    if (seg >= nseg) return;   // warp-uniform; no block-wide barrier follows
+    int *base = base_s[warp];
+    for (int e = lane; e < E; e += 32) base[e] = seg_base[(size_t)seg * E + e];
+    __syncwarp();
+    const int64_t p0 = (int64_t)seg * kSegTokens * k;
+    const int64_t p1 = min(p0 + (int64_t)kSegTokens * k, (int64_t)N * k);
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int64_t pc = p0; pc < p1; pc += 32) {
+        const int64_t p = pc + lane;
+        const bool live = p < p1;
+        int e = live ? idx[p] : -1;
+        const bool valid = live && e >= 0 && e < E;
+        if (live && !valid) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+        if (!valid) e = -1 - lane;   // unique key: never matches another lane
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        int rank = 0;
+        if (valid) rank = base[e] + __popc(same & lt_mask);
+        __syncwarp();
+        // the lowest lane of each group advances that expert's running base
+        if (valid && (same & lt_mask) == 0) base[e] += __popc(same);
+        __syncwarp();
+        if (live) {
+            int slot = -1;
+            if (valid && rank < capacity) {
+                slot = expert_offsets[e] + rank;
+                perm[slot] = (int32_t)p;
+            }
+            slot_pos[p] = slot;
+        }
+    }
+}
+
+// One warp per token: read the token's row once (16-byte vectors), write it to every
+// kept slot. Stores of one instruction cover 512 contiguous bytes of one send row.
+template <typename T>
+__global__ void __launch_bounds__(256)
+permute_kernel(const T *__restrict__ x, int N, int H, int k, const int32_t *__restrict__ slot_pos,
+               T *__restrict__ send) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= N) return;
+    const int my_slot = (lane < k) ? slot_pos[(size_t)t * k + lane] : -1;
+    const int nvec = H / Vec16<T>::N;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+    for (int v0 = 0; v0 < nvec; v0 += 32 * 4) {
+        uint4 r[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int v = v0 + u * 32 + lane;
+            if (v < nvec) r[u] = __ldg(src + v);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+            if (slot < 0) continue;
+            uint4 *dst = reinterpret_cast<uint4 *>(send + (size_t)slot * H);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < nvec) dst[v] = r[u];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_histogram(const LayerDims &d, const int32_t *topk_idx, int32_t *seg_hist,
+                             int32_t *status, cudaStream_t s) {
+    const int nseg = ceil_div(d.N, kSegTokens);
+    histogram_kernel<<<nseg, 256, 0, s>>>(topk_idx, d.N, d.k, d.E, seg_hist, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const LayerDims &d, const int32_t *seg_hist, int32_t *seg_base,
+                        int32_t *routed_counts, int32_t *counts, int32_t *expert_offsets,
+                        int32_t *part_offsets, cudaStream_t s) {
+    const int nseg = ceil_div(d.N, kSegTokens);
+    scan_kernel<<<1, kScanThreads, 0, s>>>(seg_hist, nseg, d.E, d.P, d.capacity, seg_base,
+                                           routed_counts, counts, expert_offsets, part_offsets);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_assign(const LayerDims &d, const int32_t *topk_idx, const int32_t *seg_base,
+                          const int32_t *expert_offsets, int32_t *slot_pos, int32_t *perm,
+                          int32_t *status, cudaStream_t s) {
+    const int nseg = ceil_div(d.N, kSegTokens);
+    assign_kernel<<<ceil_div(nseg, 8), 256, 0, s>>>(topk_idx, d.N, d.k, d.E, d.capacity, seg_base,
+                                                    expert_offsets, slot_pos, perm, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const LayerDims &d, const void *x, const int32_t *slot_pos,
+                           void *send, cudaStream_t s) {
+    const int grid = ceil_div(d.N, 8);
+    if (d.dtype == MOE_DTYPE_BF16)
+        permute_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            (const __nv_bfloat16 *)x, d.N, d.H, d.k, slot_pos, (__nv_bfloat16 *)send);
+    else
+        permute_kernel<float><<<grid, 256, 0, s>>>((const float *)x, d.N, d.H, d.k, slot_pos,
+                                                   (float *)send);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

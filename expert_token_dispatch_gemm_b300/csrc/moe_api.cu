@@ -1,0 +1,486 @@
+// The C ABI declared in include/moe.h: argument validation (complete before anything is
+// enqueued), workspace layout, and the launch sequence of each step and of the layer.
+#include <limits.h>
+#include <stdarg.h>
+#include <math.h>
+#include <stdio.h>
+
+#include <algorithm>
+#include <string>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status_t fail(moe_status_t s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+moe_status_t fail(moe_status_t s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+moe_status_t cuda_fail(cudaError_t e, const char *what) {
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MOE_CUDA(call, what)                                 \
+    do {                                                     \
+        cudaError_t e_ = (call);                             \
+        if (e_ != cudaSuccess) return cuda_fail(e_, (what)); \
+    } while (0)
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates the sizes and derives the kernel-side dimensions.
+moe_status_t check_config(const moe_config *cfg, LayerDims *d) {
+    if (cfg == nullptr) return fail(MOE_ERR_INVALID_ARG, "cfg is NULL");
+    const int64_t N = cfg->num_tokens, H = cfg->hidden, I = cfg->intermediate;
+    if (N < 0) return fail(MOE_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)N);
+    if (H < 8 || H % 8) return fail(MOE_ERR_INVALID_ARG, "hidden must be a positive multiple of 8 (got %lld)", (long long)H);
+    if (I < 8 || I % 8) return fail(MOE_ERR_INVALID_ARG, "intermediate must be a positive multiple of 8 (got %lld)", (long long)I);
+    if (cfg->num_experts < 1) return fail(MOE_ERR_INVALID_ARG, "num_experts must be >= 1");
+    if (cfg->num_experts > kMaxExperts)
+        return fail(MOE_ERR_UNSUPPORTED, "num_experts %d exceeds %d", cfg->num_experts, kMaxExperts);
+    if (cfg->top_k < 1 || cfg->top_k > cfg->num_experts)
+        return fail(MOE_ERR_INVALID_ARG, "top_k must be in [1, num_experts] (got %d)", cfg->top_k);
+    if (cfg->top_k > kMaxTopK)
+        return fail(MOE_ERR_UNSUPPORTED, "top_k %d exceeds %d", cfg->top_k, kMaxTopK);
+    if (cfg->ep_size < 1 || cfg->num_experts % cfg->ep_size)
+        return fail(MOE_ERR_INVALID_ARG, "ep_size (%d) must divide num_experts (%d)", cfg->ep_size,
+                    cfg->num_experts);
+    if (isnan(cfg->capacity_factor)) return fail(MOE_ERR_INVALID_ARG, "capacity_factor is NaN");
+    if (cfg->mode != MOE_MODE_DISPATCH && cfg->mode != MOE_MODE_MASK_SUM)
+        return fail(MOE_ERR_INVALID_ARG, "unknown mode %d", cfg->mode);
+    if (cfg->dtype != MOE_DTYPE_BF16 && cfg->dtype != MOE_DTYPE_FP32)
+        return fail(MOE_ERR_INVALID_ARG, "unknown dtype %d", cfg->dtype);
+    if (cfg->has_bias != 0 && cfg->has_bias != 1) return fail(MOE_ERR_INVALID_ARG, "has_bias must be 0 or 1");
+    const int64_t pairs = N * cfg->top_k;
+    const int64_t Ipad = (I + kGateUpBlock - 1) / kGateUpBlock * kGateUpBlock;
+    if (pairs > INT_MAX / 2 || H > (1 << 20) || Ipad > (1 << 20) ||
+        pairs * std::max(H, Ipad) > ((int64_t)1 << 40))
+        return fail(MOE_ERR_UNSUPPORTED, "sizes too large for 32-bit row indices");
+    d->N = (int)N;
+    d->H = (int)H;
+    d->I = (int)I;
+    d->Ipad = (int)Ipad;
+    d->E = cfg->num_experts;
+    d->k = cfg->top_k;
+    d->P = cfg->ep_size;
+    d->dtype = cfg->dtype;
+    d->capacity = INT_MAX;
+    if (cfg->capacity_factor > 0.f) {
+        // cf * N * k is exact in double (24-bit cf times an integer below 2^29); if the
+        // exact quotient by E is an integer the division returns it exactly, otherwise it
+        // lies at least 1/E from the next integer, far beyond the rounding error, so
+        // ceil() of the double equals the exact ceiling.
+        const double c = ceil((double)cfg->capacity_factor * (double)N * cfg->top_k / cfg->num_experts);
+        d->capacity = c >= (double)N ? (N > 0 ? (int)N : 0) : (int)c;
+        if (d->capacity < 1 && N > 0) d->capacity = 1;
+    }
+    return MOE_OK;
+}
+
+size_t esize(const LayerDims &d) { return d.dtype == MOE_DTYPE_BF16 ? 2 : 4; }
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace layout, every region 256-byte aligned.
+struct Workspace {
+    int32_t *status;       // [8]
+    int32_t *seg_hist;     // [nseg, E]
+    int32_t *seg_base;     // [nseg, E]
+    int32_t *topk_idx;     // [N*k]
+    float *topk_w;         // [N*k]
+    int32_t *routed;       // [E]
+    int32_t *counts;       // [E]
+    int32_t *eoff;         // [E+1]
+    int32_t *poff;         // [P+1]
+    int32_t *perm;         // [N*k]
+    int32_t *slot_pos;     // [N*k]
+    void *send;            // [N*k, H]
+    void *h;               // [N*k, Ipad]
+    void *slots;           // [N*k, H]
+    float *partials;       // [P, N, H] fp32 (mask-and-sum mode only)
+    size_t bytes;
+};
+
+Workspace carve(const LayerDims &d, int mode, void *base) {
+    Workspace w = {};
+    uint8_t *p = static_cast<uint8_t *>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        void *r = p ? p + off : nullptr;
+        off += align256(bytes);
+        return r;
+    };
+    const size_t nseg = (size_t)ceil_div(d.N, kSegTokens);
+    const size_t pairs = (size_t)d.N * d.k;
+    w.status = (int32_t *)take(8 * sizeof(int32_t));
+    w.seg_hist = (int32_t *)take(nseg * d.E * sizeof(int32_t));
+    w.seg_base = (int32_t *)take(nseg * d.E * sizeof(int32_t));
+    w.topk_idx = (int32_t *)take(pairs * sizeof(int32_t));
+    w.topk_w = (float *)take(pairs * sizeof(float));
+    w.routed = (int32_t *)take(d.E * sizeof(int32_t));
+    w.counts = (int32_t *)take(d.E * sizeof(int32_t));
+    w.eoff = (int32_t *)take((d.E + 1) * sizeof(int32_t));
+    w.poff = (int32_t *)take((d.P + 1) * sizeof(int32_t));
+    w.perm = (int32_t *)take(pairs * sizeof(int32_t));
+    w.slot_pos = (int32_t *)take(pairs * sizeof(int32_t));
+    w.send = take(pairs * d.H * esize(d));
+    w.h = take(pairs * d.Ipad * esize(d));
+    w.slots = take(pairs * d.H * esize(d));
+    w.partials = (float *)(mode == MOE_MODE_MASK_SUM ? take((size_t)d.P * d.N * d.H * sizeof(float))
+                                                      : nullptr);
+    w.bytes = off;
+    return w;
+}
+
+moe_status_t check_workspace(const LayerDims &d, int mode, void *ws, size_t ws_bytes,
+                             Workspace *out) {
+    const Workspace need = carve(d, mode, nullptr);
+    if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return fail(MOE_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < need.bytes)
+        return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", ws_bytes, need.bytes);
+    *out = carve(d, mode, ws);
+    return MOE_OK;
+}
+
+moe_status_t need_ptr(const void *p, const char *name, bool vec) {
+    if (p == nullptr) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
+    if (vec && !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s must be 16-byte aligned", name);
+    return MOE_OK;
+}
+#define NEED(p, vec)                                    \
+    do {                                                \
+        moe_status_t s_ = need_ptr((p), #p, (vec));     \
+        if (s_ != MOE_OK) return s_;                    \
+    } while (0)
+
+int num_sms() {
+    int dev = 0, n = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
+
+// --------------------------------------------------------------- step bodies
+moe_status_t run_route(const LayerDims &d, const void *x, const void *wr, const float *b,
+                       int32_t *idx, float *w, int32_t *hist, cudaStream_t s) {
+    MOE_CUDA(launch_route(d, x, wr, b, idx, w, hist, s), "route kernel");
+    return MOE_OK;
+}
+
+moe_status_t run_dispatch_from_hist(const LayerDims &d, const int32_t *idx, const void *x,
+                                    const Workspace &w, int32_t *routed, int32_t *counts,
+                                    int32_t *eoff, int32_t *poff, int32_t *perm, int32_t *slot_pos,
+                                    void *send, cudaStream_t s) {
+    MOE_CUDA(launch_scan(d, w.seg_hist, w.seg_base, routed, counts, eoff, poff, s), "scan kernel");
+    MOE_CUDA(launch_assign(d, idx, w.seg_base, eoff, slot_pos, perm, w.status, s), "assign kernel");
+    MOE_CUDA(launch_permute(d, x, slot_pos, send, s), "permute kernel");
+    return MOE_OK;
+}
+
+moe_status_t run_gate_up(const LayerDims &d, const void *send, const int32_t *eoff, int e0, int e1,
+                         const void *packed, const Workspace &w, cudaStream_t s) {
+    if (d.dtype == MOE_DTYPE_BF16)
+        MOE_CUDA(launch_tc_gate_up(d, send, eoff, e0, e1, packed, w.h, w.status, num_sms(), s),
+                 "tensor-core gate/up kernel");
+    else
+        MOE_CUDA(launch_simt_gate_up(d, (const float *)send, eoff, e0, e1, (const float *)packed,
+                                     (float *)w.h, s),
+                 "fp32 gate/up kernel");
+    return MOE_OK;
+}
+
+moe_status_t run_down(const LayerDims &d, const int32_t *eoff, int e0, int e1, const void *wd,
+                      const int32_t *perm, const float *tw, void *slots, const Workspace &w,
+                      cudaStream_t s) {
+    if (d.dtype == MOE_DTYPE_BF16)
+        MOE_CUDA(launch_tc_down(d, w.h, eoff, e0, e1, wd, perm, tw, slots, w.status, num_sms(), s),
+                 "tensor-core down kernel");
+    else
+        MOE_CUDA(launch_simt_down(d, (const float *)w.h, eoff, e0, e1, (const float *)wd, perm, tw,
+                                  (float *)slots, s),
+                 "fp32 down kernel");
+    return MOE_OK;
+}
+
+moe_status_t run_experts(const LayerDims &d, const void *send, const int32_t *eoff, int e0, int e1,
+                         const void *packed, const void *wd, const int32_t *perm, const float *tw,
+                         void *slots, const Workspace &w, cudaStream_t s) {
+    moe_status_t st = run_gate_up(d, send, eoff, e0, e1, packed, w, s);
+    if (st != MOE_OK) return st;
+    return run_down(d, eoff, e0, e1, wd, perm, tw, slots, w, s);
+}
+
+moe_status_t run_combine(const LayerDims &d, int mode, const void *slots, const int32_t *idx,
+                         const int32_t *slot_pos, void *out, const Workspace &w, cudaStream_t s) {
+    if (mode == MOE_MODE_DISPATCH) {
+        MOE_CUDA(launch_combine(d, slots, slot_pos, out, s), "combine kernel");
+    } else {
+        MOE_CUDA(launch_mask_partials(d, slots, idx, slot_pos, w.partials, s), "mask partials kernel");
+        MOE_CUDA(launch_partition_sum(d, w.partials, out, s), "partition sum kernel");
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+const char *moe_last_error(void) { return g_last_error.c_str(); }
+
+moe_status_t moe_workspace_size(const moe_config *cfg, size_t *bytes) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    if (bytes == nullptr) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = carve(d, cfg->mode, nullptr).bytes;
+    g_last_error.clear();
+    return MOE_OK;
+}
+
+moe_status_t moe_packed_gate_up_size(const moe_config *cfg, size_t *bytes) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    if (bytes == nullptr) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = (size_t)d.E * 2 * d.Ipad * d.H * esize(d);
+    g_last_error.clear();
+    return MOE_OK;
+}
+
+moe_status_t moe_pack_weights(const moe_config *cfg, const void *w_gate, const void *w_up,
+                              void *w_gate_up_packed, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    NEED(w_gate, true);
+    NEED(w_up, true);
+    NEED(w_gate_up_packed, true);
+    g_last_error.clear();
+    MOE_CUDA(launch_pack_gate_up(d, w_gate, w_up, w_gate_up_packed, (cudaStream_t)stream),
+             "pack kernel");
+    return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_config *cfg, const void *x, const void *w_router,
+                       const float *b_router, int32_t *topk_idx, float *topk_w, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    if (d.N == 0) return MOE_OK;
+    NEED(x, true);
+    NEED(w_router, true);
+    if (cfg->has_bias) NEED(b_router, false);
+    NEED(topk_idx, false);
+    NEED(topk_w, false);
+    g_last_error.clear();
+    return run_route(d, x, w_router, cfg->has_bias ? b_router : nullptr, topk_idx, topk_w, nullptr,
+                     (cudaStream_t)stream);
+}
+
+moe_status_t moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x,
+                          int32_t *routed_counts, int32_t *counts, int32_t *expert_offsets,
+                          int32_t *part_offsets, int32_t *perm, int32_t *slot_pos, void *send,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    NEED(routed_counts, false);
+    NEED(counts, false);
+    NEED(expert_offsets, false);
+    NEED(part_offsets, false);
+    Workspace w;
+    st = check_workspace(d, cfg->mode, workspace, workspace_bytes, &w);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (d.N == 0) {   // empty batch: zero counts and offsets, nothing else
+        MOE_CUDA(cudaMemsetAsync(routed_counts, 0, d.E * sizeof(int32_t), s), "memset");
+        MOE_CUDA(cudaMemsetAsync(counts, 0, d.E * sizeof(int32_t), s), "memset");
+        MOE_CUDA(cudaMemsetAsync(expert_offsets, 0, (d.E + 1) * sizeof(int32_t), s), "memset");
+        MOE_CUDA(cudaMemsetAsync(part_offsets, 0, (d.P + 1) * sizeof(int32_t), s), "memset");
+        return MOE_OK;
+    }
+    NEED(topk_idx, false);
+    NEED(x, true);
+    NEED(perm, false);
+    NEED(slot_pos, false);
+    NEED(send, true);
+    g_last_error.clear();
+    MOE_CUDA(launch_histogram(d, topk_idx, w.seg_hist, w.status, s), "histogram kernel");
+    return run_dispatch_from_hist(d, topk_idx, x, w, routed_counts, counts, expert_offsets,
+                                  part_offsets, perm, slot_pos, send, s);
+}
+
+moe_status_t moe_expert_ffn(const moe_config *cfg, const void *send, const int32_t *expert_offsets,
+                            int32_t expert_begin, int32_t expert_end, const void *w_gate_up_packed,
+                            const void *w_down, const int32_t *perm, const float *topk_w,
+                            void *out_slots, void *workspace, size_t workspace_bytes, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    if (expert_begin < 0 || expert_end > d.E || expert_begin >= expert_end)
+        return fail(MOE_ERR_INVALID_ARG, "expert range [%d, %d) not inside [0, %d)", expert_begin,
+                    expert_end, d.E);
+    Workspace w;
+    st = check_workspace(d, cfg->mode, workspace, workspace_bytes, &w);
+    if (st != MOE_OK) return st;
+    if (d.N == 0) return MOE_OK;
+    NEED(send, true);
+    NEED(expert_offsets, false);
+    NEED(w_gate_up_packed, true);
+    NEED(w_down, true);
+    NEED(perm, false);
+    NEED(topk_w, false);
+    NEED(out_slots, true);
+    g_last_error.clear();
+    return run_experts(d, send, expert_offsets, expert_begin, expert_end, w_gate_up_packed, w_down,
+                       perm, topk_w, out_slots, w, (cudaStream_t)stream);
+}
+
+moe_status_t moe_combine(const moe_config *cfg, const void *out_slots, const int32_t *topk_idx,
+                         const int32_t *slot_pos, void *out, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    Workspace w;
+    st = check_workspace(d, cfg->mode, workspace, workspace_bytes, &w);
+    if (st != MOE_OK) return st;
+    if (d.N == 0) return MOE_OK;
+    NEED(out_slots, true);
+    NEED(slot_pos, false);
+    if (cfg->mode == MOE_MODE_MASK_SUM) NEED(topk_idx, false);
+    NEED(out, true);
+    g_last_error.clear();
+    return run_combine(d, cfg->mode, out_slots, topk_idx, slot_pos, out, w, (cudaStream_t)stream);
+}
+
+moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void *w_router,
+                               const float *b_router, const void *w_gate_up_packed,
+                               const void *w_down, void *out, const moe_diagnostics *diag,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    Workspace w;
+    st = check_workspace(d, cfg->mode, workspace, workspace_bytes, &w);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    moe_diagnostics none = {};
+    const moe_diagnostics &g = diag ? *diag : none;
+    int32_t *idx = g.topk_idx ? g.topk_idx : w.topk_idx;
+    float *tw = g.topk_w ? g.topk_w : w.topk_w;
+    int32_t *routed = g.routed_counts ? g.routed_counts : w.routed;
+    int32_t *counts = g.counts ? g.counts : w.counts;
+    int32_t *eoff = g.expert_offsets ? g.expert_offsets : w.eoff;
+    int32_t *poff = g.part_offsets ? g.part_offsets : w.poff;
+    int32_t *perm = g.perm ? g.perm : w.perm;
+    int32_t *slot_pos = g.slot_pos ? g.slot_pos : w.slot_pos;
+    if (d.N == 0) {
+        g_last_error.clear();
+        if (g.routed_counts) MOE_CUDA(cudaMemsetAsync(routed, 0, d.E * 4, s), "memset");
+        if (g.counts) MOE_CUDA(cudaMemsetAsync(counts, 0, d.E * 4, s), "memset");
+        if (g.expert_offsets) MOE_CUDA(cudaMemsetAsync(eoff, 0, (d.E + 1) * 4, s), "memset");
+        if (g.part_offsets) MOE_CUDA(cudaMemsetAsync(poff, 0, (d.P + 1) * 4, s), "memset");
+        return MOE_OK;
+    }
+    NEED(x, true);
+    NEED(w_router, true);
+    if (cfg->has_bias) NEED(b_router, false);
+    NEED(w_gate_up_packed, true);
+    NEED(w_down, true);
+    NEED(out, true);
+    g_last_error.clear();
+    void *const *ev = g.stage_events;
+    auto mark = [&](int stage) -> moe_status_t {
+        if (ev == nullptr) return MOE_OK;
+        MOE_CUDA(cudaEventRecord((cudaEvent_t)ev[stage], s), "stage event record");
+        return MOE_OK;
+    };
+#define MOE_MARK(i)                 \
+    do {                            \
+        st = mark(i);               \
+        if (st != MOE_OK) return st; \
+    } while (0)
+
+    MOE_MARK(MOE_STAGE_ROUTE);
+    MOE_CUDA(launch_route(d, x, w_router, cfg->has_bias ? b_router : nullptr, idx, tw, w.seg_hist, s),
+             "route kernel");
+    MOE_MARK(MOE_STAGE_SCAN);
+    MOE_CUDA(launch_scan(d, w.seg_hist, w.seg_base, routed, counts, eoff, poff, s), "scan kernel");
+    MOE_MARK(MOE_STAGE_ASSIGN);
+    MOE_CUDA(launch_assign(d, idx, w.seg_base, eoff, slot_pos, perm, w.status, s), "assign kernel");
+    MOE_MARK(MOE_STAGE_PERMUTE);
+    MOE_CUDA(launch_permute(d, x, slot_pos, w.send, s), "permute kernel");
+    MOE_MARK(MOE_STAGE_GATE_UP);
+    if (cfg->mode == MOE_MODE_DISPATCH) {
+        st = run_gate_up(d, w.send, eoff, 0, d.E, w_gate_up_packed, w, s);
+        if (st != MOE_OK) return st;
+        MOE_MARK(MOE_STAGE_DOWN);
+        st = run_down(d, eoff, 0, d.E, w_down, perm, tw, w.slots, w, s);
+        if (st != MOE_OK) return st;
+    } else {   // each partition runs its own experts, as the ep_size ranks would
+        const int per = d.E / d.P;
+        for (int p = 0; p < d.P && st == MOE_OK; ++p)
+            st = run_experts(d, w.send, eoff, p * per, (p + 1) * per, w_gate_up_packed, w_down, perm,
+                             tw, w.slots, w, s);
+        if (st != MOE_OK) return st;
+        MOE_MARK(MOE_STAGE_DOWN);
+    }
+    MOE_MARK(MOE_STAGE_COMBINE);
+    st = run_combine(d, cfg->mode, w.slots, idx, slot_pos, out, w, s);
+    if (st != MOE_OK) return st;
+    MOE_MARK(MOE_NUM_STAGES);
+#undef MOE_MARK
+    return MOE_OK;
+}
+
+moe_status_t moe_read_device_status(const moe_config *cfg, void *workspace, size_t workspace_bytes,
+                                    int32_t *flags, int32_t reset, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    Workspace w;
+    st = check_workspace(d, cfg->mode, workspace, workspace_bytes, &w);
+    if (st != MOE_OK) return st;
+    if (flags == nullptr) return fail(MOE_ERR_INVALID_ARG, "flags is NULL");
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t v = 0;
+    MOE_CUDA(cudaMemcpyAsync(&v, w.status, sizeof v, cudaMemcpyDeviceToHost, s), "status read");
+    MOE_CUDA(cudaStreamSynchronize(s), "stream sync");
+    if (reset) {
+        MOE_CUDA(cudaMemsetAsync(w.status, 0, sizeof v, s), "status reset");
+        MOE_CUDA(cudaStreamSynchronize(s), "stream sync");
+    }
+    *flags = v;
+    g_last_error.clear();
+    if (v & MOE_DEV_TIMEOUT) return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out");
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,192 @@
+// Step 1 -- routing: logits = x W_r^T (+ b), top-k with ties to the lower expert id,
+// softmax over the k chosen logits, and the per-segment expert histogram that the
+// dispatch scan consumes. (Ultralytics glossary "Expert Parallelism", section "How tokens
+// move between GPUs", step 1 and its routing example.)
+//
+// One CTA of 256 threads routes kSegTokens = 64 tokens. The 64 x E logit tile is an
+// FFMA register-blocked product over H in chunks staged through shared memory (each
+// thread owns RT tokens x RE experts); logits stay on chip. One warp then selects each
+// token's top-k by k rounds of a warp arg-max on (value desc, id asc).
+// Exactness: products of the stored values are exact in fp32 and, for inputs on the
+// dyadic grids of the exact test variant, every partial sum is too, so the chosen ids
+// do not depend on the summation order.
+#include <float.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteKChunk = 32;
+
+template <typename T, int RE, int EG>
+__global__ void __launch_bounds__(kRouteThreads)
+route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__restrict__ bias,
+             int N, int H, int E, int k, int32_t *__restrict__ topk_idx,
+             float *__restrict__ topk_w, int32_t *__restrict__ seg_hist) {
+    constexpr int TB = kSegTokens;
+    constexpr int KC = kRouteKChunk;
+    constexpr int EP = RE * EG;               // experts padded to the thread layout
+    constexpr int TGN = kRouteThreads / EG;   // token groups
+    constexpr int RT = TB / TGN;              // tokens per thread
+    static_assert(RT >= 1 && TB % TGN == 0, "thread layout");
+    extern __shared__ float smem[];
+    float *xs = smem;                    // [TB][KC+1]
+    float *ws = xs + TB * (KC + 1);      // [EP][KC+1]
+    __shared__ int hist_s[kMaxExperts];
+
+    const int tid = threadIdx.x;
+    const int eg = tid % EG, tg = tid / EG;
+    const int t0 = blockIdx.x * TB;
+    for (int e = tid; e < E; e += kRouteThreads) hist_s[e] = 0;
+
+    float acc[RT][RE];
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int q = 0; q < RE; ++q) acc[r][q] = 0.f;
+
+    for (int h0 = 0; h0 < H; h0 += KC) {
+        for (int i = tid; i < TB * KC; i += kRouteThreads) {
+            const int r = i / KC, c = i % KC, t = t0 + r, h = h0 + c;
+            xs[r * (KC + 1) + c] = (t < N && h < H) ? to_f32(x[(size_t)t * H + h]) : 0.f;
+        }
+        for (int i = tid; i < EP * KC; i += kRouteThreads) {
+            const int r = i / KC, c = i % KC, h = h0 + c;
+            ws[r * (KC + 1) + c] = (r < E && h < H) ? to_f32(wr[(size_t)r * H + h]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int c = 0; c < KC; ++c) {
+            float a[RT], b[RE];
+#pragma unroll
+            for (int r = 0; r < RT; ++r) a[r] = xs[(tg + r * TGN) * (KC + 1) + c];
+#pragma unroll
+            for (int q = 0; q < RE; ++q) b[q] = ws[(eg + q * EG) * (KC + 1) + c];
+#pragma unroll
+            for (int r = 0; r < RT; ++r)
+#pragma unroll
+                for (int q = 0; q < RE; ++q) acc[r][q] = fmaf(a[r], b[q], acc[r][q]);
+        }
+        __syncthreads();
+    }
+
+    // logits tile to shared memory (reuses the staging buffers)
+    float *lg = smem;   // [TB][EP+1]
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int q = 0; q < RE; ++q) {
+            const int e = eg + q * EG;
+            float v = acc[r][q];
+            if (bias != nullptr && e < E) v += bias[e];
+            lg[(tg + r * TGN) * (EP + 1) + e] = v;
+        }
+    __syncthreads();
+
+    // top-k: one warp per token
+    constexpr int EPL = (EP + 31) / 32;
+    const int warp = tid / 32, lane = tid % 32;
+    for (int tl = warp; tl < TB; tl += kRouteThreads / 32) {
+        const int t = t0 + tl;
+        if (t >= N) break;
+        float v[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            const float l = (e < E) ? lg[tl * (EP + 1) + e] : -INFINITY;
+            v[i] = isnan(l) ? -INFINITY : l;   // a NaN logit ranks last
+        }
+        unsigned taken = 0;
+        float my_v = 0.f;
+        int my_i = 0;
+        for (int j = 0; j < k; ++j) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+                    bv = v[i];
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if (lane == j) {
+                my_v = bv;
+                my_i = bi;
+            }
+        }
+        // softmax over the chosen logits; slot 0 holds the largest
+        const float m = __shfl_sync(0xffffffffu, my_v, 0);
+        const float ex = (lane < k) ? expf(my_v - m) : 0.f;
+        float sum = ex;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane < k) {
+            topk_idx[(size_t)t * k + lane] = my_i;
+            topk_w[(size_t)t * k + lane] = ex / sum;
+            atomicAdd(&hist_s[my_i], 1);
+        }
+    }
+    if (seg_hist != nullptr) {
+        __syncthreads();
+        for (int e = tid; e < E; e += kRouteThreads) seg_hist[(size_t)blockIdx.x * E + e] = hist_s[e];
+    }
+}
+
+template <typename T, int RE, int EG>
+cudaError_t launch_route_t(const LayerDims &d, const T *x, const T *wr, const float *b,
+                           int32_t *idx, float *w, int32_t *hist, cudaStream_t s) {
+    constexpr int EP = RE * EG;
+    const size_t stage = (size_t)(kSegTokens + EP) * (kRouteKChunk + 1) * sizeof(float);
+    const size_t logits = (size_t)kSegTokens * (EP + 1) * sizeof(float);
+    const size_t smem = stage > logits ? stage : logits;
+    auto kern = route_kernel<T, RE, EG>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    const int grid = ceil_div(d.N, kSegTokens);
+    kern<<<grid, kRouteThreads, smem, s>>>(x, wr, b, d.N, d.H, d.E, d.k, idx, w, hist);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_route_dt(const LayerDims &d, const T *x, const T *wr, const float *b,
+                            int32_t *idx, float *w, int32_t *hist, cudaStream_t s) {
+    // experts per thread RE and expert groups EG, EP = RE*EG >= E
+    if (d.E <= 4) return launch_route_t<T, 1, 4>(d, x, wr, b, idx, w, hist, s);
+    if (d.E <= 8) return launch_route_t<T, 1, 8>(d, x, wr, b, idx, w, hist, s);
+    if (d.E <= 16) return launch_route_t<T, 1, 16>(d, x, wr, b, idx, w, hist, s);
+    if (d.E <= 32) return launch_route_t<T, 2, 16>(d, x, wr, b, idx, w, hist, s);
+    if (d.E <= 64) return launch_route_t<T, 4, 16>(d, x, wr, b, idx, w, hist, s);
+    if (d.E <= 128) return launch_route_t<T, 8, 16>(d, x, wr, b, idx, w, hist, s);
+    return launch_route_t<T, 16, 16>(d, x, wr, b, idx, w, hist, s);
+}
+
+}  // namespace
+
+cudaError_t launch_route(const LayerDims &d, const void *x, const void *w_router,
+                         const float *b_router, int32_t *topk_idx, float *topk_w,
+                         int32_t *seg_hist, cudaStream_t s) {
+    if (d.dtype == MOE_DTYPE_BF16)
+        return launch_route_dt<__nv_bfloat16>(d, (const __nv_bfloat16 *)x,
+                                              (const __nv_bfloat16 *)w_router, b_router,
+                                              topk_idx, topk_w, seg_hist, s);
+    return launch_route_dt<float>(d, (const float *)x, (const float *)w_router, b_router,
+                                  topk_idx, topk_w, seg_hist, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,264 @@
+/*
+ * moe.h -- C ABI of the single-GPU expert-parallel MoE layer forward (B300, sm_103a).
+ *
+ * The layer follows the four steps of an expert-parallel MoE layer as the Ultralytics
+ * glossary page "Expert Parallelism" states them (section "How tokens move between
+ * GPUs"): (1) a router scores every token against every expert and keeps the k best;
+ * (2) each token's hidden state is sent to the partition that owns each chosen expert;
+ * (3) every partition runs its local experts on the rows it received; (4) the outputs
+ * return to their token, are weighted by the router scores and summed. The Hugging Face
+ * "Expert parallelism" docs describe the same token-dispatch path (section "Token
+ * dispatch") and the alternative masking + all-reduce rule ("ep_router" +
+ * "moe_tp_experts", section "DistributedConfig").
+ *
+ * On one GPU the ep_size "ranks" are logical partitions of device memory: expert e
+ * belongs to partition e / (E / ep_size) (Hugging Face page, "How the sizes combine");
+ * the first all-to-all becomes the write into a send buffer grouped by expert (so each
+ * partition's rows are contiguous), the second becomes the weighted un-permute.
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer argument is a DEVICE pointer owned by the caller unless stated
+ *    otherwise; the library allocates no memory in any entry point and keeps no
+ *    pointer after returning.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Work is enqueued asynchronously on it; no entry point synchronises the host,
+ *    except moe_read_device_status.
+ *  - Matrices are dense row-major. Element type of x, w_router, expert weights, send,
+ *    out_slots and out is cfg->dtype (MOE_DTYPE_BF16 or MOE_DTYPE_FP32); router bias,
+ *    routing weights and accumulation are fp32; indices are int32.
+ *  - All arguments are validated before anything is enqueued (the Hugging Face page
+ *    likewise rejects a bad plan "before anything is sharded"). On error nothing is
+ *    launched and the call returns a status other than MOE_OK; moe_last_error() then
+ *    gives a one-line reason (thread-local, valid until the next call on the thread).
+ *  - num_tokens == 0 is valid and enqueues nothing.
+ *  - Pointers to matrices must be 16-byte aligned; hidden and intermediate must be
+ *    multiples of 8.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status_t {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad size, pointer, alignment, dtype or mode */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels handle (e.g. E>256) */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than moe_workspace_size */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
+    MOE_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (see device status) */
+} moe_status_t;
+
+enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP32 = 1 };
+enum { MOE_MODE_DISPATCH = 0, MOE_MODE_MASK_SUM = 1 };
+
+/* Device status word bits (moe_read_device_status). */
+enum {
+    MOE_DEV_OK = 0,
+    MOE_DEV_TIMEOUT = 1,        /* a pipeline wait exceeded its limit; results invalid */
+    MOE_DEV_BAD_EXPERT_ID = 2   /* a topk_idx entry outside [0, E); that pair was dropped */
+};
+
+/*
+ * Sizes of one layer call. The argument list follows the pages' statement of the
+ * problem: hidden states (num_tokens x hidden), a router over num_experts experts,
+ * top_k experts per token (Ultralytics page, step 1: "usually one, two or eight"),
+ * ep_size partitions that must divide num_experts (Hugging Face page, launch rules),
+ * an optional capacity factor (Ultralytics page, "Load balancing and capacity") and
+ * the dispatch-versus-mask-and-sum mode.
+ *
+ *  num_tokens       N >= 0
+ *  hidden           H, multiple of 8
+ *  intermediate     I, SwiGLU expert intermediate size, multiple of 8
+ *  num_experts      E, 1..256
+ *  top_k            k, 1..min(E, 32)
+ *  ep_size          P, divides E
+ *  capacity_factor  <= 0: no limit. Otherwise every expert keeps at most
+ *                   C = ceil(capacity_factor * N * k / E) (token, expert) pairs, the
+ *                   first C in token order; the rest contribute zero (no
+ *                   renormalisation). NaN is rejected.
+ *  mode             MOE_MODE_DISPATCH or MOE_MODE_MASK_SUM
+ *  dtype            MOE_DTYPE_BF16 (tcgen05 tensor-core experts) or MOE_DTYPE_FP32
+ *                   (fp32 FFMA experts)
+ *  has_bias         1 if the router has a bias vector (fp32 [E])
+ */
+typedef struct moe_config {
+    int64_t num_tokens;
+    int64_t hidden;
+    int64_t intermediate;
+    int32_t num_experts;
+    int32_t top_k;
+    int32_t ep_size;
+    float capacity_factor;
+    int32_t mode;
+    int32_t dtype;
+    int32_t has_bias;
+} moe_config;
+
+/* Stage boundaries recorded by moe_layer_forward when moe_diagnostics.stage_events is
+ * set: event i is recorded on the stream just before stage i is enqueued, event
+ * MOE_NUM_STAGES after the last one. In mask-and-sum mode the per-partition expert
+ * launches all fall in MOE_STAGE_GATE_UP and MOE_STAGE_DOWN is empty. */
+enum {
+    MOE_STAGE_ROUTE = 0,     /* router + top-k + softmax + segment histogram: 1 kernel */
+    MOE_STAGE_SCAN = 1,      /* counts, offsets, segment bases: 1 kernel */
+    MOE_STAGE_ASSIGN = 2,    /* stable slot of every pair: 1 kernel */
+    MOE_STAGE_PERMUTE = 3,   /* hidden-state rows into the send buffer: 1 kernel */
+    MOE_STAGE_GATE_UP = 4,   /* grouped GEMM gate/up + SwiGLU: 1 kernel (P in mask mode) */
+    MOE_STAGE_DOWN = 5,      /* grouped GEMM down + weighted un-permute: 1 kernel */
+    MOE_STAGE_COMBINE = 6,   /* slot sum (1 kernel) or partials + partition sum (2) */
+    MOE_NUM_STAGES = 7
+};
+
+/* Optional outputs of moe_layer_forward: every non-NULL pointer receives the same
+ * array the corresponding step entry point would write. */
+typedef struct moe_diagnostics {
+    int32_t *topk_idx;        /* [N, k] */
+    float *topk_w;            /* [N, k] */
+    int32_t *routed_counts;   /* [E]    */
+    int32_t *counts;          /* [E]    */
+    int32_t *expert_offsets;  /* [E+1]  */
+    int32_t *part_offsets;    /* [P+1]  */
+    int32_t *perm;            /* [N*k]  (first expert_offsets[E] entries meaningful) */
+    int32_t *slot_pos;        /* [N*k]  */
+    /* NULL, or MOE_NUM_STAGES + 1 cudaEvent_t handles (created by the caller) to record
+     * at the stage boundaries, for per-kernel timing on the caller's stream. */
+    void *const *stage_events;
+} moe_diagnostics;
+
+/* Human-readable name of a status code (static string). */
+const char *moe_status_string(moe_status_t status);
+
+/* Reason for the last non-OK status returned on the calling thread (static until the
+ * next call on that thread; "" if none). */
+const char *moe_last_error(void);
+
+/* Bytes of device workspace that moe_layer_forward needs for `cfg`; the same size is
+ * enough for every other entry point of the same cfg. Writes *bytes; returns
+ * MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED for a config the library rejects.
+ * The workspace must be 256-byte aligned. Its first 32 bytes hold the device status
+ * word (moe_read_device_status): zero them once before the first call. */
+moe_status_t moe_workspace_size(const moe_config *cfg, size_t *bytes);
+
+/* Bytes of the packed gate/up weight buffer moe_pack_weights writes for `cfg`. */
+moe_status_t moe_packed_gate_up_size(const moe_config *cfg, size_t *bytes);
+
+/*
+ * One-time weight preparation (not part of the timed forward). Interleaves each
+ * expert's gate and up projections in blocks of 128 output rows, zero-padding I up to
+ * a multiple of 128, so that one tensor-core tile produces matching gate and up
+ * columns for the fused SwiGLU.
+ *   w_gate, w_up        [E, I, H] dtype (nn.Linear layout: out x in)
+ *   w_gate_up_packed    [E, 2*Ipad, H] dtype, Ipad = ceil(I/128)*128; for block b,
+ *                       rows 256b..256b+127 are gate rows 128b.., the next 128 are up rows
+ */
+moe_status_t moe_pack_weights(const moe_config *cfg, const void *w_gate, const void *w_up,
+                              void *w_gate_up_packed, void *stream);
+
+/*
+ * Step 1 -- routing (Ultralytics page, "How tokens move between GPUs", step 1 and its
+ * routing example: a linear router, top-k of the raw logits).
+ *   x         [N, H] dtype
+ *   w_router  [E, H] dtype (nn.Linear layout)
+ *   b_router  [E] fp32, or NULL when cfg->has_bias == 0
+ *   topk_idx  [N, k] int32 out: chosen experts, descending logit, ties to lower id
+ *   topk_w    [N, k] fp32 out: softmax over the k chosen logits
+ * Logits are accumulated in fp32 and never written to memory.
+ */
+moe_status_t moe_route(const moe_config *cfg, const void *x, const void *w_router,
+                       const float *b_router, int32_t *topk_idx, float *topk_w,
+                       void *stream);
+
+/*
+ * Step 2 -- dispatch (Hugging Face page, "Token dispatch": every (token, expert) pair
+ * goes to the rank that owns the expert; Ultralytics page, step 2 and "Load balancing
+ * and capacity"). Builds the send layout grouped by expert (hence by partition) and
+ * copies each kept pair's hidden-state row into it. Pair p = t*k + j.
+ *   topk_idx        [N, k] int32 in (ids outside [0,E) are dropped, see device status)
+ *   x               [N, H] dtype in
+ *   routed_counts   [E] out: pairs routed to each expert (before capacity)
+ *   counts          [E] out: pairs kept
+ *   expert_offsets  [E+1] out: exclusive prefix sum of counts
+ *   part_offsets    [P+1] out: expert_offsets[p*E/P] (rows of partition p)
+ *   perm            [N*k] out: perm[r] = pair held by send row r, r < expert_offsets[E]
+ *   slot_pos        [N*k] out: send row of pair p, -1 if dropped
+ *   send            [N*k, H] dtype out: send[r] = x[perm[r] / k]
+ *   workspace       >= moe_workspace_size bytes (histograms)
+ * Results are bit-exact and deterministic: within an expert, rows are in token order.
+ */
+moe_status_t moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x,
+                          int32_t *routed_counts, int32_t *counts, int32_t *expert_offsets,
+                          int32_t *part_offsets, int32_t *perm, int32_t *slot_pos,
+                          void *send, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/*
+ * Step 3 -- local experts (Ultralytics page, step 3; Hugging Face page, "grouped_gemm"
+ * rule: expert weights split along the expert dimension). For every expert e in
+ * [expert_begin, expert_end) -- all experts, or one partition's range -- runs the
+ * SwiGLU FFN y = W_down (silu(W_gate x) * (W_up x)) on send rows
+ * [expert_offsets[e], expert_offsets[e+1]) as a grouped GEMM, and writes the weighted
+ * un-permuted result out_slots[perm[r]] = topk_w[perm[r]] * y_r (the return all-to-all
+ * fused into the epilogue). Rows of other experts and dropped pairs are not written.
+ *   send              [N*k, H] dtype
+ *   expert_offsets    [E+1] int32
+ *   w_gate_up_packed  from moe_pack_weights
+ *   w_down            [E, H, I] dtype
+ *   perm, topk_w      as written by moe_dispatch / moe_route
+ *   out_slots         [N*k, H] dtype out (row = pair id)
+ */
+moe_status_t moe_expert_ffn(const moe_config *cfg, const void *send,
+                            const int32_t *expert_offsets, int32_t expert_begin,
+                            int32_t expert_end, const void *w_gate_up_packed,
+                            const void *w_down, const int32_t *perm, const float *topk_w,
+                            void *out_slots, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
+/*
+ * Step 4 -- combine (Ultralytics page, step 4: results weighted by the router scores
+ * and summed at the token's origin).
+ *   MOE_MODE_DISPATCH: out[t] = sum over kept slots j, in slot order, of
+ *                      out_slots[t*k + j] (already weighted).
+ *   MOE_MODE_MASK_SUM: every partition p first forms its masked partial output
+ *                      partial_p[t] = sum of token t's kept slots whose expert lives in
+ *                      p (fp32, in the workspace), then out = partial_0 + ... +
+ *                      partial_{P-1} in partition order (the all-reduce of the
+ *                      "ep_router" + "moe_tp_experts" rule).
+ *   out_slots  [N*k, H] dtype; topk_idx, slot_pos [N*k] int32; out [N, H] dtype.
+ * A token whose pairs were all dropped gets a zero row.
+ */
+moe_status_t moe_combine(const moe_config *cfg, const void *out_slots,
+                         const int32_t *topk_idx, const int32_t *slot_pos, void *out,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The whole layer: route -> dispatch -> local experts -> combine, enqueued on `stream`
+ * with no host synchronisation. Intermediates live in `workspace`; `diag` (may be
+ * NULL) selects which of them are also written to caller buffers. In mask-and-sum
+ * mode the experts run once per partition (ep_size launches), like ep_size ranks.
+ *   x [N,H], w_router [E,H], b_router [E] or NULL, w_gate_up_packed, w_down [E,H,I],
+ *   out [N,H] dtype.
+ */
+moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void *w_router,
+                               const float *b_router, const void *w_gate_up_packed,
+                               const void *w_down, void *out, const moe_diagnostics *diag,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, reads the device status word kept in `workspace` (an OR of
+ * MOE_DEV_* bits accumulated since the last reset) into *flags, and clears it when
+ * `reset` != 0. Returns MOE_ERR_TIMEOUT if MOE_DEV_TIMEOUT is set.
+ */
+moe_status_t moe_read_device_status(const moe_config *cfg, void *workspace,
+                                    size_t workspace_bytes, int32_t *flags, int32_t reset,
+                                    void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

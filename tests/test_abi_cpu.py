@@ -1,0 +1,161 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every entry point the
+header declares, and validates arguments before touching CUDA."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
+                 "moe_layer_forward", "moe_workspace_size", "moe_pack_weights"):
+        assert must in names
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import expert_token_dispatch_gemm_b300 as m
+    return m
+
+
+def test_library_exports_every_declared_symbol(moe):
+    lib = ctypes.CDLL(moe.binding._LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.binding._LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (moe_\w+)$", out, flags=re.M))
+    assert set(declared_functions()) <= exported
+
+
+def test_library_is_built_for_sm103a_only(moe):
+    out = subprocess.run(["cuobjdump", "--list-elf", moe.binding._LIB_PATH],
+                         capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    arches = set(re.findall(r"sm_(\d+a?)", out.stdout))
+    assert arches == {"103a"}, arches
+
+
+def cfg(moe, **kw):
+    base = dict(N=64, H=64, I=32, E=8, top_k=2, ep_size=4)
+    base.update(kw)
+    return moe.config(**base)
+
+
+def status_of(moe, c):
+    n = ctypes.c_size_t(0)
+    return moe.lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(n)), n.value
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(), 0),
+    (dict(N=0), 0),
+    (dict(E=6, ep_size=4), 1),       # ep_size must divide E
+    (dict(H=60), 1),                 # hidden multiple of 8
+    (dict(I=12), 1),
+    (dict(top_k=9), 1),              # k <= E
+    (dict(top_k=0), 1),
+    (dict(N=-1), 1),
+    (dict(E=512, ep_size=8), 2),     # beyond the kernels' limit
+    (dict(E=64, top_k=33, ep_size=8), 2),
+    (dict(capacity_factor=float("nan")), 1),
+    (dict(capacity_factor=1.25), 0),
+    (dict(mode="mask_sum"), 0),
+    (dict(dtype="fp32"), 0),
+])
+def test_config_validation(moe, kw, status):
+    c = cfg(moe, **kw)
+    st, n = status_of(moe, c)
+    assert st == status, moe.lib.moe_last_error()
+    if st == 0:
+        assert n > 0
+    else:
+        assert moe.lib.moe_last_error().decode()
+
+
+def test_workspace_size_grows_with_tokens_and_mask_mode(moe):
+    _, a = status_of(moe, cfg(moe, N=64))
+    _, b = status_of(moe, cfg(moe, N=640))
+    _, c = status_of(moe, cfg(moe, N=640, mode="mask_sum"))
+    assert a < b < c
+    # the send buffer, h and out_slots alone need pairs * (2H + Ipad) * 2 bytes
+    pairs = 640 * 2
+    assert b >= pairs * (2 * 64 + 128) * 2
+    assert c - b >= 4 * 640 * 64 * 4
+
+
+def test_packed_size(moe):
+    n = ctypes.c_size_t(0)
+    c = cfg(moe, I=200)
+    assert moe.lib.moe_packed_gate_up_size(ctypes.byref(c), ctypes.byref(n)) == 0
+    assert n.value == 8 * 2 * 256 * 64 * 2   # Ipad = 256
+
+
+FAKE = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: validation fails first
+
+
+def test_forward_rejects_missing_or_small_workspace(moe):
+    c = cfg(moe)
+    P = FAKE
+    st = moe.lib.moe_layer_forward(ctypes.byref(c), P, P, None, P, P, P, None, None, 0, None)
+    assert st == moe.binding.MOE_ERR_WORKSPACE
+    st = moe.lib.moe_layer_forward(ctypes.byref(c), P, P, None, P, P, P, None, P, 100, None)
+    assert st == moe.binding.MOE_ERR_WORKSPACE
+    assert "needed" in moe.lib.moe_last_error().decode()
+
+
+def test_forward_rejects_misaligned_or_null_pointers(moe):
+    c = cfg(moe)
+    _, n = status_of(moe, c)
+    P = FAKE
+    bad = ctypes.c_void_p((1 << 20) + 8)
+    st = moe.lib.moe_layer_forward(ctypes.byref(c), bad, P, None, P, P, P, None, P, n, None)
+    assert st == moe.binding.MOE_ERR_INVALID_ARG
+    assert "x must be 16-byte aligned" in moe.lib.moe_last_error().decode()
+    st = moe.lib.moe_layer_forward(ctypes.byref(c), None, P, None, P, P, P, None, P, n, None)
+    assert st == moe.binding.MOE_ERR_INVALID_ARG
+    cb = cfg(moe, has_bias=True)
+    st = moe.lib.moe_layer_forward(ctypes.byref(cb), P, P, None, P, P, P, None, P, n, None)
+    assert st == moe.binding.MOE_ERR_INVALID_ARG
+    assert "b_router" in moe.lib.moe_last_error().decode()
+    st = moe.lib.moe_route(None, P, P, None, P, P, None)
+    assert st == moe.binding.MOE_ERR_INVALID_ARG
+
+
+def test_expert_range_validation(moe):
+    c = cfg(moe)
+    _, n = status_of(moe, c)
+    P = FAKE
+    for b, e in ((0, 0), (-1, 4), (4, 9), (5, 3)):
+        st = moe.lib.moe_expert_ffn(ctypes.byref(c), P, P, b, e, P, P, P, P, P, P, n, None)
+        assert st == moe.binding.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(moe):
+    c = cfg(moe, N=0)
+    _, n = status_of(moe, c)
+    # no diagnostics requested: nothing is enqueued, so no CUDA call is needed
+    st = moe.lib.moe_layer_forward(ctypes.byref(c), None, None, None, None, None, None, None,
+                                   FAKE, n, None)
+    assert st == 0
+    assert moe.lib.moe_route(ctypes.byref(c), None, None, None, None, None, None) == 0
+
+
+def test_status_strings(moe):
+    for s in range(6):
+        assert moe.lib.moe_status_string(s).decode().startswith("MOE_")

@@ -77,9 +77,9 @@ ALL_SHAPES = (PR1_FP32, GPTOSS, E8_TOP2, SKEWED_CAP, DECODE)
 BY_NAME = {s.name: s for s in ALL_SHAPES}
 
 
-def _gen(seed: int, tensor_id: int, device) -> torch.Generator:
+def _gen(seed: int, tensor_id: int, device, sub: int = 0) -> torch.Generator:
     g = torch.Generator(device=device)
-    g.manual_seed(1_000_003 * int(seed) + 7919 * tensor_id + 17)
+    g.manual_seed(1_000_003 * int(seed) + 7919 * tensor_id + 104_729 * sub + 17)
     return g
 
 
@@ -141,15 +141,23 @@ def layer_inputs(shape: LayerShape, seed: int = 0, variant: str = "perf",
     out["b_router"] = b
 
     if with_experts:
-        for key, rows, cols, tid in (("w_gate", I, H, _T_WG), ("w_up", I, H, _T_WU),
-                                     ("w_down", H, I, _T_WD)):
+        for key in ("w_gate", "w_up", "w_down"):
+            rows, cols = (H, I) if key == "w_down" else (I, H)
             w = torch.empty(E, rows, cols, device=device, dtype=dt)
-            g = _gen(seed, tid, device)
             for e in range(E):   # per expert, to bound the fp32 temporary
-                w[e] = (torch.randn(rows, cols, generator=g, device=device,
-                                    dtype=torch.float32) * shape.w_std).to(dt)
+                w[e] = expert_weight(shape, key, e, seed, device)
             out[key] = w
     return out
+
+
+def expert_weight(shape: LayerShape, key: str, e: int, seed: int = 0, device="cpu"):
+    """One expert's weight ("w_gate"/"w_up" [I, H] or "w_down" [H, I]) in the storage
+    dtype, ~ N(0, w_std^2), from its own generator stream (so it can be drawn alone)."""
+    tid = {"w_gate": _T_WG, "w_up": _T_WU, "w_down": _T_WD}[key]
+    rows, cols = (shape.H, shape.I) if key == "w_down" else (shape.I, shape.H)
+    g = _gen(seed, tid, device, sub=e + 1)
+    return (torch.randn(rows, cols, generator=g, device=device, dtype=torch.float32)
+            * shape.w_std).to(shape.torch_dtype)
 
 
 def snippet_inputs():
