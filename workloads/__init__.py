@@ -74,7 +74,14 @@ DECODE = LayerShape("decode_n128_h2880_e128_k4", N=128, H=2880, I=2880, E=128, t
                     ep_size=8)
 
 ALL_SHAPES = (PR1_FP32, GPTOSS, E8_TOP2, SKEWED_CAP, DECODE)
-BY_NAME = {s.name: s for s in ALL_SHAPES}
+
+# The gpt-oss-shaped layer scaled down to 16 experts and 1024 tokens: the same per-expert
+# GEMM shapes (about 256 rows per expert) with ~1.5 GB on the device, small enough for
+# full profiler captures.
+GPTOSS_PROFILE = LayerShape("gptoss_profile_n1024_h2880_e16_k4", N=1024, H=2880, I=2880,
+                            E=16, top_k=4, ep_size=8)
+
+BY_NAME = {s.name: s for s in ALL_SHAPES + (GPTOSS_PROFILE,)}
 
 
 def _gen(seed: int, tensor_id: int, device, sub: int = 0) -> torch.Generator:
