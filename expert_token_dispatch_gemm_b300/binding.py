@@ -69,6 +69,7 @@ def _load():
         "moe_pack_weights": (ctypes.c_int, [cfgp, P, P, P, P]),
         "moe_route": (ctypes.c_int, [cfgp, P, P, P, P, P, P]),
         "moe_dispatch": (ctypes.c_int, [cfgp, P, P, P, P, P, P, P, P, P, P, S, P]),
+        "moe_dispatch_noalloc": (ctypes.c_int, [cfgp, P, P, P, P, P, P, P, P, P, P]),
         "moe_expert_ffn": (ctypes.c_int, [cfgp, P, P, I32, I32, P, P, P, P, P, P, S, P]),
         "moe_combine": (ctypes.c_int, [cfgp, P, P, P, P, P, S, P]),
         "moe_layer_forward": (ctypes.c_int, [cfgp, P, P, P, P, P, P,
@@ -164,6 +165,19 @@ def moe_dispatch(cfg, topk_idx, x, routed_counts, counts, expert_offsets, part_o
                             _ptr(slot_pos, "slot_pos", i32), _ptr(send, "send", dt),
                             _ptr(workspace, "workspace"), workspace.numel(), _stream()),
            "moe_dispatch")
+
+
+def moe_dispatch_noalloc(cfg, topk_idx, x, routed_counts, counts, expert_offsets, part_offsets,
+                         perm, slot_pos, send):
+    """moe_dispatch for callers that cannot allocate: no workspace argument."""
+    dt = cfg.torch_dtype
+    i32 = torch.int32
+    _check(lib.moe_dispatch_noalloc(
+        ctypes.byref(cfg), _ptr(topk_idx, "topk_idx", i32), _ptr(x, "x", dt),
+        _ptr(routed_counts, "routed_counts", i32), _ptr(counts, "counts", i32),
+        _ptr(expert_offsets, "expert_offsets", i32), _ptr(part_offsets, "part_offsets", i32),
+        _ptr(perm, "perm", i32), _ptr(slot_pos, "slot_pos", i32), _ptr(send, "send", dt),
+        _stream()), "moe_dispatch_noalloc")
 
 
 def moe_expert_ffn(cfg, send, expert_offsets, expert_begin, expert_end, w_gate_up_packed,

@@ -6,6 +6,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -229,6 +230,35 @@ moe_status_t run_combine(const LayerDims &d, int mode, const void *slots, const 
         MOE_CUDA(launch_mask_partials(d, slots, idx, slot_pos, w.partials, s), "mask partials kernel");
         MOE_CUDA(launch_partition_sum(d, w.partials, out, s), "partition sum kernel");
     }
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- no-allocation dispatch
+// Scratch of moe_dispatch_noalloc: a status word (padded to 256 bytes), then the
+// per-segment histograms and the per-segment rank bases, each up to
+// kNoAllocMaxSegExperts ints. Every GPU that loads the library holds these 2 MiB until
+// the process exits.
+constexpr int kNoAllocMaxSegExperts = 1 << 18;
+constexpr int kNoAllocStatusInts = 64;
+__device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocStatusInts + 2 * kNoAllocMaxSegExperts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int32_t *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device
+// (the array's name is only a host-side stand-in in host code).
+moe_status_t noalloc_scratch(int32_t **out) {
+    int dev = 0;
+    MOE_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        MOE_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress");
+        g_noalloc_ptr[dev] = static_cast<int32_t *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
     return MOE_OK;
 }
 
@@ -481,6 +511,55 @@ moe_status_t moe_read_device_status(const moe_config *cfg, void *workspace, size
     g_last_error.clear();
     if (v & MOE_DEV_TIMEOUT) return fail(MOE_ERR_TIMEOUT, "a device-side wait timed out");
     return MOE_OK;
+}
+
+moe_status_t moe_dispatch_noalloc(const moe_config *cfg, const int32_t *topk_idx, const void *x,
+                                  int32_t *routed_counts, int32_t *counts,
+                                  int32_t *expert_offsets, int32_t *part_offsets, int32_t *perm,
+                                  int32_t *slot_pos, void *send, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    const int64_t seg_experts = (int64_t)ceil_div(d.N, kSegTokens) * d.E;
+    if (seg_experts > kNoAllocMaxSegExperts)
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "moe_dispatch_noalloc: ceil(num_tokens/%d) * num_experts = %lld exceeds its "
+                    "fixed scratch of %d; use moe_dispatch with a workspace",
+                    kSegTokens, (long long)seg_experts, kNoAllocMaxSegExperts);
+    NEED(routed_counts, false);
+    NEED(counts, false);
+    NEED(expert_offsets, false);
+    NEED(part_offsets, false);
+    if (d.N > 0) {
+        NEED(topk_idx, false);
+        NEED(x, true);
+        NEED(perm, false);
+        NEED(slot_pos, false);
+        NEED(send, true);
+    }
+    int32_t *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != MOE_OK) return st;
+    g_last_error.clear();
+    cudaStream_t s = (cudaStream_t)stream;
+    if (d.N == 0) {
+        MOE_CUDA(cudaMemsetAsync(routed_counts, 0, d.E * sizeof(int32_t), s), "memset");
+        MOE_CUDA(cudaMemsetAsync(counts, 0, d.E * sizeof(int32_t), s), "memset");
+        MOE_CUDA(cudaMemsetAsync(expert_offsets, 0, (d.E + 1) * sizeof(int32_t), s), "memset");
+        MOE_CUDA(cudaMemsetAsync(part_offsets, 0, (d.P + 1) * sizeof(int32_t), s), "memset");
+        return MOE_OK;
+    }
+    // The histogram kernel writes every [segment, expert] entry and the scan every base,
+    // so only the status word carries over from the previous call: clear it.
+    int32_t *status = scratch;
+    Workspace w = {};
+    w.status = status;
+    w.seg_hist = scratch + kNoAllocStatusInts;
+    w.seg_base = w.seg_hist + seg_experts;
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "status reset");
+    MOE_CUDA(launch_histogram(d, topk_idx, w.seg_hist, w.status, s), "histogram kernel");
+    return run_dispatch_from_hist(d, topk_idx, x, w, routed_counts, counts, expert_offsets,
+                                  part_offsets, perm, slot_pos, send, s);
 }
 
 }  // extern "C"

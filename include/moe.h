@@ -197,6 +197,34 @@ moe_status_t moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const 
                           void *stream);
 
 /*
+ * moe_dispatch without a workspace argument. The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory on their own -- code that
+ * runs where cudaMalloc is unavailable or forbidden (inside a host callback, or under an
+ * allocator that owns all device memory and hands out only the layer's inputs and
+ * outputs) and therefore cannot provide moe_dispatch's workspace.
+ *
+ * Same arguments, results and errors as moe_dispatch, minus workspace and its size. The
+ * per-segment histograms and rank bases live instead in a fixed array of device memory
+ * inside the library (2 MiB, plus 256 bytes for a status word), which every GPU that
+ * loads the library keeps until the process exits. Limit: ceil(num_tokens / 64) *
+ * num_experts must not exceed 262144 (for example 65536 tokens with 256 experts);
+ * larger calls return MOE_ERR_UNSUPPORTED and enqueue nothing.
+ *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *  - The first call on a device looks up the array's device address on that device
+ *    (cudaGetSymbolAddress, with that device current); make that first call before
+ *    any stream capture.
+ *  - All calls share the one array: calls whose work overlaps on the GPU (on different
+ *    streams, or from different threads) race and corrupt each other's results. Order
+ *    them on one stream or synchronise between them.
+ *  - Pairs with an expert id outside [0, E) are dropped, as in moe_dispatch; this entry
+ *    point does not report them.
+ */
+moe_status_t moe_dispatch_noalloc(const moe_config *cfg, const int32_t *topk_idx, const void *x,
+                                  int32_t *routed_counts, int32_t *counts,
+                                  int32_t *expert_offsets, int32_t *part_offsets, int32_t *perm,
+                                  int32_t *slot_pos, void *send, void *stream);
+
+/*
  * Step 3 -- local experts (Ultralytics page, step 3; Hugging Face page, "grouped_gemm"
  * rule: expert weights split along the expert dimension). For every expert e in
  * [expert_begin, expert_end) -- all experts, or one partition's range -- runs the
