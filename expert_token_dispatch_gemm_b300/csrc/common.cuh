@@ -104,6 +104,12 @@ cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *exp
                            const float *topk_w, void *out_slots, int32_t *status, int num_sms,
                            cudaStream_t s);
 
+// Tensor-core (bf16) router: logits, top-k, softmax and segment histogram in one kernel.
+// seg_hist and status may be null.
+cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_router,
+                            const float *bias, int32_t *topk_idx, float *topk_w,
+                            int32_t *seg_hist, int32_t *status, int num_sms, cudaStream_t s);
+
 // fp32 FFMA grouped FFN.
 cudaError_t launch_simt_gate_up(const LayerDims &d, const float *send,
                                 const int32_t *expert_offsets, int e_begin, int e_end,

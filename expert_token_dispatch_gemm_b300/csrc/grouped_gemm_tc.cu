@@ -3,9 +3,12 @@
 // experts on the rows it received; Hugging Face "Expert parallelism" docs: the
 // "grouped_gemm" rule splits expert weights along the expert dimension).
 //
-// Two instantiations of one persistent, warp-specialised kernel:
+// Three instantiations of one persistent, warp-specialised kernel:
 //   gate_up : h = silu(x W_g^T) * (x W_u^T)      A = send [rows, H], B = packed gate/up
 //   down    : out_slots[perm[r]] = w * (h W_d^T)  A = h [rows, I],    B = W_d [E*H, I]
+//   route   : logits = x W_r^T (+ b), then top-k / softmax / segment histogram in the
+//             epilogue (Ultralytics glossary, step 1): A = x [N, H], B = W_r [E, H],
+//             MMA N = E rounded up to 16; each epilogue thread owns one token's logits.
 // The tile space is (expert, n tile, m tile) over variable-length expert segments; a
 // 128-row M tile may run past its segment, those rows are computed on neighbouring
 // data and never stored.
@@ -43,14 +46,20 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
 // M >> 4 at bit 24.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t make_idesc(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
 
-enum { EPI_SWIGLU = 0, EPI_DOWN = 1 };
+enum { EPI_SWIGLU = 0, EPI_DOWN = 1, EPI_ROUTE = 2 };
+static_assert(BM == 2 * kSegTokens, "a route tile covers two histogram segments");
 
 struct TcParams {
-    const int32_t *expert_offsets;
+    const int32_t *expert_offsets;   // nullptr: one segment of `rows` rows (routing)
+    int rows;
     int e_begin, ne;
+    int bn;                  // MMA N of every tile (multiple of 16, <= BN)
+    uint32_t idesc;
     int num_kb;              // K blocks of BK
     int n_tiles;             // N tiles per expert
     int b_rows_per_expert;   // rows between experts in B's tensor map
@@ -60,7 +69,13 @@ struct TcParams {
     const int32_t *perm;
     const float *topk_w;
     int H;
-    int32_t *status;
+    // EPI_ROUTE
+    int E, k, nseg;
+    const float *bias;       // [E] or nullptr
+    int32_t *route_idx;      // [N, k] out
+    float *route_w;          // [N, k] out
+    int32_t *seg_hist;       // [nseg, E] or nullptr
+    int32_t *status;         // or nullptr
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -108,7 +123,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
             if (*abort_s) return false;
             if (globaltimer() - t0 > kWaitLimitNs) {
                 *abort_s = 1;
-                atomicOr(status, MOE_DEV_TIMEOUT);
+                if (status != nullptr) atomicOr(status, MOE_DEV_TIMEOUT);
                 return false;
             }
         }
@@ -150,12 +165,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
     return d;
 }
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t accumulate) {
+                                          uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
@@ -195,17 +210,46 @@ __device__ __forceinline__ uint4 pack8_bf16(const float *f) {
     return v;
 }
 
+// Sorted (descending) top-KMAX list in registers; empty slots have idx < 0. A new value
+// enters behind equal ones, so scanning experts in increasing id keeps ties ordered by
+// the lower id.
+template <int KMAX>
+__device__ __forceinline__ void topk_insert(float (&val)[KMAX], int (&idx)[KMAX], float v, int e) {
+    if (!(v > val[KMAX - 1] || idx[KMAX - 1] < 0)) return;
+#pragma unroll
+    for (int j = KMAX - 1; j > 0; --j) {
+        const bool beat_prev = v > val[j - 1] || idx[j - 1] < 0;
+        const bool beat_cur = v > val[j] || idx[j] < 0;
+        if (beat_prev) {
+            val[j] = val[j - 1];
+            idx[j] = idx[j - 1];
+        } else if (beat_cur) {
+            val[j] = v;
+            idx[j] = e;
+        }
+    }
+    if (v > val[0] || idx[0] < 0) {
+        val[0] = v;
+        idx[0] = e;
+    }
+}
+
+// Barrier among the four epilogue warps only.
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 struct SmemLayout {
     static constexpr uint32_t a_off = 0;
     static constexpr uint32_t b_off = STAGES * A_BYTES;
     static constexpr uint32_t bar_off = STAGES * STAGE_BYTES;
     static constexpr uint32_t misc_off = bar_off + 16 * 8;
     static constexpr uint32_t tables_off = misc_off + 16;
-    static constexpr uint32_t end = tables_off + 2 * (kMaxExperts + 1) * 4;
+    static constexpr uint32_t bias_off = tables_off + 2 * (kMaxExperts + 1) * 4;
+    static constexpr uint32_t hist_off = bias_off + kMaxExperts * 4;
+    static constexpr uint32_t end = hist_off + 2 * kMaxExperts * 4;
     static constexpr uint32_t alloc = end + 1024;   // slack to align the base to 1024
 };
 
-template <int EPI>
+template <int EPI, int KMAX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
@@ -222,10 +266,19 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     volatile int *abort_s = reinterpret_cast<volatile int *>(smem + SmemLayout::misc_off + 4);
     int *eo = reinterpret_cast<int *>(smem + SmemLayout::tables_off);
     int *mtp = eo + (kMaxExperts + 1);
+    float *bias_s = reinterpret_cast<float *>(smem + SmemLayout::bias_off);
+    int *hist_s = reinterpret_cast<int *>(smem + SmemLayout::hist_off);   // [2][E]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0) {
-        build_tile_tables(p.expert_offsets, p.e_begin, p.ne, BM, eo, mtp);
+        if (p.expert_offsets != nullptr) {
+            build_tile_tables(p.expert_offsets, p.e_begin, p.ne, BM, eo, mtp);
+        } else if (lane == 0) {
+            eo[0] = 0;
+            eo[1] = p.rows;
+            mtp[0] = 0;
+            mtp[1] = (p.rows + BM - 1) / BM;
+        }
         if (lane == 0) {
             tma_prefetch_desc(&tmap_a);
             tma_prefetch_desc(&tmap_b);
@@ -236,6 +289,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      "r"(TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else if (warp == 3) {
+        if (EPI == EPI_ROUTE)
+            for (int e = lane; e < p.E; e += 32) bias_s[e] = p.bias != nullptr ? p.bias[e] : 0.f;
     } else if (warp == 2 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -270,7 +326,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], A_BYTES + (uint32_t)p.bn * BK * 2);
                     const uint32_t fb = smem_u32(&full[stage]);
                     tma_load_2d(smem_u32(smem + SmemLayout::a_off + stage * A_BYTES), &tmap_a, fb,
                                 kb * BK, a_row);
@@ -313,7 +369,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         umma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32),
-                                  smem_desc_sw128(b_addr + kk * 32), (kb | kk) != 0);
+                                  smem_desc_sw128(b_addr + kk * 32), p.idesc, (kb | kk) != 0);
                     issued = true;
                     umma_commit(&empty[stage]);
                     if (++stage == STAGES) {
@@ -339,9 +395,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const int r = q * 32 + lane;      // accumulator row = tile row
         int acc = 0;
         uint32_t acc_phase = 0;
+        const int etid = threadIdx.x - 64;   // 0..127 across the epilogue warps
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             int i, m, n;
             decode_tile(tile, mtp, p.ne, p.n_tiles, i, m, n);
+            if (EPI == EPI_ROUTE) {   // previous tile's histogram is flushed; clear it
+                epilogue_sync();
+                for (int j = etid; j < 2 * p.E; j += 128) hist_s[j] = 0;
+                epilogue_sync();
+            }
             // tcgen05.ld is warp-collective: the whole warp leaves together on abort
             const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_s, p.status);
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -350,7 +412,53 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const bool valid = seg_row < eo[i + 1] - eo[i];
             const int grow = eo[i] + seg_row;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            if (EPI == EPI_SWIGLU) {
+            if (EPI == EPI_ROUTE) {
+                float val[KMAX];
+                int idx[KMAX];
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    val[j] = -INFINITY;
+                    idx[j] = -1;
+                }
+                for (int c = 0; c < p.bn; c += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int e = c + j;
+                        if (e < p.E) {
+                            const float l = v[j] + bias_s[e];
+                            topk_insert<KMAX>(val, idx, isnan(l) ? -INFINITY : l, e);
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);   // logits are in registers: free the accumulator
+                if (valid) {
+                    float ex[KMAX], sum = 0.f;
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j) {
+                        ex[j] = j < p.k ? expf(val[j] - val[0]) : 0.f;
+                        sum += ex[j];
+                    }
+                    const float inv = 1.0f / sum;
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j)
+                        if (j < p.k) {
+                            p.route_idx[(size_t)grow * p.k + j] = idx[j];
+                            p.route_w[(size_t)grow * p.k + j] = ex[j] * inv;
+                            if (p.seg_hist != nullptr)
+                                atomicAdd(&hist_s[(r >> 6) * p.E + idx[j]], 1);
+                        }
+                }
+                if (p.seg_hist != nullptr) {
+                    epilogue_sync();
+                    for (int j = etid; j < 2 * p.E; j += 128) {
+                        const int seg = 2 * m + j / p.E;
+                        if (seg < p.nseg) p.seg_hist[(size_t)seg * p.E + j % p.E] = hist_s[j];
+                    }
+                }
+            } else if (EPI == EPI_SWIGLU) {
                 __nv_bfloat16 *dst = p.h + (size_t)grow * p.h_ld + n * (BN / 2);
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
@@ -393,8 +501,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            if (EPI != EPI_ROUTE) {
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);
+            }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -450,11 +560,11 @@ cudaError_t make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int EPI>
+template <int EPI, int KMAX>
 cudaError_t launch_tc(const CUtensorMap &ma, const CUtensorMap &mb, const TcParams &prm,
                       int max_tiles, int num_sms, cudaStream_t s) {
     if (max_tiles <= 0) return cudaSuccess;
-    auto kern = grouped_gemm_tc_kernel<EPI>;
+    auto kern = grouped_gemm_tc_kernel<EPI, KMAX>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -482,6 +592,8 @@ cudaError_t launch_tc_gate_up(const LayerDims &d, const void *send, const int32_
     prm.expert_offsets = expert_offsets;
     prm.e_begin = e_begin;
     prm.ne = e_end - e_begin;
+    prm.bn = BN;
+    prm.idesc = make_idesc(BM, BN);
     prm.num_kb = ceil_div(d.H, BK);
     prm.n_tiles = 2 * d.Ipad / BN;
     prm.b_rows_per_expert = 2 * d.Ipad;
@@ -490,7 +602,8 @@ cudaError_t launch_tc_gate_up(const LayerDims &d, const void *send, const int32_
     prm.H = d.H;
     prm.status = status;
     const int64_t max_tiles = (ceil_div64(rows, BM) + prm.ne) * prm.n_tiles;
-    return launch_tc<EPI_SWIGLU>(ma, mb, prm, (int)std::min<int64_t>(max_tiles, 1 << 30), num_sms, s);
+    return launch_tc<EPI_SWIGLU, 1>(ma, mb, prm, (int)std::min<int64_t>(max_tiles, 1 << 30),
+                                    num_sms, s);
 }
 
 cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *expert_offsets,
@@ -507,6 +620,8 @@ cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *exp
     prm.expert_offsets = expert_offsets;
     prm.e_begin = e_begin;
     prm.ne = e_end - e_begin;
+    prm.bn = BN;
+    prm.idesc = make_idesc(BM, BN);
     prm.num_kb = ceil_div(d.I, BK);
     prm.n_tiles = ceil_div(d.H, BN);
     prm.b_rows_per_expert = d.H;
@@ -516,7 +631,41 @@ cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *exp
     prm.H = d.H;
     prm.status = status;
     const int64_t max_tiles = (ceil_div64(rows, BM) + prm.ne) * prm.n_tiles;
-    return launch_tc<EPI_DOWN>(ma, mb, prm, (int)std::min<int64_t>(max_tiles, 1 << 30), num_sms, s);
+    return launch_tc<EPI_DOWN, 1>(ma, mb, prm, (int)std::min<int64_t>(max_tiles, 1 << 30),
+                                  num_sms, s);
+}
+
+cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_router,
+                            const float *bias, int32_t *topk_idx, float *topk_w,
+                            int32_t *seg_hist, int32_t *status, int num_sms, cudaStream_t s) {
+    const int bn = (d.E + 15) / 16 * 16;
+    CUtensorMap ma, mb;
+    cudaError_t e = make_map(&ma, x, d.N, d.H, d.H, BM);
+    if (e != cudaSuccess) return e;
+    e = make_map(&mb, w_router, d.E, d.H, d.H, (uint32_t)bn);
+    if (e != cudaSuccess) return e;
+    TcParams prm = {};
+    prm.expert_offsets = nullptr;
+    prm.rows = d.N;
+    prm.e_begin = 0;
+    prm.ne = 1;
+    prm.bn = bn;
+    prm.idesc = make_idesc(BM, bn);
+    prm.num_kb = ceil_div(d.H, BK);
+    prm.n_tiles = 1;
+    prm.b_rows_per_expert = 0;
+    prm.H = d.H;
+    prm.E = d.E;
+    prm.k = d.k;
+    prm.nseg = ceil_div(d.N, kSegTokens);
+    prm.bias = bias;
+    prm.route_idx = topk_idx;
+    prm.route_w = topk_w;
+    prm.seg_hist = seg_hist;
+    prm.status = status;
+    const int tiles = ceil_div(d.N, BM);
+    if (d.k <= 8) return launch_tc<EPI_ROUTE, 8>(ma, mb, prm, tiles, num_sms, s);
+    return launch_tc<EPI_ROUTE, 32>(ma, mb, prm, tiles, num_sms, s);
 }
 
 }  // namespace moe

@@ -173,9 +173,16 @@ int num_sms() {
 }
 
 // --------------------------------------------------------------- step bodies
+// bf16 layers route on the tensor cores; fp32 layers on the FFMA router (single-pass
+// TF32 would round the fp32 inputs). `hist` (may be null) receives the segment
+// histogram; `status` (may be null) the device status bits.
 moe_status_t run_route(const LayerDims &d, const void *x, const void *wr, const float *b,
-                       int32_t *idx, float *w, int32_t *hist, cudaStream_t s) {
-    MOE_CUDA(launch_route(d, x, wr, b, idx, w, hist, s), "route kernel");
+                       int32_t *idx, float *w, int32_t *hist, int32_t *status, cudaStream_t s) {
+    if (d.dtype == MOE_DTYPE_BF16)
+        MOE_CUDA(launch_tc_route(d, x, wr, b, idx, w, hist, status, num_sms(), s),
+                 "tensor-core route kernel");
+    else
+        MOE_CUDA(launch_route(d, x, wr, b, idx, w, hist, s), "route kernel");
     return MOE_OK;
 }
 
@@ -330,7 +337,7 @@ moe_status_t moe_route(const moe_config *cfg, const void *x, const void *w_route
     NEED(topk_w, false);
     g_last_error.clear();
     return run_route(d, x, w_router, cfg->has_bias ? b_router : nullptr, topk_idx, topk_w, nullptr,
-                     (cudaStream_t)stream);
+                     nullptr, (cudaStream_t)stream);
 }
 
 moe_status_t moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x,
@@ -459,8 +466,9 @@ moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void 
     } while (0)
 
     MOE_MARK(MOE_STAGE_ROUTE);
-    MOE_CUDA(launch_route(d, x, w_router, cfg->has_bias ? b_router : nullptr, idx, tw, w.seg_hist, s),
-             "route kernel");
+    st = run_route(d, x, w_router, cfg->has_bias ? b_router : nullptr, idx, tw, w.seg_hist,
+                   w.status, s);
+    if (st != MOE_OK) return st;
     MOE_MARK(MOE_STAGE_SCAN);
     MOE_CUDA(launch_scan(d, w.seg_hist, w.seg_base, routed, counts, eoff, poff, s), "scan kernel");
     MOE_MARK(MOE_STAGE_ASSIGN);
