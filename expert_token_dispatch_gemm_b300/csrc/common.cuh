@@ -15,8 +15,11 @@ namespace moe {
 constexpr int kSegTokens = 64;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
-// Output rows per interleaved gate/up block of the packed weights.
-constexpr int kGateUpBlock = 128;
+// Gate rows per interleaved gate/up block of the packed weights: block b holds gate rows
+// 64b..64b+63 followed by the matching up rows. The intermediate size is padded to
+// kIpadAlign (two blocks: the 256 weight rows of one tensor-core tile).
+constexpr int kGateUpBlock = 64;
+constexpr int kIpadAlign = 128;
 
 // Rows per M tile of the grouped GEMMs (tensor-core path and fp32 path).
 constexpr int kTcBlockM = 128;

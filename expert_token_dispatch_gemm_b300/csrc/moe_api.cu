@@ -63,7 +63,7 @@ moe_status_t check_config(const moe_config *cfg, LayerDims *d) {
         return fail(MOE_ERR_INVALID_ARG, "unknown dtype %d", cfg->dtype);
     if (cfg->has_bias != 0 && cfg->has_bias != 1) return fail(MOE_ERR_INVALID_ARG, "has_bias must be 0 or 1");
     const int64_t pairs = N * cfg->top_k;
-    const int64_t Ipad = (I + kGateUpBlock - 1) / kGateUpBlock * kGateUpBlock;
+    const int64_t Ipad = (I + kIpadAlign - 1) / kIpadAlign * kIpadAlign;
     if (pairs > INT_MAX / 2 || H > (1 << 20) || Ipad > (1 << 20) ||
         pairs * std::max(H, Ipad) > ((int64_t)1 << 40))
         return fail(MOE_ERR_UNSUPPORTED, "sizes too large for 32-bit row indices");

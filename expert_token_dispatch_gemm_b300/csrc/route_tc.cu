@@ -1,0 +1,375 @@
+// Step 1 on the tensor cores -- routing for bf16 layers (Ultralytics glossary "Expert
+// Parallelism", section "How tokens move between GPUs", step 1 and its routing example):
+// logits = x W_r^T (+ b) accumulate in TMEM, M = 128 tokens by N = E rounded up to 16;
+// each epilogue thread owns one token's logits, keeps its top-k in registers (ties to
+// the lower expert id), applies the softmax over the k chosen logits and adds the
+// token's experts to the per-segment histogram that the dispatch scan consumes.
+//
+// Per CTA (one per SM, 192 threads, persistent over 128-token tiles):
+//   warp 0      TMA producer: 128x64 x tile + E x 64 router tile per stage, 128-byte
+//               swizzle, 4-stage ring guarded by full/empty mbarriers;
+//   warp 1      allocates 512 TMEM columns (two accumulators) and one thread issues
+//               tcgen05.mma (M=128, N=round16(E), K=16, bf16 in, fp32 acc);
+//   warps 2..5  epilogue: tcgen05.ld of the logits of their TMEM lane quarter, top-k,
+//               softmax, histogram; the accumulator is released as soon as the logits
+//               are in registers, so MMA and epilogue overlap.
+// Exactness: bf16 products are exact in fp32 and, for inputs on the dyadic grids of the
+// exact test variant, every partial sum is too, so the chosen ids do not depend on the
+// order in which the tensor cores accumulate.
+// Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
+// MOE_DEV_TIMEOUT in the status word, stops issuing work, waits (bounded) for its own
+// copies and MMAs in flight, frees TMEM and returns.
+#include "sm100.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = kTcBlockM;   // 128
+constexpr int BN = 256;         // accumulator columns reserved per tile (E <= 256)
+constexpr int STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+static_assert(BM == 2 * kSegTokens, "a route tile covers two histogram segments");
+
+struct RouteParams {
+    int rows;                // tokens
+    int bn;                  // MMA N (E rounded up to 16)
+    uint32_t idesc;
+    int num_kb;              // K blocks of BK
+    int E, k, nseg;
+    const float *bias;       // [E] or nullptr
+    int32_t *route_idx;      // [N, k] out
+    float *route_w;          // [N, k] out
+    int32_t *seg_hist;       // [nseg, E] or nullptr
+    int32_t *status;         // or nullptr
+};
+
+// Sorted (descending) top-KMAX list in registers; empty slots have idx < 0. A new value
+// enters behind equal ones, so scanning experts in increasing id keeps ties ordered by
+// the lower id.
+template <int KMAX>
+__device__ __forceinline__ void topk_insert(float (&val)[KMAX], int (&idx)[KMAX], float v, int e) {
+    if (!(v > val[KMAX - 1] || idx[KMAX - 1] < 0)) return;
+#pragma unroll
+    for (int j = KMAX - 1; j > 0; --j) {
+        const bool beat_prev = v > val[j - 1] || idx[j - 1] < 0;
+        const bool beat_cur = v > val[j] || idx[j] < 0;
+        if (beat_prev) {
+            val[j] = val[j - 1];
+            idx[j] = idx[j - 1];
+        } else if (beat_cur) {
+            val[j] = v;
+            idx[j] = e;
+        }
+    }
+    if (v > val[0] || idx[0] < 0) {
+        val[0] = v;
+        idx[0] = e;
+    }
+}
+
+struct SmemLayout {
+    static constexpr uint32_t a_off = 0;
+    static constexpr uint32_t b_off = STAGES * A_BYTES;
+    static constexpr uint32_t bar_off = STAGES * STAGE_BYTES;
+    static constexpr uint32_t misc_off = bar_off + 16 * 8;
+    static constexpr uint32_t bias_off = misc_off + 16;
+    static constexpr uint32_t hist_off = bias_off + kMaxExperts * 4;
+    static constexpr uint32_t end = hist_off + 2 * kMaxExperts * 4;
+    static constexpr uint32_t alloc = end + 1024;   // slack to align the base to 1024
+};
+
+template <int KMAX>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                const __grid_constant__ CUtensorMap tmap_w, const RouteParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SmemLayout::bar_off);
+    uint64_t *full = bars;                  // [STAGES]
+    uint64_t *empty = bars + STAGES;        // [STAGES]
+    uint64_t *tfull = bars + 2 * STAGES;    // [2]
+    uint64_t *tempty = tfull + 2;           // [2]
+    uint64_t *mma_done = tempty + 2;        // [1]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayout::misc_off);
+    volatile int *abort_s = reinterpret_cast<volatile int *>(smem + SmemLayout::misc_off + 4);
+    float *bias_s = reinterpret_cast<float *>(smem + SmemLayout::bias_off);
+    int *hist_s = reinterpret_cast<int *>(smem + SmemLayout::hist_off);   // [2][E]
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_x);
+            tma_prefetch_desc(&tmap_w);
+        }
+    } else if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else if (warp == 3) {
+        for (int e = lane; e < p.E; e += 32) bias_s[e] = p.bias != nullptr ? p.bias[e] : 0.f;
+    } else if (warp == 2 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(mma_done, 1);
+        *abort_s = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = (p.rows + BM - 1) / BM;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, armed_parity = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_s, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], A_BYTES + (uint32_t)p.bn * BK * 2);
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    tma_load_2d(smem_u32(smem + SmemLayout::a_off + stage * A_BYTES), &tmap_x, fb,
+                                kb * BK, tile * BM);
+                    tma_load_2d(smem_u32(smem + SmemLayout::b_off + stage * B_BYTES), &tmap_w, fb,
+                                kb * BK, 0);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // no copy may still be landing when the CTA exits
+            for (int s = 0; s < STAGES; ++s)
+                if ((armed >> s) & 1u) {
+                    volatile int no_abort = 0;
+                    mbar_wait(&full[s], (armed_parity >> s) & 1u, &no_abort, p.status);
+                }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ------------------------------------------ MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool issued = false, ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_s, p.status)) break;
+                fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_s, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t a_addr = smem_u32(smem + SmemLayout::a_off + stage * A_BYTES);
+                    const uint32_t b_addr = smem_u32(smem + SmemLayout::b_off + stage * B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32),
+                                 smem_desc_sw128(b_addr + kk * 32), p.idesc, (kb | kk) != 0);
+                    issued = true;
+                    commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                commit(&tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (issued) {   // every MMA done before TMEM is freed
+                commit(mma_done);
+                volatile int no_abort = 0;
+                mbar_wait(mma_done, 0, &no_abort, p.status);
+            }
+        }
+    } else {   // ------------------------------------------------------ epilogue
+        const int q = warp & 3;           // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;      // accumulator row = token of the tile
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const int etid = threadIdx.x - 64;   // 0..127 across the epilogue warps
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            // previous tile's histogram is flushed; clear it
+            epilogue_sync();
+            for (int j = etid; j < 2 * p.E; j += 128) hist_s[j] = 0;
+            epilogue_sync();
+            // tcgen05.ld is warp-collective and the epilogue warps share named
+            // barriers: all four leave together on abort
+            const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_s, p.status);
+            if (!epilogue_all(ok)) break;
+            fence_after();
+            const int tok = tile * BM + r;
+            const bool valid = tok < p.rows;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            float val[KMAX];
+            int idx[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                val[j] = -INFINITY;
+                idx[j] = -1;
+            }
+            for (int c = 0; c < p.bn; c += 32) {
+                float v[32];
+                tmem_ld32(taddr + c, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int e = c + j;
+                    if (e < p.E) {
+                        const float l = v[j] + bias_s[e];
+                        topk_insert<KMAX>(val, idx, isnan(l) ? -INFINITY : l, e);
+                    }
+                }
+            }
+            fence_before();
+            mbar_arrive(&tempty[acc]);   // logits are in registers: free the accumulator
+            if (valid) {
+                float ex[KMAX], sum = 0.f;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    ex[j] = j < p.k ? expf(val[j] - val[0]) : 0.f;
+                    sum += ex[j];
+                }
+                const float inv = 1.0f / sum;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j)
+                    if (j < p.k) {
+                        p.route_idx[(size_t)tok * p.k + j] = idx[j];
+                        p.route_w[(size_t)tok * p.k + j] = ex[j] * inv;
+                        if (p.seg_hist != nullptr) atomicAdd(&hist_s[(r >> 6) * p.E + idx[j]], 1);
+                    }
+            }
+            if (p.seg_hist != nullptr) {
+                epilogue_sync();
+                for (int j = etid; j < 2 * p.E; j += 128) {
+                    const int seg = 2 * tile + j / p.E;
+                    if (seg < p.nseg) p.seg_hist[(size_t)seg * p.E + j % p.E] = hist_s[j];
+                }
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+template <int KMAX>
+cudaError_t launch_route_tc(const CUtensorMap &mx, const CUtensorMap &mw, const RouteParams &prm,
+                            int tiles, int num_sms, cudaStream_t s) {
+    if (tiles <= 0) return cudaSuccess;
+    auto kern = route_tc_kernel<KMAX>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SmemLayout::alloc);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    kern<<<grid, NUM_THREADS, SmemLayout::alloc, s>>>(mx, mw, prm);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t get_encoder(EncodeTiledFn *fn) {
+    static EncodeTiledFn cached = nullptr;
+    if (cached == nullptr) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess) return e;
+        if (q != cudaDriverEntryPointSuccess || ptr == nullptr) return cudaErrorNotSupported;
+        cached = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    *fn = cached;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t tc::make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                         uint64_t ld, uint32_t box_rows) {
+    EncodeTiledFn enc;
+    cudaError_t e = get_encoder(&enc);
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_router,
+                            const float *bias, int32_t *topk_idx, float *topk_w,
+                            int32_t *seg_hist, int32_t *status, int num_sms, cudaStream_t s) {
+    const int bn = (d.E + 15) / 16 * 16;
+    CUtensorMap mx, mw;
+    cudaError_t e = tc::make_map(&mx, x, d.N, d.H, d.H, BM);
+    if (e != cudaSuccess) return e;
+    e = tc::make_map(&mw, w_router, d.E, d.H, d.H, (uint32_t)bn);
+    if (e != cudaSuccess) return e;
+    RouteParams prm = {};
+    prm.rows = d.N;
+    prm.bn = bn;
+    prm.idesc = make_idesc(BM, bn);
+    prm.num_kb = ceil_div(d.H, BK);
+    prm.E = d.E;
+    prm.k = d.k;
+    prm.nseg = ceil_div(d.N, kSegTokens);
+    prm.bias = bias;
+    prm.route_idx = topk_idx;
+    prm.route_w = topk_w;
+    prm.seg_hist = seg_hist;
+    prm.status = status;
+    const int tiles = ceil_div(d.N, BM);
+    if (d.k <= 8) return launch_route_tc<8>(mx, mw, prm, tiles, num_sms, s);
+    return launch_route_tc<32>(mx, mw, prm, tiles, num_sms, s);
+}
+
+}  // namespace moe

@@ -149,12 +149,12 @@ moe_status_t moe_packed_gate_up_size(const moe_config *cfg, size_t *bytes);
 
 /*
  * One-time weight preparation (not part of the timed forward). Interleaves each
- * expert's gate and up projections in blocks of 128 output rows, zero-padding I up to
- * a multiple of 128, so that one tensor-core tile produces matching gate and up
- * columns for the fused SwiGLU.
+ * expert's gate and up projections in blocks of 64 output rows, zero-padding I up to
+ * a multiple of 128, so that the accumulator of one SM holds matching gate and up rows
+ * for the fused SwiGLU.
  *   w_gate, w_up        [E, I, H] dtype (nn.Linear layout: out x in)
  *   w_gate_up_packed    [E, 2*Ipad, H] dtype, Ipad = ceil(I/128)*128; for block b,
- *                       rows 256b..256b+127 are gate rows 128b.., the next 128 are up rows
+ *                       rows 128b..128b+63 are gate rows 64b.., the next 64 are up rows
  */
 moe_status_t moe_pack_weights(const moe_config *cfg, const void *w_gate, const void *w_up,
                               void *w_gate_up_packed, void *stream);

@@ -29,6 +29,8 @@ SMALL = [
     S("fp32_ragged", N=333, H=96, I=72, E=6, top_k=3, ep_size=3, dtype="fp32", bias=True),
     S("fp32_cap", N=640, H=64, I=40, E=8, top_k=2, ep_size=2, dtype="fp32",
       capacity_factor=0.75, zipf_s=1.1),
+    # ~550 tokens per expert: three 256-token tiles, the last one nearly empty
+    S("bf16_long_segments", N=1100, H=136, I=72, E=2, top_k=1, ep_size=2),
 ]
 
 
