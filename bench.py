@@ -427,7 +427,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_from_device(shape, inp)
 
-    launches_per_step = 7 if args.mode == "dispatch" else 4 + 2 * shape.ep_size + 2
+    launches_per_step = 7   # route, scan, assign, permute, gate_up, down, combine
     if rank == 0:
         line = dict(metric=METRIC, value=round(value, 1), unit="tokens/s", n_gpus=world,
                     steps=args.steps, warmup=args.warmup, ms_per_step=round(ms_step, 4),

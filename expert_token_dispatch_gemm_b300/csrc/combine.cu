@@ -7,8 +7,10 @@
 // Mask-and-sum rule (Hugging Face docs, "DistributedConfig": "ep_router" masks the
 // experts of other ranks, "moe_tp_experts" computes the local ones, an all-reduce sums
 // the rank outputs): every partition forms its partial output from the slots whose
-// expert it owns; the partials are then summed in partition order.
-// All three kernels are one warp per token with 16-byte vector accesses: HBM-bound.
+// expert it owns; the partials are then summed in partition order. An expert's slots
+// are the same whichever launch computed them, so the experts run once for all
+// partitions and the masking and the ordered sum happen here.
+// Both kernels are one warp per token with 16-byte vector accesses: HBM-bound.
 #include "common.cuh"
 
 namespace moe {
@@ -41,66 +43,55 @@ combine_kernel(const T *__restrict__ slots, const int32_t *__restrict__ slot_pos
     }
 }
 
+// Mask-and-sum: partition p's partial output of token t is the fp32 sum, in slot order,
+// of the slots whose expert partition p owns (the other partitions' experts are masked
+// out); the partials are then added in partition order. Partials stay in registers.
 template <typename T>
 __global__ void __launch_bounds__(256)
-mask_partials_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
-                     const int32_t *__restrict__ slot_pos, int N, int k, int H, int E, int P,
-                     float *__restrict__ partials) {
+mask_sum_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
+                const int32_t *__restrict__ slot_pos, int N, int k, int H, int E, int P,
+                T *__restrict__ out) {
     using V = Vec16<T>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int t = blockIdx.x * 8 + warp;
     if (t >= N) return;
     const int per_part = E / P;
     int owner = -1;
-    if (lane < k && slot_pos[(size_t)t * k + lane] >= 0) {
-        const int e = idx[(size_t)t * k + lane];
-        owner = e / per_part;
-    }
+    if (lane < k && slot_pos[(size_t)t * k + lane] >= 0) owner = idx[(size_t)t * k + lane] / per_part;
+    // partitions that own at least one kept slot of this token, in increasing order; an
+    // empty partition's partial is 0 and adding it leaves the sum unchanged
     const int nvec = H / V::N;
     const uint4 *src = reinterpret_cast<const uint4 *>(slots + (size_t)t * k * H);
-    for (int p = 0; p < P; ++p) {
-        const unsigned mine = __ballot_sync(0xffffffffu, owner == p);
-        float4 *dst = reinterpret_cast<float4 *>(partials + ((size_t)p * N + t) * H);
-        for (int v = lane; v < nvec; v += 32) {
-            float acc[V::N];
-#pragma unroll
-            for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
-            for (int j = 0; j < k; ++j) {
-                if (!((mine >> j) & 1u)) continue;
-                float f[V::N];
-                V::to_float(__ldg(src + (size_t)j * nvec + v), f);
-#pragma unroll
-                for (int i = 0; i < V::N; ++i) acc[i] += f[i];
-            }
-#pragma unroll
-            for (int i = 0; i < V::N; i += 4)
-                dst[(size_t)v * (V::N / 4) + i / 4] = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-        }
-    }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(256)
-partition_sum_kernel(const float *__restrict__ partials, int N, int H, int P, T *__restrict__ out) {
-    using V = Vec16<T>;
-    const int64_t nvec = (int64_t)N * H / V::N;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+    uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)t * H);
+    for (int v = lane; v < nvec; v += 32) {
         float acc[V::N];
 #pragma unroll
         for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
-        for (int p = 0; p < P; ++p) {
-            const float4 *src = reinterpret_cast<const float4 *>(partials + (size_t)p * N * H) + v * (V::N / 4);
-#pragma unroll
-            for (int i = 0; i < V::N; i += 4) {
-                const float4 f = __ldg(src + i / 4);
-                acc[i] += f.x;
-                acc[i + 1] += f.y;
-                acc[i + 2] += f.z;
-                acc[i + 3] += f.w;
+        int p = -1;
+        unsigned todo = __ballot_sync(0xffffffffu, owner >= 0) & ((k < 32) ? ((1u << k) - 1u) : ~0u);
+        while (todo) {
+            // lowest partition among the remaining slots
+            int pmin = 0x7fffffff;
+            for (unsigned m = todo; m; m &= m - 1) {
+                const int o = __shfl_sync(0xffffffffu, owner, __ffs(m) - 1);
+                pmin = o < pmin ? o : pmin;
             }
+            p = pmin;
+            const unsigned mine = __ballot_sync(0xffffffffu, owner == p);
+            float part[V::N];
+#pragma unroll
+            for (int i = 0; i < V::N; ++i) part[i] = 0.f;
+            for (unsigned m = mine; m; m &= m - 1) {
+                float f[V::N];
+                V::to_float(__ldg(src + (size_t)(__ffs(m) - 1) * nvec + v), f);
+#pragma unroll
+                for (int i = 0; i < V::N; ++i) part[i] += f[i];
+            }
+#pragma unroll
+            for (int i = 0; i < V::N; ++i) acc[i] += part[i];
+            todo &= ~mine;
         }
-        reinterpret_cast<uint4 *>(out)[v] = V::from_float(acc);
+        dst[v] = V::from_float(acc);
     }
 }
 
@@ -142,29 +133,16 @@ cudaError_t launch_combine(const LayerDims &d, const void *out_slots, const int3
     return cudaGetLastError();
 }
 
-cudaError_t launch_mask_partials(const LayerDims &d, const void *out_slots,
-                                 const int32_t *topk_idx, const int32_t *slot_pos,
-                                 float *partials, cudaStream_t s) {
+cudaError_t launch_mask_sum(const LayerDims &d, const void *out_slots, const int32_t *topk_idx,
+                            const int32_t *slot_pos, void *out, cudaStream_t s) {
     const int grid = ceil_div(d.N, 8);
     if (d.dtype == MOE_DTYPE_BF16)
-        mask_partials_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            (const __nv_bfloat16 *)out_slots, topk_idx, slot_pos, d.N, d.k, d.H, d.E, d.P, partials);
+        mask_sum_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            (const __nv_bfloat16 *)out_slots, topk_idx, slot_pos, d.N, d.k, d.H, d.E, d.P,
+            (__nv_bfloat16 *)out);
     else
-        mask_partials_kernel<float><<<grid, 256, 0, s>>>((const float *)out_slots, topk_idx,
-                                                         slot_pos, d.N, d.k, d.H, d.E, d.P,
-                                                         partials);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_partition_sum(const LayerDims &d, const float *partials, void *out,
-                                 cudaStream_t s) {
-    const int64_t nvec = (int64_t)d.N * d.H / (d.dtype == MOE_DTYPE_BF16 ? 8 : 4);
-    const int grid = (int)std::min<int64_t>(ceil_div64(nvec, 256), 148 * 16);
-    if (d.dtype == MOE_DTYPE_BF16)
-        partition_sum_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(partials, d.N, d.H, d.P,
-                                                                 (__nv_bfloat16 *)out);
-    else
-        partition_sum_kernel<float><<<grid, 256, 0, s>>>(partials, d.N, d.H, d.P, (float *)out);
+        mask_sum_kernel<float><<<grid, 256, 0, s>>>((const float *)out_slots, topk_idx, slot_pos,
+                                                    d.N, d.k, d.H, d.E, d.P, (float *)out);
     return cudaGetLastError();
 }
 

@@ -123,11 +123,8 @@ cudaError_t launch_simt_down(const LayerDims &d, const float *h, const int32_t *
 
 cudaError_t launch_combine(const LayerDims &d, const void *out_slots, const int32_t *slot_pos,
                            void *out, cudaStream_t s);
-cudaError_t launch_mask_partials(const LayerDims &d, const void *out_slots,
-                                 const int32_t *topk_idx, const int32_t *slot_pos,
-                                 float *partials, cudaStream_t s);
-cudaError_t launch_partition_sum(const LayerDims &d, const float *partials, void *out,
-                                 cudaStream_t s);
+cudaError_t launch_mask_sum(const LayerDims &d, const void *out_slots, const int32_t *topk_idx,
+                            const int32_t *slot_pos, void *out, cudaStream_t s);
 
 }  // namespace moe
 

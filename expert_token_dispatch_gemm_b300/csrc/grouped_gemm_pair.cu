@@ -17,8 +17,8 @@
 // the same 64 intermediate features; the epilogue pairs them through shared memory.
 //
 // Per CTA (192 threads, one CTA per SM, persistent over the tile list):
-//   warp 0      TMA producer: 128 x 64 weight tile + 128 x 64 token tile per stage,
-//               128-byte swizzle, 6-stage ring. Both CTAs' copies complete on the even
+//   warp 0      TMA producer: 128 x 64 weight tile + (N/2, rounded up to 16, 32, 64 or
+//               128) x 64 token tile per stage, 128-byte swizzle, 6-stage ring. Both CTAs' copies complete on the even
 //               CTA's full barrier, which the even CTA arms with the pair's bytes.
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) in both
 //               CTAs; in the even CTA one thread issues the pair MMAs and commits them
@@ -40,19 +40,9 @@ constexpr int PM = 256;                 // weight rows per tile (the pair's M)
 constexpr int CM = PM / 2;              // weight rows per CTA
 constexpr int PN = 256;                 // max tokens per tile (the MMA's N)
 constexpr int CN = PN / 2;              // token rows staged per CTA (TMA box height)
-#ifndef MOE_PAIR_STAGES
-#define MOE_PAIR_STAGES 6
-#endif
-#ifndef MOE_PAIR_PREFETCH_KB
-#define MOE_PAIR_PREFETCH_KB 0
-#endif
-constexpr int STAGES = MOE_PAIR_STAGES;
-// Weight k-blocks requested into L2 ahead of the staged loads by the first token tile of
-// each weight tile (0: none). The ring alone covers ~STAGES k-blocks of DRAM latency.
-constexpr int PREFETCH_KB = MOE_PAIR_PREFETCH_KB;
+constexpr int STAGES = 6;
 constexpr uint32_t A_BYTES = CM * BK * 2;
 constexpr uint32_t B_BYTES = CN * BK * 2;
-constexpr uint32_t PAIR_TX = 2 * (A_BYTES + B_BYTES);
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * PN;
 constexpr int CHUNK = 32;               // token columns per epilogue step
@@ -60,6 +50,16 @@ constexpr int GU_FEATS = kGateUpBlock;  // intermediate features per CTA in gate
 static_assert(2 * GU_FEATS == CM, "a CTA's weight rows are one gate/up block");
 
 enum { EPI_SWIGLU = 0, EPI_DOWN = 1 };
+
+// Weight map (box 128 rows) and token maps with box heights 16, 32, 64 and 128 rows:
+// a tile stages only the token rows its MMA reads (N/2 per CTA).
+struct PairMaps {
+    CUtensorMap w;
+    CUtensorMap t[4];
+};
+__host__ __device__ constexpr int token_box_index(int half_rows) {
+    return half_rows <= 16 ? 0 : half_rows <= 32 ? 1 : half_rows <= 64 ? 2 : 3;
+}
 
 struct PairParams {
     const int32_t *expert_offsets;
@@ -81,8 +81,8 @@ struct Smem {
     static constexpr uint32_t b_off = STAGES * A_BYTES;
     static constexpr uint32_t epi_off = b_off + STAGES * B_BYTES;      // 16 KB staging
     static constexpr uint32_t epi_bytes = 2 * CHUNK * GU_FEATS * 4;
-    static constexpr uint32_t pairs_off = epi_off + epi_bytes;        // [CHUNK] int + [CHUNK] float
-    static constexpr uint32_t bar_off = pairs_off + 2 * CHUNK * 4;
+    static constexpr uint32_t pairs_off = epi_off + epi_bytes;        // [PN] int + [PN] float
+    static constexpr uint32_t bar_off = pairs_off + 2 * PN * 4;
     static constexpr uint32_t misc_off = bar_off + 24 * 8;
     static constexpr uint32_t tables_off = misc_off + 16;
     static constexpr uint32_t end = tables_off + 2 * (kMaxExperts + 1) * 4;
@@ -108,8 +108,7 @@ __device__ __forceinline__ Tile tile_at(int t, const int *mtp, const int *eo, in
 
 template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                         const __grid_constant__ CUtensorMap tmap_t, const PairParams p) {
+grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const PairParams p) {
     extern __shared__ uint8_t smem_raw[];
     // The dynamic shared-memory base is the same in both CTAs, so is every offset below:
     // the pair MMA addresses both CTAs' tiles with the even CTA's descriptors.
@@ -132,10 +131,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     if (warp == 0) {
         build_tile_tables(p.expert_offsets, p.e_begin, p.ne, PN, eo, mtp);
-        if (lane == 0) {
-            tma_prefetch_desc(&tmap_w);
-            tma_prefetch_desc(&tmap_t);
-        }
+        if (lane < 5) tma_prefetch_desc(lane == 0 ? &maps.w : &maps.t[lane - 1]);
     } else if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
@@ -168,39 +164,23 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
             int stage = 0;
             uint32_t phase = 0, armed = 0, armed_parity = 0;
             bool ok = true;
-            const bool prefetch = PREFETCH_KB > 0 && p.num_kb > PREFETCH_KB;
-            int pf_tile = -1, pf_row = 0;
             for (int t = pair; ok && t < total; t += num_pairs) {
                 const Tile tl = tile_at(t, mtp, eo, p.ne, p.f_tiles);
                 const int w_row = (p.e_begin + tl.i) * p.a_rows_per_expert + tl.f * PM + cta * CM;
                 const int t_row = tl.tok0 + (int)cta * (tl.nmma >> 1);
+                const int bsel = token_box_index(tl.nmma >> 1);
+                const CUtensorMap *tmap_t = &maps.t[bsel];
+                const uint32_t tx = 2 * (A_BYTES + (uint32_t)(16 << bsel) * BK * 2);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (prefetch) {   // this CTA's weight rows PREFETCH_KB k-blocks ahead
-                        int tn = t, kn = kb + PREFETCH_KB;
-                        if (kn >= p.num_kb) {
-                            tn += num_pairs;
-                            kn -= p.num_kb;
-                        }
-                        if (tn < total) {
-                            if (tn != pf_tile) {
-                                const Tile nx = tile_at(tn, mtp, eo, p.ne, p.f_tiles);
-                                pf_row = nx.m == 0 ? (p.e_begin + nx.i) * p.a_rows_per_expert +
-                                                         nx.f * PM + cta * CM
-                                                   : -1;
-                                pf_tile = tn;
-                            }
-                            if (pf_row >= 0) tma_prefetch_l2(&tmap_w, kn * BK, pf_row);
-                        }
-                    }
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_s, p.status)) {
                         ok = false;
                         break;
                     }
-                    if (cta == 0) mbar_arrive_expect_tx(&full[stage], PAIR_TX);
+                    if (cta == 0) mbar_arrive_expect_tx(&full[stage], tx);
                     const uint32_t fb = full_even0 + stage * 8;
-                    tma_load_2d_pair(smem_u32(smem + Smem::a_off + stage * A_BYTES), &tmap_w, fb,
+                    tma_load_2d_pair(smem_u32(smem + Smem::a_off + stage * A_BYTES), &maps.w, fb,
                                      kb * BK, w_row);
-                    tma_load_2d_pair(smem_u32(smem + Smem::b_off + stage * B_BYTES), &tmap_t, fb,
+                    tma_load_2d_pair(smem_u32(smem + Smem::b_off + stage * B_BYTES), tmap_t, fb,
                                      kb * BK, t_row);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -270,13 +250,26 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const uint32_t tempty_even0 = mapa_shared(smem_u32(&tempty[0]), 0);
         float *stage_f = reinterpret_cast<float *>(smem + Smem::epi_off);
         __nv_bfloat16 *stage_h = reinterpret_cast<__nv_bfloat16 *>(smem + Smem::epi_off);
-        int *pair_s = reinterpret_cast<int *>(smem + Smem::pairs_off);
+        int *pair_s = reinterpret_cast<int *>(smem + Smem::pairs_off);      // [PN]
+        float *wgt_s = reinterpret_cast<float *>(pair_s + PN);              // [PN]
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = pair; t < total; t += num_pairs) {
             const Tile tl = tile_at(t, mtp, eo, p.ne, p.f_tiles);
+            if (EPI == EPI_DOWN) {
+                // pair id and routing weight of every token of the tile, loaded while
+                // the tile's MMAs run (the previous tile's readers passed a barrier)
+#pragma unroll 2
+                for (int j = etid; j < tl.nmma; j += 128) {
+                    const bool tv = j < tl.ntok;
+                    const int pr = tv ? p.perm[tl.tok0 + j] : -1;
+                    pair_s[j] = pr;
+                    wgt_s[j] = tv ? p.topk_w[pr] : 0.f;
+                }
+            }
             // tcgen05.ld is warp-collective and the epilogue warps share named
-            // barriers: all four leave together on abort
+            // barriers: all four leave together on abort (the vote is also the barrier
+            // after which the tile's pair ids are visible)
             const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_s, p.status);
             if (!epilogue_all(ok)) break;
             fence_after();
@@ -319,12 +312,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     }
                     epilogue_sync();
                 } else {
-                    // routing weight of the chunk's tokens, one per lane
-                    const bool tv = c + lane < tl.ntok;
-                    const int pr = tv ? p.perm[tl.tok0 + c + lane] : 0;
-                    const float w = tv ? p.topk_w[pr] : 0.f;
-                    if (q == 0) pair_s[lane] = tv ? pr : -1;
-                    const int f = q * 32 + lane;   // weight row of this CTA
+                    const float w = wgt_s[c + lane];   // routing weight of token c + lane
+                    const int f = q * 32 + lane;       // weight row of this CTA
 #pragma unroll
                     for (int j = 0; j < CHUNK; ++j)
                         stage_h[j * CM + f] = __float2bfloat16_rn(__shfl_sync(0xffffffffu, w, j) * v[j]);
@@ -335,7 +324,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     for (int s = 0; s < 4; ++s) {
                         const int item = etid + 128 * s;
                         const int j = item >> 4, f8 = (item & 15) * 8;
-                        const int prj = pair_s[j];
+                        const int prj = pair_s[c + j];
                         if (prj >= 0 && col0 + f8 < p.H)
                             *reinterpret_cast<uint4 *>(p.out_slots + (size_t)prj * p.H + col0 + f8) =
                                 *reinterpret_cast<const uint4 *>(stage_h + j * CM + f8);
@@ -361,10 +350,18 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
     }
 }
 
+cudaError_t make_maps(PairMaps *m, const void *w, uint64_t w_rows, uint64_t w_cols, uint64_t w_ld,
+                      const void *t, uint64_t t_rows, uint64_t t_cols, uint64_t t_ld) {
+    cudaError_t e = make_map(&m->w, w, w_rows, w_cols, w_ld, CM);
+    for (int b = 0; b < 4 && e == cudaSuccess; ++b)
+        e = make_map(&m->t[b], t, t_rows, t_cols, t_ld, 16u << b);
+    return e;
+}
+
 // Clusters of two that fit on the device at once (one CTA per SM), cached per kernel.
 template <int EPI>
-cudaError_t launch_pair(const CUtensorMap &mw, const CUtensorMap &mt, const PairParams &prm,
-                        int64_t max_tiles, cudaStream_t s) {
+cudaError_t launch_pair(const PairMaps &maps, const PairParams &prm, int64_t max_tiles,
+                        cudaStream_t s) {
     if (max_tiles <= 0) return cudaSuccess;
     auto kern = grouped_gemm_pair_kernel<EPI>;
     static int max_clusters = 0;
@@ -402,7 +399,7 @@ cudaError_t launch_pair(const CUtensorMap &mw, const CUtensorMap &mt, const Pair
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, mw, mt, prm);
+    return cudaLaunchKernelEx(&cfg, kern, maps, prm);
 }
 
 }  // namespace
@@ -411,10 +408,9 @@ cudaError_t launch_tc_gate_up(const LayerDims &d, const void *send, const int32_
                               int e_begin, int e_end, const void *packed, void *h,
                               int32_t *status, int /*num_sms*/, cudaStream_t s) {
     const int64_t rows = (int64_t)d.N * d.k;
-    CUtensorMap mw, mt;
-    cudaError_t e = make_map(&mw, packed, (uint64_t)d.E * 2 * d.Ipad, d.H, d.H, CM);
-    if (e != cudaSuccess) return e;
-    e = make_map(&mt, send, rows, d.H, d.H, CN);
+    PairMaps maps;
+    cudaError_t e = make_maps(&maps, packed, (uint64_t)d.E * 2 * d.Ipad, d.H, d.H, send, rows,
+                              d.H, d.H);
     if (e != cudaSuccess) return e;
     PairParams prm = {};
     prm.expert_offsets = expert_offsets;
@@ -428,7 +424,7 @@ cudaError_t launch_tc_gate_up(const LayerDims &d, const void *send, const int32_
     prm.H = d.H;
     prm.status = status;
     const int64_t max_tiles = (ceil_div64(rows, PN) + prm.ne) * prm.f_tiles;
-    return launch_pair<EPI_SWIGLU>(mw, mt, prm, max_tiles, s);
+    return launch_pair<EPI_SWIGLU>(maps, prm, max_tiles, s);
 }
 
 cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *expert_offsets,
@@ -436,10 +432,8 @@ cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *exp
                            const float *topk_w, void *out_slots, int32_t *status, int /*num_sms*/,
                            cudaStream_t s) {
     const int64_t rows = (int64_t)d.N * d.k;
-    CUtensorMap mw, mt;
-    cudaError_t e = make_map(&mw, w_down, (uint64_t)d.E * d.H, d.I, d.I, CM);
-    if (e != cudaSuccess) return e;
-    e = make_map(&mt, h, rows, d.I, d.Ipad, CN);
+    PairMaps maps;
+    cudaError_t e = make_maps(&maps, w_down, (uint64_t)d.E * d.H, d.I, d.I, h, rows, d.I, d.Ipad);
     if (e != cudaSuccess) return e;
     PairParams prm = {};
     prm.expert_offsets = expert_offsets;
@@ -454,7 +448,7 @@ cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *exp
     prm.H = d.H;
     prm.status = status;
     const int64_t max_tiles = (ceil_div64(rows, PN) + prm.ne) * prm.f_tiles;
-    return launch_pair<EPI_DOWN>(mw, mt, prm, max_tiles, s);
+    return launch_pair<EPI_DOWN>(maps, prm, max_tiles, s);
 }
 
 }  // namespace moe

@@ -107,7 +107,6 @@ struct Workspace {
     void *send;            // [N*k, H]
     void *h;               // [N*k, Ipad]
     void *slots;           // [N*k, H]
-    float *partials;       // [P, N, H] fp32 (mask-and-sum mode only)
     size_t bytes;
 };
 
@@ -136,8 +135,6 @@ Workspace carve(const LayerDims &d, int mode, void *base) {
     w.send = take(pairs * d.H * esize(d));
     w.h = take(pairs * d.Ipad * esize(d));
     w.slots = take(pairs * d.H * esize(d));
-    w.partials = (float *)(mode == MOE_MODE_MASK_SUM ? take((size_t)d.P * d.N * d.H * sizeof(float))
-                                                      : nullptr);
     w.bytes = off;
     return w;
 }
@@ -234,8 +231,7 @@ moe_status_t run_combine(const LayerDims &d, int mode, const void *slots, const 
     if (mode == MOE_MODE_DISPATCH) {
         MOE_CUDA(launch_combine(d, slots, slot_pos, out, s), "combine kernel");
     } else {
-        MOE_CUDA(launch_mask_partials(d, slots, idx, slot_pos, w.partials, s), "mask partials kernel");
-        MOE_CUDA(launch_partition_sum(d, w.partials, out, s), "partition sum kernel");
+        MOE_CUDA(launch_mask_sum(d, slots, idx, slot_pos, out, s), "mask-and-sum kernel");
     }
     return MOE_OK;
 }
@@ -476,20 +472,14 @@ moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void 
     MOE_MARK(MOE_STAGE_PERMUTE);
     MOE_CUDA(launch_permute(d, x, slot_pos, w.send, s), "permute kernel");
     MOE_MARK(MOE_STAGE_GATE_UP);
-    if (cfg->mode == MOE_MODE_DISPATCH) {
-        st = run_gate_up(d, w.send, eoff, 0, d.E, w_gate_up_packed, w, s);
-        if (st != MOE_OK) return st;
-        MOE_MARK(MOE_STAGE_DOWN);
-        st = run_down(d, eoff, 0, d.E, w_down, perm, tw, w.slots, w, s);
-        if (st != MOE_OK) return st;
-    } else {   // each partition runs its own experts, as the ep_size ranks would
-        const int per = d.E / d.P;
-        for (int p = 0; p < d.P && st == MOE_OK; ++p)
-            st = run_experts(d, w.send, eoff, p * per, (p + 1) * per, w_gate_up_packed, w_down, perm,
-                             tw, w.slots, w, s);
-        if (st != MOE_OK) return st;
-        MOE_MARK(MOE_STAGE_DOWN);
-    }
+    // Both forward rules run every partition's experts in one launch per GEMM: an
+    // expert's rows never share a tile with another expert's, so its outputs are the
+    // same as if its partition ran it alone.
+    st = run_gate_up(d, w.send, eoff, 0, d.E, w_gate_up_packed, w, s);
+    if (st != MOE_OK) return st;
+    MOE_MARK(MOE_STAGE_DOWN);
+    st = run_down(d, eoff, 0, d.E, w_down, perm, tw, w.slots, w, s);
+    if (st != MOE_OK) return st;
     MOE_MARK(MOE_STAGE_COMBINE);
     st = run_combine(d, cfg->mode, w.slots, idx, slot_pos, out, w, s);
     if (st != MOE_OK) return st;

@@ -101,16 +101,15 @@ typedef struct moe_config {
 
 /* Stage boundaries recorded by moe_layer_forward when moe_diagnostics.stage_events is
  * set: event i is recorded on the stream just before stage i is enqueued, event
- * MOE_NUM_STAGES after the last one. In mask-and-sum mode the per-partition expert
- * launches all fall in MOE_STAGE_GATE_UP and MOE_STAGE_DOWN is empty. */
+ * MOE_NUM_STAGES after the last one. */
 enum {
     MOE_STAGE_ROUTE = 0,     /* router + top-k + softmax + segment histogram: 1 kernel */
     MOE_STAGE_SCAN = 1,      /* counts, offsets, segment bases: 1 kernel */
     MOE_STAGE_ASSIGN = 2,    /* stable slot of every pair: 1 kernel */
     MOE_STAGE_PERMUTE = 3,   /* hidden-state rows into the send buffer: 1 kernel */
-    MOE_STAGE_GATE_UP = 4,   /* grouped GEMM gate/up + SwiGLU: 1 kernel (P in mask mode) */
+    MOE_STAGE_GATE_UP = 4,   /* grouped GEMM gate/up + SwiGLU: 1 kernel */
     MOE_STAGE_DOWN = 5,      /* grouped GEMM down + weighted un-permute: 1 kernel */
-    MOE_STAGE_COMBINE = 6,   /* slot sum (1 kernel) or partials + partition sum (2) */
+    MOE_STAGE_COMBINE = 6,   /* slot sum or masked partials + partition sum: 1 kernel */
     MOE_NUM_STAGES = 7
 };
 
@@ -253,7 +252,7 @@ moe_status_t moe_expert_ffn(const moe_config *cfg, const void *send,
  *                      out_slots[t*k + j] (already weighted).
  *   MOE_MODE_MASK_SUM: every partition p first forms its masked partial output
  *                      partial_p[t] = sum of token t's kept slots whose expert lives in
- *                      p (fp32, in the workspace), then out = partial_0 + ... +
+ *                      p (fp32, in slot order), then out = partial_0 + ... +
  *                      partial_{P-1} in partition order (the all-reduce of the
  *                      "ep_router" + "moe_tp_experts" rule).
  *   out_slots  [N*k, H] dtype; topk_idx, slot_pos [N*k] int32; out [N, H] dtype.
@@ -266,8 +265,9 @@ moe_status_t moe_combine(const moe_config *cfg, const void *out_slots,
 /*
  * The whole layer: route -> dispatch -> local experts -> combine, enqueued on `stream`
  * with no host synchronisation. Intermediates live in `workspace`; `diag` (may be
- * NULL) selects which of them are also written to caller buffers. In mask-and-sum
- * mode the experts run once per partition (ep_size launches), like ep_size ranks.
+ * NULL) selects which of them are also written to caller buffers. Both modes run all
+ * partitions' experts in one launch per GEMM (an expert's outputs do not depend on
+ * which launch computes them); they differ in the combine.
  *   x [N,H], w_router [E,H], b_router [E] or NULL, w_gate_up_packed, w_down [E,H,I],
  *   out [N,H] dtype.
  */

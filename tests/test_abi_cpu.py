@@ -88,15 +88,16 @@ def test_config_validation(moe, kw, status):
         assert moe.lib.moe_last_error().decode()
 
 
-def test_workspace_size_grows_with_tokens_and_mask_mode(moe):
+def test_workspace_size_grows_with_tokens_not_with_mode(moe):
     _, a = status_of(moe, cfg(moe, N=64))
     _, b = status_of(moe, cfg(moe, N=640))
     _, c = status_of(moe, cfg(moe, N=640, mode="mask_sum"))
-    assert a < b < c
+    assert a < b
     # the send buffer, h and out_slots alone need pairs * (2H + Ipad) * 2 bytes
     pairs = 640 * 2
     assert b >= pairs * (2 * 64 + 128) * 2
-    assert c - b >= 4 * 640 * 64 * 4
+    # mask-and-sum keeps each partition's partial in registers: no extra buffer
+    assert c == b
 
 
 def test_packed_size(moe):
