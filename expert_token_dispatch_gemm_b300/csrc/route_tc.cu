@@ -49,27 +49,24 @@ struct RouteParams {
     int32_t *status;         // or nullptr
 };
 
-// Sorted (descending) top-KMAX list in registers; empty slots have idx < 0. A new value
-// enters behind equal ones, so scanning experts in increasing id keeps ties ordered by
-// the lower id.
+// Sorted (descending) top-KMAX list in registers; empty slots have idx < 0 and rank
+// below everything. A candidate that beats the last entry replaces it and bubbles up
+// past strictly smaller entries only, so with experts scanned in increasing id, equal
+// logits stay ordered by the lower id.
 template <int KMAX>
-__device__ __forceinline__ void topk_insert(float (&val)[KMAX], int (&idx)[KMAX], float v, int e) {
+__device__ __forceinline__ void topk_push(float (&val)[KMAX], int (&idx)[KMAX], float v, int e) {
     if (!(v > val[KMAX - 1] || idx[KMAX - 1] < 0)) return;
+    val[KMAX - 1] = v;
+    idx[KMAX - 1] = e;
 #pragma unroll
     for (int j = KMAX - 1; j > 0; --j) {
-        const bool beat_prev = v > val[j - 1] || idx[j - 1] < 0;
-        const bool beat_cur = v > val[j] || idx[j] < 0;
-        if (beat_prev) {
-            val[j] = val[j - 1];
-            idx[j] = idx[j - 1];
-        } else if (beat_cur) {
-            val[j] = v;
-            idx[j] = e;
-        }
-    }
-    if (v > val[0] || idx[0] < 0) {
-        val[0] = v;
-        idx[0] = e;
+        const bool up = val[j] > val[j - 1] || idx[j - 1] < 0;
+        const float hv = up ? val[j] : val[j - 1], lv = up ? val[j - 1] : val[j];
+        const int hi = up ? idx[j] : idx[j - 1], li = up ? idx[j - 1] : idx[j];
+        val[j - 1] = hv;
+        val[j] = lv;
+        idx[j - 1] = hi;
+        idx[j] = li;
     }
 }
 
@@ -244,7 +241,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     const int e = c + j;
                     if (e < p.E) {
                         const float l = v[j] + bias_s[e];
-                        topk_insert<KMAX>(val, idx, isnan(l) ? -INFINITY : l, e);
+                        topk_push<KMAX>(val, idx, isnan(l) ? -INFINITY : l, e);
                     }
                 }
             }
@@ -368,7 +365,12 @@ cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_rou
     prm.seg_hist = seg_hist;
     prm.status = status;
     const int tiles = ceil_div(d.N, BM);
+    // the register list holds k rounded up to a power of two
+    if (d.k <= 1) return launch_route_tc<1>(mx, mw, prm, tiles, num_sms, s);
+    if (d.k <= 2) return launch_route_tc<2>(mx, mw, prm, tiles, num_sms, s);
+    if (d.k <= 4) return launch_route_tc<4>(mx, mw, prm, tiles, num_sms, s);
     if (d.k <= 8) return launch_route_tc<8>(mx, mw, prm, tiles, num_sms, s);
+    if (d.k <= 16) return launch_route_tc<16>(mx, mw, prm, tiles, num_sms, s);
     return launch_route_tc<32>(mx, mw, prm, tiles, num_sms, s);
 }
 

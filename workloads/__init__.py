@@ -81,7 +81,13 @@ ALL_SHAPES = (PR1_FP32, GPTOSS, E8_TOP2, SKEWED_CAP, DECODE)
 GPTOSS_PROFILE = LayerShape("gptoss_profile_n1024_h2880_e16_k4", N=1024, H=2880, I=2880,
                             E=16, top_k=4, ep_size=8)
 
-BY_NAME = {s.name: s for s in ALL_SHAPES + (GPTOSS_PROFILE,)}
+# The gpt-oss router (8192 tokens x 2880, 128 experts, top-4) in front of small experts
+# (intermediate 128): under 1 GB on the device, for profiler captures of the routing and
+# dispatch kernels at their full gpt-oss size.
+ROUTE_PROFILE = LayerShape("route_profile_n8192_h2880_e128_k4", N=8192, H=2880, I=128,
+                           E=128, top_k=4, ep_size=8)
+
+BY_NAME = {s.name: s for s in ALL_SHAPES + (GPTOSS_PROFILE, ROUTE_PROFILE)}
 
 
 def _gen(seed: int, tensor_id: int, device, sub: int = 0) -> torch.Generator:
