@@ -364,7 +364,12 @@ cudaError_t launch_pair(const PairMaps &maps, const PairParams &prm, int64_t max
                         cudaStream_t s) {
     if (max_tiles <= 0) return cudaSuccess;
     auto kern = grouped_gemm_pair_kernel<EPI>;
-    static int max_clusters = 0;
+    static int max_clusters_dev[64] = {};   // per device
+    int dev = 0;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return de;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int &max_clusters = max_clusters_dev[dev];
     if (max_clusters == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)Smem::alloc);

@@ -5,20 +5,26 @@
 // the lower expert id), applies the softmax over the k chosen logits and adds the
 // token's experts to the per-segment histogram that the dispatch scan consumes.
 //
-// Per CTA (one per SM, 192 threads, persistent over 128-token tiles):
-//   warp 0      TMA producer: 128x64 x tile + E x 64 router tile per stage, 128-byte
-//               swizzle, 4-stage ring guarded by full/empty mbarriers;
-//   warp 1      allocates 512 TMEM columns (two accumulators) and one thread issues
+// One CTA per 128-token tile. The top-k runs over column slices: with SLICES groups of
+// four epilogue warps, group g selects each token's top-k among its slice of the experts
+// and group 0 merges the other groups' lists in expert order, which keeps the ordering
+// (value descending, ties to the lower id).
+//
+// Per CTA (64 + 128 * SLICES threads, one tile):
+//   warp 0      TMA producer: 128x64 x tile + round16(E) x 64 router tile per stage,
+//               128-byte swizzle, 3-stage ring guarded by full/empty mbarriers;
+//   warp 1      allocates TMEM (round16(E) columns, at least 32) and one thread issues
 //               tcgen05.mma (M=128, N=round16(E), K=16, bf16 in, fp32 acc);
-//   warps 2..5  epilogue: tcgen05.ld of the logits of their TMEM lane quarter, top-k,
-//               softmax, histogram; the accumulator is released as soon as the logits
-//               are in registers, so MMA and epilogue overlap.
+//   warps 2..   epilogue: tcgen05.ld of the logits of their TMEM lane quarter and
+//               column slice, top-k, merge, softmax and histogram.
 // Exactness: bf16 products are exact in fp32 and, for inputs on the dyadic grids of the
 // exact test variant, every partial sum is too, so the chosen ids do not depend on the
 // order in which the tensor cores accumulate.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
-// MOE_DEV_TIMEOUT in the status word, stops issuing work, waits (bounded) for its own
-// copies and MMAs in flight, frees TMEM and returns.
+// MOE_DEV_TIMEOUT in the status word, skips the remaining work, waits (bounded) for its
+// own copies, frees TMEM and returns.
+#include <mutex>
+
 #include "sm100.cuh"
 
 namespace moe {
@@ -26,14 +32,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = kTcBlockM;   // 128
-constexpr int BN = 256;         // accumulator columns reserved per tile (E <= 256)
-constexpr int STAGES = 4;
+constexpr int BM = kTcBlockM;   // 128 tokens per tile
+constexpr int STAGES = 3;
 constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
-constexpr uint32_t TMEM_COLS = 2 * BN;
 static_assert(BM == 2 * kSegTokens, "a route tile covers two histogram segments");
 
 struct RouteParams {
@@ -41,6 +42,7 @@ struct RouteParams {
     int bn;                  // MMA N (E rounded up to 16)
     uint32_t idesc;
     int num_kb;              // K blocks of BK
+    uint32_t tmem_cols;
     int E, k, nseg;
     const float *bias;       // [E] or nullptr
     int32_t *route_idx;      // [N, k] out
@@ -49,10 +51,21 @@ struct RouteParams {
     int32_t *status;         // or nullptr
 };
 
-// Sorted (descending) top-KMAX list in registers; empty slots have idx < 0 and rank
-// below everything. A candidate that beats the last entry replaces it and bubbles up
-// past strictly smaller entries only, so with experts scanned in increasing id, equal
-// logits stay ordered by the lower id.
+// Shared-memory layout for a given MMA N.
+struct RouteSmem {
+    uint32_t b_off, bar_off, misc_off, bias_off, hist_off, alloc;
+};
+__host__ __device__ inline RouteSmem route_smem(int bn, int E) {
+    RouteSmem m;
+    m.b_off = STAGES * A_BYTES;
+    m.bar_off = m.b_off + STAGES * (uint32_t)bn * BK * 2;
+    m.misc_off = m.bar_off + 16 * 8;
+    m.bias_off = m.misc_off + 16;
+    m.hist_off = m.bias_off + (uint32_t)(E + 3) / 4 * 16;
+    m.alloc = m.hist_off + 2 * (uint32_t)E * 4 + 1024;   // + slack to align the base
+    return m;
+}
+
 template <int KMAX>
 __device__ __forceinline__ void topk_push(float (&val)[KMAX], int (&idx)[KMAX], float v, int e) {
     if (!(v > val[KMAX - 1] || idx[KMAX - 1] < 0)) return;
@@ -70,36 +83,26 @@ __device__ __forceinline__ void topk_push(float (&val)[KMAX], int (&idx)[KMAX], 
     }
 }
 
-struct SmemLayout {
-    static constexpr uint32_t a_off = 0;
-    static constexpr uint32_t b_off = STAGES * A_BYTES;
-    static constexpr uint32_t bar_off = STAGES * STAGE_BYTES;
-    static constexpr uint32_t misc_off = bar_off + 16 * 8;
-    static constexpr uint32_t bias_off = misc_off + 16;
-    static constexpr uint32_t hist_off = bias_off + kMaxExperts * 4;
-    static constexpr uint32_t end = hist_off + 2 * kMaxExperts * 4;
-    static constexpr uint32_t alloc = end + 1024;   // slack to align the base to 1024
-};
-
-template <int KMAX>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int KMAX, int SLICES>
+__global__ void __launch_bounds__(64 + 128 * SLICES, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w, const RouteParams p) {
+    constexpr int NT = 128 * SLICES;   // epilogue threads
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SmemLayout::bar_off);
+    const RouteSmem L = route_smem(p.bn, p.E);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     uint64_t *full = bars;                  // [STAGES]
     uint64_t *empty = bars + STAGES;        // [STAGES]
-    uint64_t *tfull = bars + 2 * STAGES;    // [2]
-    uint64_t *tempty = tfull + 2;           // [2]
-    uint64_t *mma_done = tempty + 2;        // [1]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayout::misc_off);
-    volatile int *abort_s = reinterpret_cast<volatile int *>(smem + SmemLayout::misc_off + 4);
-    float *bias_s = reinterpret_cast<float *>(smem + SmemLayout::bias_off);
-    int *hist_s = reinterpret_cast<int *>(smem + SmemLayout::hist_off);   // [2][E]
+    uint64_t *tfull = bars + 2 * STAGES;    // [1]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.misc_off);
+    volatile int *abort_s = reinterpret_cast<volatile int *>(smem + L.misc_off + 4);
+    float *bias_s = reinterpret_cast<float *>(smem + L.bias_off);
+    int *hist_s = reinterpret_cast<int *>(smem + L.hist_off);   // [2][E]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int tile = blockIdx.x;
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tmap_x);
@@ -108,21 +111,18 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     } else if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS)
+                     "r"(p.tmem_cols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     } else if (warp == 3) {
         for (int e = lane; e < p.E; e += 32) bias_s[e] = p.bias != nullptr ? p.bias[e] : 0.f;
+        for (int e = lane; e < 2 * p.E; e += 32) hist_s[e] = 0;
     } else if (warp == 2 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 128);
-        }
-        mbar_init(mma_done, 1);
+        mbar_init(tfull, 1);
         *abort_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -130,31 +130,24 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = (p.rows + BM - 1) / BM;
 
     if (warp == 0) {
         if (lane == 0) {   // ------------------------------------------ TMA producer
             int stage = 0;
             uint32_t phase = 0, armed = 0, armed_parity = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_s, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], A_BYTES + (uint32_t)p.bn * BK * 2);
-                    const uint32_t fb = smem_u32(&full[stage]);
-                    tma_load_2d(smem_u32(smem + SmemLayout::a_off + stage * A_BYTES), &tmap_x, fb,
-                                kb * BK, tile * BM);
-                    tma_load_2d(smem_u32(smem + SmemLayout::b_off + stage * B_BYTES), &tmap_w, fb,
-                                kb * BK, 0);
-                    armed |= 1u << stage;
-                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+            const uint32_t tx = A_BYTES + (uint32_t)p.bn * BK * 2;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_s, p.status)) break;
+                mbar_arrive_expect_tx(&full[stage], tx);
+                const uint32_t fb = smem_u32(&full[stage]);
+                tma_load_2d(smem_u32(smem + stage * A_BYTES), &tmap_x, fb, kb * BK, tile * BM);
+                tma_load_2d(smem_u32(smem + L.b_off + stage * (uint32_t)p.bn * BK * 2), &tmap_w,
+                            fb, kb * BK, 0);
+                armed |= 1u << stage;
+                armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
             // no copy may still be landing when the CTA exits
@@ -168,72 +161,47 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         if (lane == 0) {   // ------------------------------------------ MMA issuer
             int stage = 0;
             uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
-            bool issued = false, ok = true;
-            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_s, p.status)) break;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                if (!mbar_wait(&full[stage], phase, abort_s, p.status)) break;
                 fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_s, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    fence_after();
-                    const uint32_t a_addr = smem_u32(smem + SmemLayout::a_off + stage * A_BYTES);
-                    const uint32_t b_addr = smem_u32(smem + SmemLayout::b_off + stage * B_BYTES);
+                const uint32_t a_addr = smem_u32(smem + stage * A_BYTES);
+                const uint32_t b_addr = smem_u32(smem + L.b_off + stage * (uint32_t)p.bn * BK * 2);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32),
-                                 smem_desc_sw128(b_addr + kk * 32), p.idesc, (kb | kk) != 0);
-                    issued = true;
-                    commit(&empty[stage]);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                commit(&tfull[acc]);
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1u;
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_bf16(tmem_base, smem_desc_sw128(a_addr + kk * 32),
+                             smem_desc_sw128(b_addr + kk * 32), p.idesc, (kb | kk) != 0);
+                commit(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            if (issued) {   // every MMA done before TMEM is freed
-                commit(mma_done);
-                volatile int no_abort = 0;
-                mbar_wait(mma_done, 0, &no_abort, p.status);
-            }
+            // the accumulator is final (after a timeout: every issued MMA is done, and
+            // the epilogue sees the abort flag)
+            commit(tfull);
         }
     } else {   // ------------------------------------------------------ epilogue
-        const int q = warp & 3;           // TMEM lane quarter this warp may access
-        const int r = q * 32 + lane;      // accumulator row = token of the tile
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        const int etid = threadIdx.x - 64;   // 0..127 across the epilogue warps
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            // previous tile's histogram is flushed; clear it
-            epilogue_sync();
-            for (int j = etid; j < 2 * p.E; j += 128) hist_s[j] = 0;
-            epilogue_sync();
-            // tcgen05.ld is warp-collective and the epilogue warps share named
-            // barriers: all four leave together on abort
-            const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_s, p.status);
-            if (!epilogue_all(ok)) break;
-            fence_after();
-            const int tok = tile * BM + r;
-            const bool valid = tok < p.rows;
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            float val[KMAX];
-            int idx[KMAX];
+        const int q = warp & 3;                // TMEM lane quarter
+        const int slice = (warp - 2) >> 2;     // column slice of the experts
+        const int r = q * 32 + lane;           // accumulator row = token of the tile
+        const int tok = tile * BM + r;
+        const int etid = threadIdx.x - 64;     // 0 .. NT-1
+        // tcgen05.ld is warp-collective and the epilogue warps share named barriers:
+        // all of them decide together
+        const bool ok = epilogue_all<NT>(mbar_wait(tfull, 0, abort_s, p.status) && *abort_s == 0);
+        fence_after();
+        float val[KMAX];
+        int idx[KMAX];
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                val[j] = -INFINITY;
-                idx[j] = -1;
-            }
-            for (int c = 0; c < p.bn; c += 32) {
+        for (int j = 0; j < KMAX; ++j) {
+            val[j] = -INFINITY;
+            idx[j] = -1;
+        }
+        if (ok) {
+            const int cps = (p.bn + 32 * SLICES - 1) / (32 * SLICES) * 32;   // columns per slice
+            const int c1 = min(p.bn, (slice + 1) * cps);
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
+            for (int c = slice * cps; c < c1; c += 32) {
                 float v[32];
                 tmem_ld32(taddr + c, v);
 #pragma unroll
@@ -245,9 +213,27 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     }
                 }
             }
-            fence_before();
-            mbar_arrive(&tempty[acc]);   // logits are in registers: free the accumulator
-            if (valid) {
+            if (SLICES > 1) {
+                // lists of slices 1.. into the stage ring (every MMA has read it), then
+                // group 0 pushes them in slice order, i.e. in increasing expert id
+                float *lv = reinterpret_cast<float *>(smem);   // [SLICES-1][BM][KMAX]
+                int *li = reinterpret_cast<int *>(lv + (SLICES - 1) * BM * KMAX);
+                if (slice > 0)
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j) {
+                        lv[((slice - 1) * BM + r) * KMAX + j] = val[j];
+                        li[((slice - 1) * BM + r) * KMAX + j] = idx[j];
+                    }
+                epilogue_sync<NT>();
+                if (slice == 0)
+                    for (int g = 0; g < SLICES - 1; ++g)
+#pragma unroll
+                        for (int j = 0; j < KMAX; ++j) {
+                            const int e = li[(g * BM + r) * KMAX + j];
+                            if (e >= 0) topk_push<KMAX>(val, idx, lv[(g * BM + r) * KMAX + j], e);
+                        }
+            }
+            if (slice == 0 && tok < p.rows) {
                 float ex[KMAX], sum = 0.f;
 #pragma unroll
                 for (int j = 0; j < KMAX; ++j) {
@@ -264,15 +250,11 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     }
             }
             if (p.seg_hist != nullptr) {
-                epilogue_sync();
-                for (int j = etid; j < 2 * p.E; j += 128) {
+                epilogue_sync<NT>();
+                for (int j = etid; j < 2 * p.E; j += NT) {
                     const int seg = 2 * tile + j / p.E;
                     if (seg < p.nseg) p.seg_hist[(size_t)seg * p.E + j % p.E] = hist_s[j];
                 }
-            }
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1u;
             }
         }
     }
@@ -282,26 +264,49 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     if (warp == 1) {
         fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(TMEM_COLS)
+                     "r"(p.tmem_cols)
                      : "memory");
     }
 }
 
-template <int KMAX>
+template <int KMAX, int SLICES>
 cudaError_t launch_route_tc(const CUtensorMap &mx, const CUtensorMap &mw, const RouteParams &prm,
-                            int tiles, int num_sms, cudaStream_t s) {
-    if (tiles <= 0) return cudaSuccess;
-    auto kern = route_tc_kernel<KMAX>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SmemLayout::alloc);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
+                            int tiles, cudaStream_t s) {
+    auto kern = route_tc_kernel<KMAX, SLICES>;
+    const RouteSmem L = route_smem(prm.bn, prm.E);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        // the dynamic shared-memory limit, per device, only ever grows
+        static std::mutex mu;
+        static uint32_t attr_max[64] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        if (L.alloc > attr_max[dev]) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)L.alloc);
+            if (e != cudaSuccess) return e;
+            attr_max[dev] = L.alloc;
+        }
     }
-    const int grid = tiles < num_sms ? tiles : num_sms;
-    kern<<<grid, NUM_THREADS, SmemLayout::alloc, s>>>(mx, mw, prm);
+    kern<<<tiles, 64 + 128 * SLICES, L.alloc, s>>>(mx, mw, prm);
     return cudaGetLastError();
+}
+
+// Four column slices while one CTA per SM covers every tile, two otherwise (two CTAs of
+// 320 threads fit on an SM); lists longer than 8 are not sliced.
+template <int KMAX>
+cudaError_t launch_route_k(const CUtensorMap &mx, const CUtensorMap &mw, const RouteParams &prm,
+                           int tiles, int num_sms, cudaStream_t s) {
+    if (tiles <= 0) return cudaSuccess;
+    if constexpr (KMAX > 8) {
+        (void)num_sms;
+        return launch_route_tc<KMAX, 1>(mx, mw, prm, tiles, s);
+    } else {
+        if (tiles <= num_sms) return launch_route_tc<KMAX, 4>(mx, mw, prm, tiles, s);
+        return launch_route_tc<KMAX, 2>(mx, mw, prm, tiles, s);
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -356,6 +361,8 @@ cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_rou
     prm.bn = bn;
     prm.idesc = make_idesc(BM, bn);
     prm.num_kb = ceil_div(d.H, BK);
+    prm.tmem_cols = 32;
+    while ((int)prm.tmem_cols < bn) prm.tmem_cols <<= 1;
     prm.E = d.E;
     prm.k = d.k;
     prm.nseg = ceil_div(d.N, kSegTokens);
@@ -366,12 +373,12 @@ cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_rou
     prm.status = status;
     const int tiles = ceil_div(d.N, BM);
     // the register list holds k rounded up to a power of two
-    if (d.k <= 1) return launch_route_tc<1>(mx, mw, prm, tiles, num_sms, s);
-    if (d.k <= 2) return launch_route_tc<2>(mx, mw, prm, tiles, num_sms, s);
-    if (d.k <= 4) return launch_route_tc<4>(mx, mw, prm, tiles, num_sms, s);
-    if (d.k <= 8) return launch_route_tc<8>(mx, mw, prm, tiles, num_sms, s);
-    if (d.k <= 16) return launch_route_tc<16>(mx, mw, prm, tiles, num_sms, s);
-    return launch_route_tc<32>(mx, mw, prm, tiles, num_sms, s);
+    if (d.k <= 1) return launch_route_k<1>(mx, mw, prm, tiles, num_sms, s);
+    if (d.k <= 2) return launch_route_k<2>(mx, mw, prm, tiles, num_sms, s);
+    if (d.k <= 4) return launch_route_k<4>(mx, mw, prm, tiles, num_sms, s);
+    if (d.k <= 8) return launch_route_k<8>(mx, mw, prm, tiles, num_sms, s);
+    if (d.k <= 16) return launch_route_k<16>(mx, mw, prm, tiles, num_sms, s);
+    return launch_route_k<32>(mx, mw, prm, tiles, num_sms, s);
 }
 
 }  // namespace moe

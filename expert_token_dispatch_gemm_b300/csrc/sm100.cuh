@@ -204,22 +204,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Barrier over the 128 epilogue threads (named barrier 1) that also returns whether
-// `ok` holds in all of them, so the four warps leave a tile loop together.
+// Barrier over the NT epilogue threads (named barrier 1) that also returns whether `ok`
+// holds in all of them, so the epilogue warps leave a tile loop together.
+template <int NT = 128>
 __device__ __forceinline__ bool epilogue_all(bool ok) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)ok)
+        : "r"((uint32_t)ok), "n"(NT)
         : "memory");
     return r != 0;
 }
-// Barrier among the 128 epilogue threads only.
-__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier among the NT epilogue threads only.
+template <int NT = 128>
+__device__ __forceinline__ void epilogue_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 // silu with the approximate divide: for g below about -87 the denominator overflows to

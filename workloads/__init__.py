@@ -87,7 +87,11 @@ GPTOSS_PROFILE = LayerShape("gptoss_profile_n1024_h2880_e16_k4", N=1024, H=2880,
 ROUTE_PROFILE = LayerShape("route_profile_n8192_h2880_e128_k4", N=8192, H=2880, I=128,
                            E=128, top_k=4, ep_size=8)
 
-BY_NAME = {s.name: s for s in ALL_SHAPES + (GPTOSS_PROFILE, ROUTE_PROFILE)}
+# The decode router (128 tokens) in front of the same small experts.
+ROUTE_PROFILE_DECODE = LayerShape("route_profile_n128_h2880_e128_k4", N=128, H=2880, I=128,
+                                  E=128, top_k=4, ep_size=8)
+
+BY_NAME = {s.name: s for s in ALL_SHAPES + (GPTOSS_PROFILE, ROUTE_PROFILE, ROUTE_PROFILE_DECODE)}
 
 
 def _gen(seed: int, tensor_id: int, device, sub: int = 0) -> torch.Generator:
