@@ -19,6 +19,7 @@ of the same workload, extrapolated to the whole batch.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -90,6 +91,33 @@ def roofline_entry(work, ms, peaks, source, dtype):
     if tf and work["flops"]:
         out["tensor_frac"] = round(work["flops"] / t / 1e12 / tf, 4)
     return out
+
+
+# ------------------------------------------------------------------ measured DRAM traffic
+TRAFFIC_SOURCES = ("grouped_gemm_pair.cu", "sm100.cuh", "common.cuh")
+
+
+def gemm_sources_sha256():
+    """Hash of the grouped-GEMM sources: a traffic record holds only for this code."""
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "expert_token_dispatch_gemm_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload, kernel):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu record of
+    this workload, or None when there is none or the kernel has changed since."""
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm_pair_traffic_{workload}.json")
+    if kernel not in ("gate_up", "down") or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("sources_sha256") != gemm_sources_sha256():
+        return None
+    b = rec["per_launch_bytes"][kernel]
+    return int(b["dram_read"]) + int(b["dram_write"])
 
 
 # ------------------------------------------------------------------ clocks
@@ -419,7 +447,7 @@ def main():
     peaks, source = load_peaks()
     dom = max(("gate_up", "down", "route", "permute", "combine"), key=lambda n: stage_ms[n])
     roof = roofline_entry(work[dom], stage_ms[dom], peaks, source, shape.dtype)
-    roof = dict(kernel=dom, **roof, traffic=None)
+    roof = dict(kernel=dom, **roof, traffic=measured_traffic(shape.name, dom))
     per_stage = {n: dict(ms=round(stage_ms[n], 4),
                          **{k: v for k, v in roofline_entry(work[n], max(stage_ms[n], 1e-6),
                                                             peaks, source, shape.dtype).items()
