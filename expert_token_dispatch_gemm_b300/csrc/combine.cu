@@ -16,11 +16,15 @@
 namespace moe {
 namespace {
 
+// Each lane sums two 16-byte vectors of the token's row per step and issues the loads
+// of up to four slots for both before adding, so eight loads are in flight per lane;
+// the adds still run in slot order.
 template <typename T>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T *__restrict__ slots, const int32_t *__restrict__ slot_pos, int N, int k,
                int H, T *__restrict__ out) {
     using V = Vec16<T>;
+    constexpr int KU = 4, VU = 2;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int t = blockIdx.x * 8 + warp;
     if (t >= N) return;
@@ -28,18 +32,39 @@ combine_kernel(const T *__restrict__ slots, const int32_t *__restrict__ slot_pos
     const int nvec = H / V::N;
     const uint4 *src = reinterpret_cast<const uint4 *>(slots + (size_t)t * k * H);
     uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)t * H);
-    for (int v = lane; v < nvec; v += 32) {
-        float acc[V::N];
+    for (int v0 = lane; v0 < nvec; v0 += 32 * VU) {
+        float acc[VU][V::N];
 #pragma unroll
-        for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            if (!((kept >> j) & 1u)) continue;
-            float f[V::N];
-            V::to_float(__ldg(src + (size_t)j * nvec + v), f);
+        for (int w = 0; w < VU; ++w)
 #pragma unroll
-            for (int i = 0; i < V::N; ++i) acc[i] += f[i];
+            for (int i = 0; i < V::N; ++i) acc[w][i] = 0.f;
+        for (int j0 = 0; j0 < k; j0 += KU) {
+            uint4 r[KU][VU];
+#pragma unroll
+            for (int u = 0; u < KU; ++u)
+#pragma unroll
+                for (int w = 0; w < VU; ++w) {
+                    const int j = j0 + u, v = v0 + 32 * w;
+                    r[u][w] = (j < k && ((kept >> j) & 1u) && v < nvec)
+                                  ? __ldg(src + (size_t)j * nvec + v)
+                                  : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+            for (int u = 0; u < KU; ++u) {
+                const int j = j0 + u;
+                if (j < k && ((kept >> j) & 1u))
+#pragma unroll
+                    for (int w = 0; w < VU; ++w) {
+                        float f[V::N];
+                        V::to_float(r[u][w], f);
+#pragma unroll
+                        for (int i = 0; i < V::N; ++i) acc[w][i] += f[i];
+                    }
+            }
         }
-        dst[v] = V::from_float(acc);
+#pragma unroll
+        for (int w = 0; w < VU; ++w)
+            if (v0 + 32 * w < nvec) dst[v0 + 32 * w] = V::from_float(acc[w]);
     }
 }
 
@@ -63,6 +88,45 @@ mask_sum_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
     const int nvec = H / V::N;
     const uint4 *src = reinterpret_cast<const uint4 *>(slots + (size_t)t * k * H);
     uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)t * H);
+    const unsigned live = __ballot_sync(0xffffffffu, owner >= 0);
+    if (k <= 8) {
+        // every kept slot of a vector is loaded before the ordered partition sums
+        int own[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) own[j] = __shfl_sync(0xffffffffu, owner, j);
+        for (int v = lane; v < nvec; v += 32) {
+            uint4 r[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                r[j] = (j < k && own[j] >= 0) ? __ldg(src + (size_t)j * nvec + v) : make_uint4(0, 0, 0, 0);
+            float acc[V::N];
+#pragma unroll
+            for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
+            unsigned todo = live & ((1u << k) - 1u);
+            while (todo) {
+                int pmin = 0x7fffffff;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if ((todo >> j) & 1u) pmin = own[j] < pmin ? own[j] : pmin;
+                float part[V::N];
+#pragma unroll
+                for (int i = 0; i < V::N; ++i) part[i] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (((todo >> j) & 1u) && own[j] == pmin) {
+                        float f[V::N];
+                        V::to_float(r[j], f);
+#pragma unroll
+                        for (int i = 0; i < V::N; ++i) part[i] += f[i];
+                        todo &= ~(1u << j);
+                    }
+#pragma unroll
+                for (int i = 0; i < V::N; ++i) acc[i] += part[i];
+            }
+            dst[v] = V::from_float(acc);
+        }
+        return;
+    }
     for (int v = lane; v < nvec; v += 32) {
         float acc[V::N];
 #pragma unroll
