@@ -23,6 +23,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T *__restrict__ slots, const int32_t *__restrict__ slot_pos, int N, int k,
                int H, T *__restrict__ out) {
+    grid_dep_wait();
+    grid_dep_trigger();
     using V = Vec16<T>;
     constexpr int KU = 4, VU = 2;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -76,6 +78,8 @@ __global__ void __launch_bounds__(256)
 mask_sum_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
                 const int32_t *__restrict__ slot_pos, int N, int k, int H, int E, int P,
                 T *__restrict__ out) {
+    grid_dep_wait();
+    grid_dep_trigger();
     using V = Vec16<T>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int t = blockIdx.x * 8 + warp;
@@ -189,25 +193,22 @@ cudaError_t launch_combine(const LayerDims &d, const void *out_slots, const int3
                            void *out, cudaStream_t s) {
     const int grid = ceil_div(d.N, 8);
     if (d.dtype == MOE_DTYPE_BF16)
-        combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            (const __nv_bfloat16 *)out_slots, slot_pos, d.N, d.k, d.H, (__nv_bfloat16 *)out);
-    else
-        combine_kernel<float><<<grid, 256, 0, s>>>((const float *)out_slots, slot_pos, d.N, d.k,
-                                                   d.H, (float *)out);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s,
+                          (const __nv_bfloat16 *)out_slots, slot_pos, d.N, d.k, d.H,
+                          (__nv_bfloat16 *)out);
+    return launch_pdl(combine_kernel<float>, dim3(grid), dim3(256), 0, s, (const float *)out_slots,
+                      slot_pos, d.N, d.k, d.H, (float *)out);
 }
 
 cudaError_t launch_mask_sum(const LayerDims &d, const void *out_slots, const int32_t *topk_idx,
                             const int32_t *slot_pos, void *out, cudaStream_t s) {
     const int grid = ceil_div(d.N, 8);
     if (d.dtype == MOE_DTYPE_BF16)
-        mask_sum_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            (const __nv_bfloat16 *)out_slots, topk_idx, slot_pos, d.N, d.k, d.H, d.E, d.P,
-            (__nv_bfloat16 *)out);
-    else
-        mask_sum_kernel<float><<<grid, 256, 0, s>>>((const float *)out_slots, topk_idx, slot_pos,
-                                                    d.N, d.k, d.H, d.E, d.P, (float *)out);
-    return cudaGetLastError();
+        return launch_pdl(mask_sum_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s,
+                          (const __nv_bfloat16 *)out_slots, topk_idx, slot_pos, d.N, d.k, d.H, d.E,
+                          d.P, (__nv_bfloat16 *)out);
+    return launch_pdl(mask_sum_kernel<float>, dim3(grid), dim3(256), 0, s, (const float *)out_slots,
+                      topk_idx, slot_pos, d.N, d.k, d.H, d.E, d.P, (float *)out);
 }
 
 cudaError_t launch_pack_gate_up(const LayerDims &d, const void *w_gate, const void *w_up,

@@ -72,6 +72,34 @@ template <> struct Vec16<float> {
 };
 
 // ----------------------------------------------------------------------------------
+// Programmatic dependent launch. Every kernel of the forward is launched so that it may
+// start while the kernel before it in the stream finishes: it waits for that grid (and
+// its memory) before its first access to global memory, then lets the next grid launch.
+// Setup that touches no global memory (TMEM allocation, barrier initialisation) runs
+// before the wait, overlapping the previous kernel's tail.
+// ----------------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
+// ----------------------------------------------------------------------------------
 // Internal launchers (host side). Each returns the cudaError_t of its launch(es).
 // ----------------------------------------------------------------------------------
 struct LayerDims {

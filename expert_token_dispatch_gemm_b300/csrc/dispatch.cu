@@ -26,6 +26,8 @@ constexpr int kScanThreads = 1024;
 
 __global__ void histogram_kernel(const int32_t *__restrict__ idx, int N, int k, int E,
                                  int32_t *__restrict__ seg_hist, int32_t *status) {
+    grid_dep_wait();
+    grid_dep_trigger();
     __shared__ int hs[kMaxExperts];
     for (int e = threadIdx.x; e < E; e += blockDim.x) hs[e] = 0;
     __syncthreads();
@@ -49,6 +51,8 @@ scan_kernel(const int32_t *__restrict__ seg_hist, int nseg, int E, int P, int ca
             int32_t *__restrict__ seg_base, int32_t *__restrict__ routed_counts,
             int32_t *__restrict__ counts, int32_t *__restrict__ expert_offsets,
             int32_t *__restrict__ part_offsets) {
+    grid_dep_wait();
+    grid_dep_trigger();
     __shared__ int part[kScanThreads];        // [G][E] chunk sums, then exclusive bases
     __shared__ int kept_s[kMaxExperts + 1];
     const int tid = threadIdx.x;
@@ -103,6 +107,8 @@ __global__ void __launch_bounds__(256)
 assign_kernel(const int32_t *__restrict__ idx, int N, int k, int E, int capacity,
               const int32_t *__restrict__ seg_base, const int32_t *__restrict__ expert_offsets,
               int32_t *__restrict__ slot_pos, int32_t *__restrict__ perm, int32_t *status) {
+    grid_dep_wait();
+    grid_dep_trigger();
     __shared__ int base_s[8][kMaxExperts];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int seg = blockIdx.x * 8 + warp;
@@ -145,6 +151,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 permute_kernel(const T *__restrict__ x, int N, int H, int k, const int32_t *__restrict__ slot_pos,
                T *__restrict__ send) {
+    grid_dep_wait();
+    grid_dep_trigger();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int t = blockIdx.x * 8 + warp;
     if (t >= N) return;
@@ -176,38 +184,34 @@ permute_kernel(const T *__restrict__ x, int N, int H, int k, const int32_t *__re
 cudaError_t launch_histogram(const LayerDims &d, const int32_t *topk_idx, int32_t *seg_hist,
                              int32_t *status, cudaStream_t s) {
     const int nseg = ceil_div(d.N, kSegTokens);
-    histogram_kernel<<<nseg, 256, 0, s>>>(topk_idx, d.N, d.k, d.E, seg_hist, status);
-    return cudaGetLastError();
+    return launch_pdl(histogram_kernel, dim3(nseg), dim3(256), 0, s, topk_idx, d.N, d.k, d.E,
+                      seg_hist, status);
 }
 
 cudaError_t launch_scan(const LayerDims &d, const int32_t *seg_hist, int32_t *seg_base,
                         int32_t *routed_counts, int32_t *counts, int32_t *expert_offsets,
                         int32_t *part_offsets, cudaStream_t s) {
     const int nseg = ceil_div(d.N, kSegTokens);
-    scan_kernel<<<1, kScanThreads, 0, s>>>(seg_hist, nseg, d.E, d.P, d.capacity, seg_base,
-                                           routed_counts, counts, expert_offsets, part_offsets);
-    return cudaGetLastError();
+    return launch_pdl(scan_kernel, dim3(1), dim3(kScanThreads), 0, s, seg_hist, nseg, d.E, d.P,
+                      d.capacity, seg_base, routed_counts, counts, expert_offsets, part_offsets);
 }
 
 cudaError_t launch_assign(const LayerDims &d, const int32_t *topk_idx, const int32_t *seg_base,
                           const int32_t *expert_offsets, int32_t *slot_pos, int32_t *perm,
                           int32_t *status, cudaStream_t s) {
     const int nseg = ceil_div(d.N, kSegTokens);
-    assign_kernel<<<ceil_div(nseg, 8), 256, 0, s>>>(topk_idx, d.N, d.k, d.E, d.capacity, seg_base,
-                                                    expert_offsets, slot_pos, perm, status);
-    return cudaGetLastError();
+    return launch_pdl(assign_kernel, dim3(ceil_div(nseg, 8)), dim3(256), 0, s, topk_idx, d.N, d.k,
+                      d.E, d.capacity, seg_base, expert_offsets, slot_pos, perm, status);
 }
 
 cudaError_t launch_permute(const LayerDims &d, const void *x, const int32_t *slot_pos,
                            void *send, cudaStream_t s) {
     const int grid = ceil_div(d.N, 8);
     if (d.dtype == MOE_DTYPE_BF16)
-        permute_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            (const __nv_bfloat16 *)x, d.N, d.H, d.k, slot_pos, (__nv_bfloat16 *)send);
-    else
-        permute_kernel<float><<<grid, 256, 0, s>>>((const float *)x, d.N, d.H, d.k, slot_pos,
-                                                   (float *)send);
-    return cudaGetLastError();
+        return launch_pdl(permute_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s,
+                          (const __nv_bfloat16 *)x, d.N, d.H, d.k, slot_pos, (__nv_bfloat16 *)send);
+    return launch_pdl(permute_kernel<float>, dim3(grid), dim3(256), 0, s, (const float *)x, d.N, d.H,
+                      d.k, slot_pos, (float *)send);
 }
 
 }  // namespace moe

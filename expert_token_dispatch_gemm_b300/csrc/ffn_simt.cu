@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(256)
 simt_gate_up_kernel(const float *__restrict__ send, const int32_t *__restrict__ eoff, int e_begin,
                     int ne, const float *__restrict__ packed, int H, int Ipad,
                     float *__restrict__ hbuf) {
+    grid_dep_wait();
+    grid_dep_trigger();
     __shared__ int eo[kMaxExperts + 1], mtp[kMaxExperts + 1];
     __shared__ __align__(16) float As[SBK][SBM + 4];
     __shared__ __align__(16) float Gs[SBK][SBN + 4];
@@ -94,6 +96,8 @@ simt_down_kernel(const float *__restrict__ hbuf, int Ipad, int I, const int32_t 
                  int e_begin, int ne, const float *__restrict__ wd, int H,
                  const int32_t *__restrict__ perm, const float *__restrict__ topk_w,
                  float *__restrict__ slots) {
+    grid_dep_wait();
+    grid_dep_trigger();
     __shared__ int eo[kMaxExperts + 1], mtp[kMaxExperts + 1];
     __shared__ __align__(16) float As[SBK][SBM + 4];
     __shared__ __align__(16) float Bs[SBK][SBN + 4];
@@ -157,8 +161,8 @@ cudaError_t launch_simt_gate_up(const LayerDims &d, const float *send,
     const int ne = e_end - e_begin;
     const int grid = simt_grid(d, ne, d.Ipad / SBN);
     if (grid <= 0) return cudaSuccess;
-    simt_gate_up_kernel<<<grid, 256, 0, s>>>(send, expert_offsets, e_begin, ne, packed, d.H, d.Ipad, h);
-    return cudaGetLastError();
+    return launch_pdl(simt_gate_up_kernel, dim3(grid), dim3(256), 0, s, send, expert_offsets, e_begin,
+                      ne, packed, d.H, d.Ipad, h);
 }
 
 cudaError_t launch_simt_down(const LayerDims &d, const float *h, const int32_t *expert_offsets,
@@ -167,9 +171,8 @@ cudaError_t launch_simt_down(const LayerDims &d, const float *h, const int32_t *
     const int ne = e_end - e_begin;
     const int grid = simt_grid(d, ne, ceil_div(d.H, SBN));
     if (grid <= 0) return cudaSuccess;
-    simt_down_kernel<<<grid, 256, 0, s>>>(h, d.Ipad, d.I, expert_offsets, e_begin, ne, w_down, d.H,
-                                          perm, topk_w, out_slots);
-    return cudaGetLastError();
+    return launch_pdl(simt_down_kernel, dim3(grid), dim3(256), 0, s, h, d.Ipad, d.I, expert_offsets,
+                      e_begin, ne, w_down, d.H, perm, topk_w, out_slots);
 }
 
 }  // namespace moe

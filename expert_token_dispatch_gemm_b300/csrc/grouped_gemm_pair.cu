@@ -130,7 +130,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const PairParams
     const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
 
     if (warp == 0) {
-        build_tile_tables(p.expert_offsets, p.e_begin, p.ne, PN, eo, mtp);
         if (lane < 5) tma_prefetch_desc(lane == 0 ? &maps.w : &maps.t[lane - 1]);
     } else if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -151,6 +150,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const PairParams
         *abort_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    grid_dep_wait();   // the previous kernel's writes are visible from here on
+    grid_dep_trigger();
+    if (warp == 0) build_tile_tables(p.expert_offsets, p.e_begin, p.ne, PN, eo, mtp);
     fence_before();
     __syncthreads();
     cluster_sync_all();   // both CTAs' barriers exist before any cross-CTA signal
@@ -393,17 +395,19 @@ cudaError_t launch_pair(const PairMaps &maps, const PairParams &prm, int64_t max
     }
     const int clusters = (int)std::min<int64_t>(max_tiles, max_clusters);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = Smem::alloc;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, maps, prm);
 }
 

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__restrict__ bias,
              int N, int H, int E, int k, int32_t *__restrict__ topk_idx,
              float *__restrict__ topk_w, int32_t *__restrict__ seg_hist) {
+    grid_dep_wait();
+    grid_dep_trigger();
     constexpr int TB = kSegTokens;
     constexpr int KC = kRouteKChunk;
     constexpr int EP = RE * EG;               // experts padded to the thread layout
@@ -159,8 +161,8 @@ cudaError_t launch_route_t(const LayerDims &d, const T *x, const T *wr, const fl
         if (e != cudaSuccess) return e;
     }
     const int grid = ceil_div(d.N, kSegTokens);
-    kern<<<grid, kRouteThreads, smem, s>>>(x, wr, b, d.N, d.H, d.E, d.k, idx, w, hist);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kRouteThreads), smem, s, x, wr, b, d.N, d.H, d.E, d.k,
+                      idx, w, hist);
 }
 
 template <typename T>

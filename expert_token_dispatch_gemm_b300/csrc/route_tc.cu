@@ -114,9 +114,6 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                      "r"(p.tmem_cols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    } else if (warp == 3) {
-        for (int e = lane; e < p.E; e += 32) bias_s[e] = p.bias != nullptr ? p.bias[e] : 0.f;
-        for (int e = lane; e < 2 * p.E; e += 32) hist_s[e] = 0;
     } else if (warp == 2 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -125,6 +122,12 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         mbar_init(tfull, 1);
         *abort_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    grid_dep_wait();   // the previous kernel's writes are visible from here on
+    grid_dep_trigger();
+    if (warp == 3) {
+        for (int e = lane; e < p.E; e += 32) bias_s[e] = p.bias != nullptr ? p.bias[e] : 0.f;
+        for (int e = lane; e < 2 * p.E; e += 32) hist_s[e] = 0;
     }
     fence_before();
     __syncthreads();
@@ -290,8 +293,7 @@ cudaError_t launch_route_tc(const CUtensorMap &mx, const CUtensorMap &mw, const 
             attr_max[dev] = L.alloc;
         }
     }
-    kern<<<tiles, 64 + 128 * SLICES, L.alloc, s>>>(mx, mw, prm);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(tiles), dim3(64 + 128 * SLICES), L.alloc, s, mx, mw, prm);
 }
 
 // Four column slices while one CTA per SM covers every tile, two otherwise (two CTAs of
