@@ -8,5 +8,6 @@ from .moe import (  # noqa: F401
     router_logits, top_k_experts, routing_weights, route,
     expert_partition, load_counts, expert_capacity, dispatch_layout, permute,
     silu, swiglu_expert, expert_outputs, combine_dispatch, combine_mask_sum,
-    layer_forward, token_outputs,
+    layer_forward, token_outputs, selection_scores, group_limited_top_k, route_variant,
+    update_selection_bias,
 )

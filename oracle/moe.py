@@ -76,6 +76,66 @@ def route(x, w_router, b_router, k):
     return logits, idx, routing_weights(logits, idx)
 
 
+# ---------------------------------------------------------------- routing variants
+def selection_scores(logits, selection_bias=None):
+    """[UL-EP] "Load balancing and capacity", bias-based balancing: DeepSeek-V3 adds a
+    per-expert bias to the router scores that only influences which experts are chosen.
+    s[t, e] = logits[t, e] + beta[e]; the routing weights stay a softmax over the chosen
+    experts' own logits (routing_weights(logits, idx))."""
+    s = _f64(logits)
+    if selection_bias is not None:
+        s = s + _f64(selection_bias)[None, :]
+    return s
+
+
+def group_limited_top_k(scores, k, ep_size, group_limit):
+    """[UL-EP] "Load balancing and capacity", last paragraph: DeepSeek-V3 sends each
+    token to experts on at most 4 of its 8 nodes. Here the nodes are the ep_size
+    partitions. The pages give no rule for which partitions; reading: a partition's score
+    is the best score among its experts, the group_limit best partitions are kept (equal
+    scores: lower partition id), and the k best experts inside them are chosen (equal
+    scores: lower expert id). None or group_limit >= ep_size is plain top-k.
+    Ordering key per token: (expert's partition is kept, score, -expert id), descending."""
+    s = _f64(scores)
+    N, E = s.shape
+    if group_limit is None or group_limit >= ep_size:
+        return top_k_experts(s, k)
+    owner = expert_partition(np.arange(E), E, ep_size)
+    part_best = np.stack([s[:, owner == p].max(axis=1) for p in range(ep_size)], axis=1)
+    kept_parts = np.argsort(-part_best, axis=1, kind="stable")[:, :group_limit]
+    allowed_part = np.zeros((N, ep_size), dtype=bool)
+    allowed_part[np.arange(N)[:, None], kept_parts] = True
+    allowed = allowed_part[:, owner]
+    ids = np.broadcast_to(np.arange(E), (N, E))
+    order = np.lexsort((ids, -s, ~allowed), axis=-1)
+    return order[:, :k].astype(np.int64)
+
+
+def route_variant(x, w_router, b_router, k, selection_bias=None, ep_size=1,
+                  group_limit=None):
+    """Step 1 with the routing variants: selection on logits + selection_bias, optionally
+    limited to group_limit partitions; weights from the chosen experts' logits.
+    Returns (logits, topk_idx, topk_w)."""
+    logits = router_logits(x, w_router, b_router)
+    s = selection_scores(logits, selection_bias)
+    idx = group_limited_top_k(s, k, ep_size, group_limit)
+    return logits, idx, routing_weights(logits, idx)
+
+
+def update_selection_bias(selection_bias, routed_counts, num_tokens, k, gamma):
+    """[UL-EP] bias-based balancing: after each step the bias of an overloaded expert is
+    lowered and that of an idle one raised. Reading: overloaded / idle means above /
+    below the equal share N*k/E of the step's routed assignments, and the step is a fixed
+    gamma: beta_e - gamma, beta_e + gamma, or unchanged when the load equals the share.
+    The comparison is exact in integers (count * E against N * k) and the bias is kept
+    in float32, its storage type, so the update is computed in float32."""
+    b = np.asarray(selection_bias, dtype=np.float32)
+    c = np.asarray(routed_counts, dtype=np.int64)
+    diff = c * b.shape[0] - int(num_tokens) * int(k)
+    g = np.float32(gamma)
+    return np.where(diff > 0, b - g, np.where(diff < 0, b + g, b)).astype(np.float32)
+
+
 # ---------------------------------------------------------------- step 2: dispatch
 def expert_partition(expert, num_experts, ep_size):
     """[HF-EP] "How the sizes combine": ep_size splits the expert list into ep_size
@@ -231,14 +291,16 @@ def combine_mask_sum(y_send, slot_pos, topk_idx, topk_w, num_experts, ep_size):
 
 # ---------------------------------------------------------------- the whole layer
 def layer_forward(x, w_router, b_router, w_gate, w_up, w_down, top_k, ep_size,
-                  capacity_factor=None, mode="dispatch"):
+                  capacity_factor=None, mode="dispatch", selection_bias=None,
+                  group_limit=None):
     """Route -> dispatch -> local experts -> weighted combine, all in fp64.
     Returns a dict with every intermediate (logits, topk_idx, topk_w, the dispatch
     layout, send, y_send, out and, in mask mode, partials)."""
     x = _f64(x)
     N = x.shape[0]
     E = np.shape(w_router)[0]
-    logits, idx, w = route(x, w_router, b_router, top_k)
+    logits, idx, w = route_variant(x, w_router, b_router, top_k, selection_bias, ep_size,
+                                   group_limit)
     C = expert_capacity(capacity_factor, N, top_k, E)
     lay = dispatch_layout(idx, E, ep_size, C)
     send = permute(x, lay["perm"], top_k)

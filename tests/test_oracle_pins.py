@@ -39,22 +39,37 @@ def tiny_inputs(seed, N, H, I, E, grid=None, bias=True):
     return x, wr, b, wg, wu, wd
 
 
-def brute_force_layer(x, wr, b, wg, wu, wd, k, ep_size, capacity):
+def brute_force_layer(x, wr, b, wg, wu, wd, k, ep_size, capacity, sel_bias=None,
+                      group_limit=None):
     """Dense evaluation: every expert on every token, masked to the kept top-k.
     Written independently of the oracle: explicit subscripts, 'fewer than k experts
     beat it' selection, full softmax renormalised over the selection, capacity by
-    counting earlier tokens that selected the same expert."""
+    counting earlier tokens that selected the same expert. Routing variants: selection
+    on S = L + sel_bias (weights still from L); with a group limit M a partition is
+    eligible iff fewer than M partitions beat its best score, and an expert is selected
+    iff its partition is eligible and fewer than k eligible experts beat it."""
     N, H = x.shape
     E = wr.shape[0]
     L = np.einsum("th,eh->te", x, wr)
     if b is not None:
         L = L + b[None, :]
+    S = L if sel_bias is None else L + np.asarray(sel_bias, dtype=np.float64)[None, :]
+    owner = np.arange(E) // (E // ep_size)
+    eligible = np.ones((N, E), dtype=bool)
+    if group_limit is not None:
+        for t in range(N):
+            best = [max(S[t, e] for e in range(E) if owner[e] == p) for p in range(ep_size)]
+            for e in range(E):
+                p = owner[e]
+                beaten = sum(1 for q in range(ep_size)
+                             if best[q] > best[p] or (best[q] == best[p] and q < p))
+                eligible[t, e] = beaten < group_limit
     selected = np.zeros((N, E), dtype=bool)
     for t in range(N):
         for e in range(E):
-            beaten_by = sum(1 for e2 in range(E)
-                            if L[t, e2] > L[t, e] or (L[t, e2] == L[t, e] and e2 < e))
-            selected[t, e] = beaten_by < k
+            beaten_by = sum(1 for e2 in range(E) if eligible[t, e2] and
+                            (S[t, e2] > S[t, e] or (S[t, e2] == S[t, e] and e2 < e)))
+            selected[t, e] = eligible[t, e] and beaten_by < k
     full = scipy.special.softmax(L, axis=1)
     weight = np.where(selected, full, 0.0)
     weight = weight / weight.sum(axis=1, keepdims=True)
@@ -389,3 +404,150 @@ def test_planted_drop_order_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(om, "dispatch_layout", keep_last)
     res, bf = _oracle_with_bf((5, 7, 10, 7, 3, 1, 1, 0.01, None))
     assert rel_err(res["out"], bf["out"]) > 1e-6
+
+
+# ------------------------------------------------------------------ routing variants
+# [UL-EP] "Load balancing and capacity": a per-expert bias that only influences the
+# choice of experts, updated after each step; at most M partitions (nodes) per token.
+VARIANT_CASES = [
+    # case index into TINY_CASES, selection-bias scale, group limit
+    (0, 0.5, None), (1, 0.3, 2), (2, 0.25, 1), (3, 0.0, 3), (6, 1.0, 2), (7, 0.2, 1),
+]
+
+
+def _variant(case_i, scale, M, mode="dispatch"):
+    seed, N, H, I, E, k, P, cf, grid = TINY_CASES[case_i]
+    x, wr, b, wg, wu, wd = tiny_inputs(seed, N, H, I, E, grid)
+    rng = np.random.default_rng(100 + case_i)
+    beta = np.round(rng.uniform(-1, 1, E) * scale * 8) / 8     # dyadic: exact sums
+    if M is not None and M * (E // P) < k:
+        M = -(-k // (E // P))
+    res = oracle.layer_forward(x, wr, b, wg, wu, wd, k, P, cf, mode, selection_bias=beta,
+                               group_limit=M)
+    bf = brute_force_layer(x, wr, b, wg, wu, wd, k, P, res["capacity"], sel_bias=beta,
+                           group_limit=M)
+    return res, bf, dict(E=E, P=P, k=k, M=M, beta=beta, x=x, wr=wr, b=b)
+
+
+@pytest.mark.parametrize("mode", ["dispatch", "mask_sum"])
+@pytest.mark.parametrize("vc", VARIANT_CASES, ids=lambda v: f"case{v[0]}-s{v[1]}-M{v[2]}")
+def test_variant_oracle_equals_dense_brute_force(vc, mode):
+    res, bf, _ = _variant(*vc, mode=mode)
+    sel = np.zeros_like(bf["selected"])
+    np.put_along_axis(sel, res["topk_idx"], True, axis=1)
+    assert np.array_equal(sel, bf["selected"])
+    w = np.zeros(sel.shape)
+    np.put_along_axis(w, res["topk_idx"], res["topk_w"], axis=1)
+    assert rel_err(w, bf["weight"]) < 1e-12
+    assert rel_err(res["out"], bf["out"]) < 1e-12
+
+
+def test_zero_or_constant_selection_bias_is_plain_routing():
+    x, wr, b, *_ = tiny_inputs(3, 9, 8, 4, 8, grid=0.25)
+    _, idx0, w0 = oracle.route(x, wr, b, 3)
+    for beta in (np.zeros(8), np.full(8, 0.75)):
+        _, idx, w = oracle.route_variant(x, wr, b, 3, selection_bias=beta)
+        assert np.array_equal(idx, idx0) and np.array_equal(w, w0)
+
+
+def test_selection_bias_moves_the_choice_but_weights_use_raw_logits():
+    # two experts chosen out of three; a large bias on expert 2 forces it into every
+    # selection, and the pair's weights follow the logistic closed form of the RAW
+    # logits: w0 = 1 / (1 + exp(l1 - l0))
+    L = np.array([[2.0, 1.0, 0.0], [0.5, 3.0, -1.0], [1.0, 1.0, 1.0]])
+    beta = np.array([0.0, 0.0, 10.0])
+    idx = oracle.group_limited_top_k(oracle.selection_scores(L, beta), 2, 1, None)
+    assert idx.tolist() == [[2, 0], [2, 1], [2, 0]]
+    w = oracle.routing_weights(L, idx)
+    for t in range(3):
+        l0, l1 = L[t, idx[t, 0]], L[t, idx[t, 1]]
+        assert abs(w[t, 0] - 1.0 / (1.0 + math.exp(l1 - l0))) < 1e-15
+
+
+def test_group_limit_reduces_to_plain_top_k():
+    x, wr, b, *_ = tiny_inputs(2, 16, 12, 6, 6)
+    L = oracle.router_logits(x, wr, b)
+    plain = oracle.top_k_experts(L, 3)
+    assert np.array_equal(oracle.group_limited_top_k(L, 3, 3, 3), plain)
+    assert np.array_equal(oracle.group_limited_top_k(L, 3, 3, None), plain)
+    # tokens whose plain top-k already spans at most M partitions keep it
+    owner = plain // 2
+    spans = np.array([len(set(r)) for r in owner])
+    lim = oracle.group_limited_top_k(L, 3, 3, 2)
+    assert np.array_equal(lim[spans <= 2], plain[spans <= 2])
+    assert np.all([len(set(r)) <= 2 for r in lim // 2])
+
+
+def test_group_limit_one_keeps_the_argmax_partition():
+    rng = np.random.default_rng(7)
+    L = rng.standard_normal((40, 12))
+    idx = oracle.group_limited_top_k(L, 3, 4, 1)        # 4 partitions of 3 experts
+    for t in range(40):
+        p = int(np.argmax(L[t])) // 3
+        inside = list(range(3 * p, 3 * p + 3))
+        assert sorted(idx[t].tolist()) == sorted(inside)
+        assert idx[t].tolist() == sorted(inside, key=lambda e: (-L[t, e], e))
+
+
+def test_selection_bias_update_closed_form():
+    beta = np.array([0.5, -0.25, 0.0, 1.0], dtype=np.float32)
+    # N = 6 tokens, k = 2: equal share 3 per expert
+    new = oracle.update_selection_bias(beta, [5, 1, 3, 3], 6, 2, 0.125)
+    assert new.dtype == np.float32
+    assert new.tolist() == [0.375, -0.125, 0.0, 1.0]
+    same = oracle.update_selection_bias(beta, [3, 3, 3, 3], 6, 2, 0.125)
+    assert np.array_equal(same, beta)
+
+
+VARIANT_MUTANTS = ["weights_from_biased_scores", "partition_score_is_sum",
+                   "partition_ties_to_higher_id", "group_limit_ignored"]
+
+
+def _mutant(name):
+    real_w, real_g = om.routing_weights, om.group_limited_top_k
+    if name == "weights_from_biased_scores":
+        def route_variant(x, w_router, b_router, k, selection_bias=None, ep_size=1,
+                          group_limit=None):
+            logits = om.router_logits(x, w_router, b_router)
+            s = om.selection_scores(logits, selection_bias)
+            idx = real_g(s, k, ep_size, group_limit)
+            return logits, idx, real_w(s, idx)
+        return "route_variant", route_variant
+
+    def glt(scores, k, ep_size, group_limit):
+        s = np.asarray(scores, dtype=np.float64)
+        N, E = s.shape
+        if group_limit is None or group_limit >= ep_size:
+            return om.top_k_experts(s, k)
+        if name == "group_limit_ignored":
+            return om.top_k_experts(s, k)
+        owner = np.arange(E) // (E // ep_size)
+        red = (lambda a: a.sum(axis=1)) if name == "partition_score_is_sum" else (
+            lambda a: a.max(axis=1))
+        best = np.stack([red(s[:, owner == p]) for p in range(ep_size)], axis=1)
+        if name == "partition_ties_to_higher_id":
+            kept = np.argsort(-best[:, ::-1], axis=1, kind="stable")[:, :group_limit]
+            kept = ep_size - 1 - kept
+        else:
+            kept = np.argsort(-best, axis=1, kind="stable")[:, :group_limit]
+        allowed_part = np.zeros((N, ep_size), dtype=bool)
+        allowed_part[np.arange(N)[:, None], kept] = True
+        allowed = allowed_part[:, owner]
+        ids = np.broadcast_to(np.arange(E), (N, E))
+        return np.lexsort((ids, -s, ~allowed), axis=-1)[:, :k].astype(np.int64)
+    return "group_limited_top_k", glt
+
+
+@pytest.mark.parametrize("name", VARIANT_MUTANTS)
+def test_planted_variant_mistake_is_caught(name, monkeypatch):
+    fn, bad = _mutant(name)
+    monkeypatch.setattr(om, fn, bad)
+    caught = False
+    for vc in VARIANT_CASES + [(2, 0.0, 1), (6, 0.0, 1), (3, 0.0, 1)]:
+        res, bf, _ = _variant(*vc)
+        sel = np.zeros_like(bf["selected"])
+        np.put_along_axis(sel, res["topk_idx"], True, axis=1)
+        if not np.array_equal(sel, bf["selected"]) or rel_err(res["out"], bf["out"]) > 1e-12:
+            caught = True
+            break
+    assert caught, f"planted mistake {name} went unnoticed"
