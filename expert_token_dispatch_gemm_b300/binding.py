@@ -36,7 +36,8 @@ class MoeConfig(ctypes.Structure):
                 ("intermediate", ctypes.c_int64), ("num_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("ep_size", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("mode", ctypes.c_int32),
-                ("dtype", ctypes.c_int32), ("has_bias", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("has_bias", ctypes.c_int32),
+                ("group_limit", ctypes.c_int32), ("selection_bias", ctypes.c_void_p)]
 
     @property
     def torch_dtype(self):
@@ -68,6 +69,7 @@ def _load():
         "moe_packed_gate_up_size": (ctypes.c_int, [cfgp, ctypes.POINTER(S)]),
         "moe_pack_weights": (ctypes.c_int, [cfgp, P, P, P, P]),
         "moe_route": (ctypes.c_int, [cfgp, P, P, P, P, P, P]),
+        "moe_update_selection_bias": (ctypes.c_int, [cfgp, P, P, ctypes.c_float, P]),
         "moe_dispatch": (ctypes.c_int, [cfgp, P, P, P, P, P, P, P, P, P, P, S, P]),
         "moe_dispatch_noalloc": (ctypes.c_int, [cfgp, P, P, P, P, P, P, P, P, P, P]),
         "moe_expert_ffn": (ctypes.c_int, [cfgp, P, P, I32, I32, P, P, P, P, P, P, S, P]),
@@ -87,11 +89,16 @@ lib = _load()
 
 
 def config(N, H, I, E, top_k, ep_size, capacity_factor=None, mode="dispatch",
-           dtype="bf16", has_bias=False) -> MoeConfig:
+           dtype="bf16", has_bias=False, group_limit=0, selection_bias=None) -> MoeConfig:
+    """struct moe_config. selection_bias: None or an fp32 [E] CUDA tensor, which the
+    caller keeps alive while the config is in use."""
     return MoeConfig(int(N), int(H), int(I), int(E), int(top_k), int(ep_size),
                      float(capacity_factor) if capacity_factor else 0.0,
                      MOE_MODE_DISPATCH if mode == "dispatch" else MOE_MODE_MASK_SUM,
-                     MOE_DTYPE_BF16 if dtype == "bf16" else MOE_DTYPE_FP32, int(bool(has_bias)))
+                     MOE_DTYPE_BF16 if dtype == "bf16" else MOE_DTYPE_FP32, int(bool(has_bias)),
+                     int(group_limit or 0),
+                     None if selection_bias is None
+                     else _ptr(selection_bias, "selection_bias", torch.float32).value)
 
 
 def _check(status: int, func: str):
@@ -152,6 +159,14 @@ def moe_route(cfg, x, w_router, b_router, topk_idx, topk_w):
                          _ptr(b_router, "b_router", torch.float32),
                          _ptr(topk_idx, "topk_idx", torch.int32),
                          _ptr(topk_w, "topk_w", torch.float32), _stream()), "moe_route")
+
+
+def moe_update_selection_bias(cfg, routed_counts, selection_bias, gamma):
+    _check(lib.moe_update_selection_bias(ctypes.byref(cfg),
+                                         _ptr(routed_counts, "routed_counts", torch.int32),
+                                         _ptr(selection_bias, "selection_bias", torch.float32),
+                                         ctypes.c_float(gamma), _stream()),
+           "moe_update_selection_bias")
 
 
 def moe_dispatch(cfg, topk_idx, x, routed_counts, counts, expert_offsets, part_offsets, perm,

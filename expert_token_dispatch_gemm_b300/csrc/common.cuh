@@ -106,11 +106,19 @@ struct LayerDims {
     int N, H, I, Ipad, E, k, P;
     int capacity;      // INT32_MAX when unlimited
     int dtype;         // MOE_DTYPE_*
+    int group_limit;   // partitions a token may use; 0 when unlimited
+    const float *sel_bias;   // [E] selection-only bias or nullptr
 };
+// Largest group limit and partition count of the group-limited routing.
+constexpr int kMaxGroupLimit = 8;
+constexpr int kMaxGroupPartitions = 64;
 
 cudaError_t launch_route(const LayerDims &d, const void *x, const void *w_router,
                          const float *b_router, int32_t *topk_idx, float *topk_w,
                          int32_t *seg_hist /* [nseg, E] or nullptr */, cudaStream_t s);
+
+cudaError_t launch_update_selection_bias(const LayerDims &d, const int32_t *routed_counts,
+                                        float *selection_bias, float gamma, cudaStream_t s);
 
 cudaError_t launch_histogram(const LayerDims &d, const int32_t *topk_idx, int32_t *seg_hist,
                              int32_t *status, cudaStream_t s);

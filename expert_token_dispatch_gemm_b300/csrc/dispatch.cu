@@ -179,7 +179,28 @@ permute_kernel(const T *__restrict__ x, int N, int H, int k, const int32_t *__re
     }
 }
 
+// After-step update of the selection-only bias (Ultralytics glossary, "Load balancing
+// and capacity"): an expert above the equal share N*k/E of the step's routed pairs is
+// lowered by gamma, one below it raised, compared exactly as count*E against N*k.
+__global__ void __launch_bounds__(256)
+update_selection_bias_kernel(int E, long long share_num, const int32_t *__restrict__ counts,
+                             float *__restrict__ bias, float gamma) {
+    grid_dep_wait();
+    grid_dep_trigger();
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+        const long long diff = (long long)counts[e] * E - share_num;
+        const float b = bias[e];
+        bias[e] = diff > 0 ? __fsub_rn(b, gamma) : diff < 0 ? __fadd_rn(b, gamma) : b;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_update_selection_bias(const LayerDims &d, const int32_t *routed_counts,
+                                        float *selection_bias, float gamma, cudaStream_t s) {
+    return launch_pdl(update_selection_bias_kernel, dim3(1), dim3(256), 0, s, d.E,
+                      (long long)d.N * d.k, routed_counts, selection_bias, gamma);
+}
 
 cudaError_t launch_histogram(const LayerDims &d, const int32_t *topk_idx, int32_t *seg_hist,
                              int32_t *status, cudaStream_t s) {

@@ -76,6 +76,22 @@ moe_status_t check_config(const moe_config *cfg, LayerDims *d) {
     d->P = cfg->ep_size;
     d->dtype = cfg->dtype;
     d->capacity = INT_MAX;
+    if (cfg->group_limit < 0)
+        return fail(MOE_ERR_INVALID_ARG, "group_limit must be >= 0 (got %d)", cfg->group_limit);
+    d->group_limit = cfg->group_limit < cfg->ep_size ? cfg->group_limit : 0;
+    if (d->group_limit > 0) {
+        if ((int64_t)d->group_limit * (cfg->num_experts / cfg->ep_size) < cfg->top_k)
+            return fail(MOE_ERR_INVALID_ARG,
+                        "group_limit %d partitions of %d experts hold fewer than top_k = %d",
+                        d->group_limit, cfg->num_experts / cfg->ep_size, cfg->top_k);
+        if (d->group_limit > kMaxGroupLimit || cfg->ep_size > kMaxGroupPartitions)
+            return fail(MOE_ERR_UNSUPPORTED,
+                        "group-limited routing supports group_limit <= %d and ep_size <= %d",
+                        kMaxGroupLimit, kMaxGroupPartitions);
+    }
+    if (cfg->selection_bias != nullptr && (reinterpret_cast<uintptr_t>(cfg->selection_bias) & 3u))
+        return fail(MOE_ERR_INVALID_ARG, "selection_bias must be 4-byte aligned");
+    d->sel_bias = cfg->selection_bias;
     if (cfg->capacity_factor > 0.f) {
         // cf * N * k is exact in double (24-bit cf times an integer below 2^29); if the
         // exact quotient by E is an integer the division returns it exactly, otherwise it
@@ -334,6 +350,21 @@ moe_status_t moe_route(const moe_config *cfg, const void *x, const void *w_route
     g_last_error.clear();
     return run_route(d, x, w_router, cfg->has_bias ? b_router : nullptr, topk_idx, topk_w, nullptr,
                      nullptr, (cudaStream_t)stream);
+}
+
+moe_status_t moe_update_selection_bias(const moe_config *cfg, const int32_t *routed_counts,
+                                       float *selection_bias, float gamma, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    if (isnan(gamma) || isinf(gamma)) return fail(MOE_ERR_INVALID_ARG, "gamma must be finite");
+    NEED(routed_counts, false);
+    NEED(selection_bias, false);
+    g_last_error.clear();
+    MOE_CUDA(launch_update_selection_bias(d, routed_counts, selection_bias, gamma,
+                                          (cudaStream_t)stream),
+             "selection bias update kernel");
+    return MOE_OK;
 }
 
 moe_status_t moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x,

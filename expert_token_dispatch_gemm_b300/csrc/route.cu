@@ -23,8 +23,9 @@ constexpr int kRouteKChunk = 32;
 template <typename T, int RE, int EG>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__restrict__ bias,
-             int N, int H, int E, int k, int32_t *__restrict__ topk_idx,
-             float *__restrict__ topk_w, int32_t *__restrict__ seg_hist) {
+             const float *__restrict__ sel_bias, int group_limit, int P, int N, int H, int E,
+             int k, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+             int32_t *__restrict__ seg_hist) {
     grid_dep_wait();
     grid_dep_trigger();
     constexpr int TB = kSegTokens;
@@ -87,20 +88,69 @@ route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__r
         }
     __syncthreads();
 
-    // top-k: one warp per token
+    // top-k: one warp per token. Selection on logit + selection bias (a NaN ranks
+    // last), optionally among the experts of the group_limit best partitions; the
+    // weights are the softmax of the chosen experts' logits.
     constexpr int EPL = (EP + 31) / 32;
     const int warp = tid / 32, lane = tid % 32;
+    const int per_part = E / P;
     for (int tl = warp; tl < TB; tl += kRouteThreads / 32) {
         const int t = t0 + tl;
         if (t >= N) break;
-        float v[EPL];
+        float v[EPL], sv[EPL];
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
             const float l = (e < E) ? lg[tl * (EP + 1) + e] : -INFINITY;
-            v[i] = isnan(l) ? -INFINITY : l;   // a NaN logit ranks last
+            const float sc = (e < E && sel_bias != nullptr) ? l + sel_bias[e] : l;
+            v[i] = isnan(l) ? -INFINITY : l;
+            sv[i] = isnan(sc) ? -INFINITY : sc;
         }
         unsigned taken = 0;
+        if (group_limit > 0) {
+            // best selection score of partitions lane and lane + 32
+            float pb[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int pp = lane + 32 * h;
+                if (pp < P)
+                    for (int e = pp * per_part; e < (pp + 1) * per_part; ++e) {
+                        const float l = lg[tl * (EP + 1) + e];
+                        const float sc = sel_bias != nullptr ? l + sel_bias[e] : l;
+                        if (!isnan(sc)) pb[h] = fmaxf(pb[h], sc);
+                    }
+            }
+            // the group_limit best partitions (ties: lower id)
+            unsigned long long kept = 0;
+            for (int m = 0; m < group_limit; ++m) {
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int pp = lane + 32 * h;
+                    if (pp < P && !((kept >> pp) & 1ull) && (pb[h] > bv || (pb[h] == bv && pp < bi))) {
+                        bv = pb[h];
+                        bi = pp;
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                    if (ov > bv || (ov == bv && oi < bi)) {
+                        bv = ov;
+                        bi = oi;
+                    }
+                }
+                kept |= 1ull << bi;
+            }
+            // experts outside the kept partitions are never chosen
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && !((kept >> (e / per_part)) & 1ull)) taken |= 1u << i;
+            }
+        }
         float my_v = 0.f;
         int my_i = 0;
         for (int j = 0; j < k; ++j) {
@@ -109,8 +159,8 @@ route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__r
 #pragma unroll
             for (int i = 0; i < EPL; ++i) {
                 const int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-                    bv = v[i];
+                if (e < E && !((taken >> i) & 1u) && (sv[i] > bv || (sv[i] == bv && e < bi))) {
+                    bv = sv[i];
                     bi = e;
                 }
             }
@@ -123,14 +173,22 @@ route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__r
                     bi = oi;
                 }
             }
+            // the chosen expert's logit, from the lane that holds it
+            float bl = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (lane + 32 * i == bi) bl = v[i];
+            bl = __shfl_sync(0xffffffffu, bl, bi & 31);
             if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
             if (lane == j) {
-                my_v = bv;
+                my_v = bl;
                 my_i = bi;
             }
         }
-        // softmax over the chosen logits; slot 0 holds the largest
-        const float m = __shfl_sync(0xffffffffu, my_v, 0);
+        // softmax over the chosen experts' logits
+        float m = lane < k ? my_v : -INFINITY;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
         const float ex = (lane < k) ? expf(my_v - m) : 0.f;
         float sum = ex;
 #pragma unroll
@@ -161,8 +219,8 @@ cudaError_t launch_route_t(const LayerDims &d, const T *x, const T *wr, const fl
         if (e != cudaSuccess) return e;
     }
     const int grid = ceil_div(d.N, kSegTokens);
-    return launch_pdl(kern, dim3(grid), dim3(kRouteThreads), smem, s, x, wr, b, d.N, d.H, d.E, d.k,
-                      idx, w, hist);
+    return launch_pdl(kern, dim3(grid), dim3(kRouteThreads), smem, s, x, wr, b, d.sel_bias,
+                      d.group_limit, d.P, d.N, d.H, d.E, d.k, idx, w, hist);
 }
 
 template <typename T>

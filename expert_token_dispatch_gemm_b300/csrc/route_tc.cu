@@ -37,6 +37,11 @@ constexpr int STAGES = 3;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 static_assert(BM == 2 * kSegTokens, "a route tile covers two histogram segments");
 
+// Routing variants (template MODE): 0 plain top-k of the logits; 1 selection on
+// logits + selection bias, weights from the logits; 2 as 1 within the group_limit best
+// partitions (one column slice, two passes over the accumulator).
+enum { ROUTE_PLAIN = 0, ROUTE_SELBIAS = 1, ROUTE_GROUP = 2 };
+
 struct RouteParams {
     int rows;                // tokens
     int bn;                  // MMA N (E rounded up to 16)
@@ -45,6 +50,8 @@ struct RouteParams {
     uint32_t tmem_cols;
     int E, k, nseg;
     const float *bias;       // [E] or nullptr
+    const float *sel_bias;   // [E] or nullptr (selection only)
+    int group_limit, per_part;   // ROUTE_GROUP: partitions kept, experts per partition
     int32_t *route_idx;      // [N, k] out
     float *route_w;          // [N, k] out
     int32_t *seg_hist;       // [nseg, E] or nullptr
@@ -53,7 +60,7 @@ struct RouteParams {
 
 // Shared-memory layout for a given MMA N.
 struct RouteSmem {
-    uint32_t b_off, bar_off, misc_off, bias_off, hist_off, alloc;
+    uint32_t b_off, bar_off, misc_off, bias_off, sbias_off, hist_off, alloc;
 };
 __host__ __device__ inline RouteSmem route_smem(int bn, int E) {
     RouteSmem m;
@@ -61,7 +68,8 @@ __host__ __device__ inline RouteSmem route_smem(int bn, int E) {
     m.bar_off = m.b_off + STAGES * (uint32_t)bn * BK * 2;
     m.misc_off = m.bar_off + 16 * 8;
     m.bias_off = m.misc_off + 16;
-    m.hist_off = m.bias_off + (uint32_t)(E + 3) / 4 * 16;
+    m.sbias_off = m.bias_off + (uint32_t)(E + 3) / 4 * 16;
+    m.hist_off = m.sbias_off + (uint32_t)(E + 3) / 4 * 16;
     m.alloc = m.hist_off + 2 * (uint32_t)E * 4 + 1024;   // + slack to align the base
     return m;
 }
@@ -83,7 +91,31 @@ __device__ __forceinline__ void topk_push(float (&val)[KMAX], int (&idx)[KMAX], 
     }
 }
 
-template <int KMAX, int SLICES>
+// As topk_push, carrying each entry's raw logit along (the routing variants select on
+// logit + selection bias but weight by the logit).
+template <int KMAX>
+__device__ __forceinline__ void topk_push_raw(float (&val)[KMAX], float (&raw)[KMAX],
+                                              int (&idx)[KMAX], float v, float l, int e) {
+    if (!(v > val[KMAX - 1] || idx[KMAX - 1] < 0)) return;
+    val[KMAX - 1] = v;
+    raw[KMAX - 1] = l;
+    idx[KMAX - 1] = e;
+#pragma unroll
+    for (int j = KMAX - 1; j > 0; --j) {
+        const bool up = val[j] > val[j - 1] || idx[j - 1] < 0;
+        const float hv = up ? val[j] : val[j - 1], lv = up ? val[j - 1] : val[j];
+        const float hr = up ? raw[j] : raw[j - 1], lr = up ? raw[j - 1] : raw[j];
+        const int hi = up ? idx[j] : idx[j - 1], li = up ? idx[j - 1] : idx[j];
+        val[j - 1] = hv;
+        val[j] = lv;
+        raw[j - 1] = hr;
+        raw[j] = lr;
+        idx[j - 1] = hi;
+        idx[j] = li;
+    }
+}
+
+template <int KMAX, int SLICES, int MODE>
 __global__ void __launch_bounds__(64 + 128 * SLICES, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w, const RouteParams p) {
@@ -99,6 +131,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.misc_off);
     volatile int *abort_s = reinterpret_cast<volatile int *>(smem + L.misc_off + 4);
     float *bias_s = reinterpret_cast<float *>(smem + L.bias_off);
+    float *sbias_s = reinterpret_cast<float *>(smem + L.sbias_off);
     int *hist_s = reinterpret_cast<int *>(smem + L.hist_off);   // [2][E]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -126,7 +159,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     grid_dep_wait();   // the previous kernel's writes are visible from here on
     grid_dep_trigger();
     if (warp == 3) {
-        for (int e = lane; e < p.E; e += 32) bias_s[e] = p.bias != nullptr ? p.bias[e] : 0.f;
+        for (int e = lane; e < p.E; e += 32) {
+            bias_s[e] = p.bias != nullptr ? p.bias[e] : 0.f;
+            sbias_s[e] = p.sel_bias != nullptr ? p.sel_bias[e] : 0.f;
+        }
         for (int e = lane; e < 2 * p.E; e += 32) hist_s[e] = 0;
     }
     fence_before();
@@ -193,26 +229,83 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         // all of them decide together
         const bool ok = epilogue_all<NT>(mbar_wait(tfull, 0, abort_s, p.status) && *abort_s == 0);
         fence_after();
-        float val[KMAX];
+        float val[KMAX], raw[KMAX];   // raw: the entry's logit (MODE > ROUTE_PLAIN)
         int idx[KMAX];
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             val[j] = -INFINITY;
+            raw[j] = -INFINITY;
             idx[j] = -1;
         }
+        // a candidate: logit l = acc + bias, selection score l (+ selection bias); a NaN
+        // ranks last
+        auto push = [&](float acc, int e) {
+            const float l = acc + bias_s[e];
+            if (MODE == ROUTE_PLAIN) {
+                topk_push<KMAX>(val, idx, isnan(l) ? -INFINITY : l, e);
+            } else {
+                const float sc = l + sbias_s[e];
+                topk_push_raw<KMAX>(val, raw, idx, isnan(sc) ? -INFINITY : sc,
+                                    isnan(l) ? -INFINITY : l, e);
+            }
+        };
         if (ok) {
-            const int cps = (p.bn + 32 * SLICES - 1) / (32 * SLICES) * 32;   // columns per slice
-            const int c1 = min(p.bn, (slice + 1) * cps);
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
-            for (int c = slice * cps; c < c1; c += 32) {
-                float v[32];
-                tmem_ld32(taddr + c, v);
+            if (MODE == ROUTE_GROUP) {
+                // pass 1: every partition's best selection score, the best partitions
+                // in a list (pushed in increasing partition id: ties keep the lower)
+                float pv[kMaxGroupLimit];
+                int pi[kMaxGroupLimit];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int e = c + j;
-                    if (e < p.E) {
-                        const float l = v[j] + bias_s[e];
-                        topk_push<KMAX>(val, idx, isnan(l) ? -INFINITY : l, e);
+                for (int j = 0; j < kMaxGroupLimit; ++j) {
+                    pv[j] = -INFINITY;
+                    pi[j] = -1;
+                }
+                float cur = -INFINITY;
+                int cur_p = 0;
+                for (int c = 0; c < p.bn; c += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int e = c + j;
+                        if (e < p.E) {
+                            const int pp = e / p.per_part;
+                            if (pp != cur_p) {
+                                topk_push<kMaxGroupLimit>(pv, pi, cur, cur_p);
+                                cur = -INFINITY;
+                                cur_p = pp;
+                            }
+                            const float sc = v[j] + bias_s[e] + sbias_s[e];
+                            cur = isnan(sc) ? cur : fmaxf(cur, sc);
+                        }
+                    }
+                }
+                topk_push<kMaxGroupLimit>(pv, pi, cur, cur_p);
+                uint64_t allowed = 0;
+#pragma unroll
+                for (int j = 0; j < kMaxGroupLimit; ++j)
+                    if (j < p.group_limit && pi[j] >= 0) allowed |= 1ull << pi[j];
+                // pass 2: the top-k among the experts of the kept partitions
+                for (int c = 0; c < p.bn; c += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int e = c + j;
+                        if (e < p.E && ((allowed >> (e / p.per_part)) & 1ull)) push(v[j], e);
+                    }
+                }
+            } else {
+                const int cps = (p.bn + 32 * SLICES - 1) / (32 * SLICES) * 32;   // columns per slice
+                const int c1 = min(p.bn, (slice + 1) * cps);
+                for (int c = slice * cps; c < c1; c += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int e = c + j;
+                        if (e < p.E) push(v[j], e);
                     }
                 }
             }
@@ -220,11 +313,13 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 // lists of slices 1.. into the stage ring (every MMA has read it), then
                 // group 0 pushes them in slice order, i.e. in increasing expert id
                 float *lv = reinterpret_cast<float *>(smem);   // [SLICES-1][BM][KMAX]
-                int *li = reinterpret_cast<int *>(lv + (SLICES - 1) * BM * KMAX);
+                float *lr = lv + (SLICES - 1) * BM * KMAX;
+                int *li = reinterpret_cast<int *>(lr + (SLICES - 1) * BM * KMAX);
                 if (slice > 0)
 #pragma unroll
                     for (int j = 0; j < KMAX; ++j) {
                         lv[((slice - 1) * BM + r) * KMAX + j] = val[j];
+                        lr[((slice - 1) * BM + r) * KMAX + j] = raw[j];
                         li[((slice - 1) * BM + r) * KMAX + j] = idx[j];
                     }
                 epilogue_sync<NT>();
@@ -232,15 +327,26 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     for (int g = 0; g < SLICES - 1; ++g)
 #pragma unroll
                         for (int j = 0; j < KMAX; ++j) {
-                            const int e = li[(g * BM + r) * KMAX + j];
-                            if (e >= 0) topk_push<KMAX>(val, idx, lv[(g * BM + r) * KMAX + j], e);
+                            const int o = (g * BM + r) * KMAX + j;
+                            const int e = li[o];
+                            if (e < 0) continue;
+                            if (MODE == ROUTE_PLAIN)
+                                topk_push<KMAX>(val, idx, lv[o], e);
+                            else
+                                topk_push_raw<KMAX>(val, raw, idx, lv[o], lr[o], e);
                         }
             }
             if (slice == 0 && tok < p.rows) {
+                // softmax over the chosen experts' logits
+                const float *lg = MODE == ROUTE_PLAIN ? val : raw;
+                float m = lg[0];
+#pragma unroll
+                for (int j = 1; j < KMAX; ++j)
+                    if (j < p.k) m = fmaxf(m, lg[j]);
                 float ex[KMAX], sum = 0.f;
 #pragma unroll
                 for (int j = 0; j < KMAX; ++j) {
-                    ex[j] = j < p.k ? expf(val[j] - val[0]) : 0.f;
+                    ex[j] = j < p.k ? expf(lg[j] - m) : 0.f;
                     sum += ex[j];
                 }
                 const float inv = 1.0f / sum;
@@ -272,10 +378,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
 }
 
-template <int KMAX, int SLICES>
+template <int KMAX, int SLICES, int MODE>
 cudaError_t launch_route_tc(const CUtensorMap &mx, const CUtensorMap &mw, const RouteParams &prm,
                             int tiles, cudaStream_t s) {
-    auto kern = route_tc_kernel<KMAX, SLICES>;
+    auto kern = route_tc_kernel<KMAX, SLICES, MODE>;
     const RouteSmem L = route_smem(prm.bn, prm.E);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -302,12 +408,19 @@ template <int KMAX>
 cudaError_t launch_route_k(const CUtensorMap &mx, const CUtensorMap &mw, const RouteParams &prm,
                            int tiles, int num_sms, cudaStream_t s) {
     if (tiles <= 0) return cudaSuccess;
+    if (prm.group_limit > 0) return launch_route_tc<KMAX, 1, ROUTE_GROUP>(mx, mw, prm, tiles, s);
     if constexpr (KMAX > 8) {
         (void)num_sms;
-        return launch_route_tc<KMAX, 1>(mx, mw, prm, tiles, s);
+        if (prm.sel_bias != nullptr)
+            return launch_route_tc<KMAX, 1, ROUTE_SELBIAS>(mx, mw, prm, tiles, s);
+        return launch_route_tc<KMAX, 1, ROUTE_PLAIN>(mx, mw, prm, tiles, s);
     } else {
-        if (tiles <= num_sms) return launch_route_tc<KMAX, 4>(mx, mw, prm, tiles, s);
-        return launch_route_tc<KMAX, 2>(mx, mw, prm, tiles, s);
+        const bool wide = tiles <= num_sms;
+        if (prm.sel_bias != nullptr)
+            return wide ? launch_route_tc<KMAX, 4, ROUTE_SELBIAS>(mx, mw, prm, tiles, s)
+                        : launch_route_tc<KMAX, 2, ROUTE_SELBIAS>(mx, mw, prm, tiles, s);
+        return wide ? launch_route_tc<KMAX, 4, ROUTE_PLAIN>(mx, mw, prm, tiles, s)
+                    : launch_route_tc<KMAX, 2, ROUTE_PLAIN>(mx, mw, prm, tiles, s);
     }
 }
 
@@ -369,6 +482,9 @@ cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_rou
     prm.k = d.k;
     prm.nseg = ceil_div(d.N, kSegTokens);
     prm.bias = bias;
+    prm.sel_bias = d.sel_bias;
+    prm.group_limit = d.group_limit;
+    prm.per_part = d.E / d.P;
     prm.route_idx = topk_idx;
     prm.route_w = topk_w;
     prm.seg_hist = seg_hist;

@@ -85,6 +85,18 @@ enum {
  *  dtype            MOE_DTYPE_BF16 (tcgen05 tensor-core experts) or MOE_DTYPE_FP32
  *                   (fp32 FFMA experts)
  *  has_bias         1 if the router has a bias vector (fp32 [E])
+ *
+ * Routing variants (Ultralytics page, "Load balancing and capacity": DeepSeek-V3's
+ * bias-based balancing and its limit on the nodes a token is sent to):
+ *  group_limit      0: none. Otherwise each token's top_k experts are taken from at
+ *                   most group_limit of the ep_size partitions: a partition scores the
+ *                   best selection score of its experts, the group_limit best partitions
+ *                   are kept (ties: lower partition id) and the top_k experts inside
+ *                   them are chosen. Needs group_limit * (E / ep_size) >= top_k,
+ *                   group_limit <= 8 and ep_size <= 64.
+ *  selection_bias   NULL, or fp32 [E] device array added to the logits for choosing
+ *                   experts only; the routing weights remain the softmax of the chosen
+ *                   experts' own logits. moe_update_selection_bias adjusts it.
  */
 typedef struct moe_config {
     int64_t num_tokens;
@@ -97,6 +109,8 @@ typedef struct moe_config {
     int32_t mode;
     int32_t dtype;
     int32_t has_bias;
+    int32_t group_limit;
+    const float *selection_bias;
 } moe_config;
 
 /* Stage boundaries recorded by moe_layer_forward when moe_diagnostics.stage_events is
@@ -171,6 +185,20 @@ moe_status_t moe_pack_weights(const moe_config *cfg, const void *w_gate, const v
 moe_status_t moe_route(const moe_config *cfg, const void *x, const void *w_router,
                        const float *b_router, int32_t *topk_idx, float *topk_w,
                        void *stream);
+
+/*
+ * After-step update of the selection bias (Ultralytics page, "Load balancing and
+ * capacity": the bias of an overloaded expert is lowered and that of an idle expert
+ * raised after each step). Overloaded / idle: routed_counts[e] above / below the equal
+ * share num_tokens * top_k / num_experts (compared exactly, as integers); the step is
+ * gamma: selection_bias[e] -= gamma or += gamma in fp32, unchanged at the share.
+ *   routed_counts   [E] int32, the step's assignments per expert before capacity
+ *                   (moe_dispatch's routed_counts)
+ *   selection_bias  [E] fp32, updated in place
+ * Both are device pointers owned by the caller. Enqueued on `stream`.
+ */
+moe_status_t moe_update_selection_bias(const moe_config *cfg, const int32_t *routed_counts,
+                                       float *selection_bias, float gamma, void *stream);
 
 /*
  * Step 2 -- dispatch (Hugging Face page, "Token dispatch": every (token, expert) pair

@@ -77,6 +77,12 @@ def status_of(moe, c):
     (dict(capacity_factor=1.25), 0),
     (dict(mode="mask_sum"), 0),
     (dict(dtype="fp32"), 0),
+    (dict(group_limit=-1), 1),
+    (dict(group_limit=1), 0),                      # 1 partition of 2 experts holds k = 2
+    (dict(group_limit=1, ep_size=8), 1),           # 1 partition of 1 expert < k = 2
+    (dict(group_limit=4), 0),                      # >= ep_size: no limit
+    (dict(E=128, ep_size=16, group_limit=9), 2),   # beyond the supported group limit
+    (dict(E=128, ep_size=128, group_limit=2), 2),  # beyond the supported partition count
 ])
 def test_config_validation(moe, kw, status):
     c = cfg(moe, **kw)
@@ -160,3 +166,10 @@ def test_empty_batch_is_a_no_op(moe):
 def test_status_strings(moe):
     for s in range(6):
         assert moe.lib.moe_status_string(s).decode().startswith("MOE_")
+
+
+def test_misaligned_selection_bias_is_rejected_before_any_access(moe):
+    c = cfg(moe)
+    c.selection_bias = 0x1002     # never dereferenced: validation comes first
+    st, _ = status_of(moe, c)
+    assert st == 1 and b"selection_bias" in moe.lib.moe_last_error()
