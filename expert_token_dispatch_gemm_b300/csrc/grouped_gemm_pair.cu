@@ -67,6 +67,9 @@ struct PairParams {
     int num_kb;              // K blocks of BK
     int f_tiles;             // PM-row weight tiles per expert
     int a_rows_per_expert;   // rows between experts in A's tensor map
+    int live_halves;         // CM-row halves of A per expert holding real weight rows;
+                             // a tile's half 2f + c at or past it is skipped (rows
+                             // past I / H: its loads, and gate_up's stores)
     __nv_bfloat16 *h;        // EPI_SWIGLU output [pairs, h_ld]
     int h_ld;
     __nv_bfloat16 *out_slots;   // EPI_DOWN output [pairs, H]
@@ -172,7 +175,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const PairParams
                 const int t_row = tl.tok0 + (int)cta * (tl.nmma >> 1);
                 const int bsel = token_box_index(tl.nmma >> 1);
                 const CUtensorMap *tmap_t = &maps.t[bsel];
-                const uint32_t tx = 2 * (A_BYTES + (uint32_t)(16 << bsel) * BK * 2);
+                // a weight half past the expert's real rows is not loaded: its MMA rows
+                // are never stored
+                const bool live0 = 2 * tl.f < p.live_halves, live1 = 2 * tl.f + 1 < p.live_halves;
+                const bool a_live = cta == 0 ? live0 : live1;
+                const uint32_t tx = (live0 ? A_BYTES : 0u) + (live1 ? A_BYTES : 0u) +
+                                    2u * (uint32_t)(16 << bsel) * BK * 2;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_s, p.status)) {
                         ok = false;
@@ -180,8 +188,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const PairParams
                     }
                     if (cta == 0) mbar_arrive_expect_tx(&full[stage], tx);
                     const uint32_t fb = full_even0 + stage * 8;
-                    tma_load_2d_pair(smem_u32(smem + Smem::a_off + stage * A_BYTES), &maps.w, fb,
-                                     kb * BK, w_row);
+                    if (a_live)
+                        tma_load_2d_pair(smem_u32(smem + Smem::a_off + stage * A_BYTES), &maps.w,
+                                         fb, kb * BK, w_row);
                     tma_load_2d_pair(smem_u32(smem + Smem::b_off + stage * B_BYTES), tmap_t, fb,
                                      kb * BK, t_row);
                     armed |= 1u << stage;
@@ -298,7 +307,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const PairParams
                     for (int s = 0; s < 2; ++s) {
                         const int item = etid + 128 * s;
                         const int j = item >> 3, f8 = (item & 7) * 8;
-                        if (c + j < tl.ntok) {
+                        if (c + j < tl.ntok && 2 * tl.f + (int)cta < p.live_halves) {
                             const float4 *g4 = reinterpret_cast<const float4 *>(stage_f + j * GU_FEATS + f8);
                             const float4 *u4 = reinterpret_cast<const float4 *>(
                                 stage_f + CHUNK * GU_FEATS + j * GU_FEATS + f8);
@@ -428,6 +437,7 @@ cudaError_t launch_tc_gate_up(const LayerDims &d, const void *send, const int32_
     prm.num_kb = ceil_div(d.H, BK);
     prm.f_tiles = 2 * d.Ipad / PM;
     prm.a_rows_per_expert = 2 * d.Ipad;
+    prm.live_halves = ceil_div(d.I, GU_FEATS);
     prm.h = (__nv_bfloat16 *)h;
     prm.h_ld = d.Ipad;
     prm.H = d.H;
@@ -451,6 +461,7 @@ cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *exp
     prm.num_kb = ceil_div(d.I, BK);
     prm.f_tiles = ceil_div(d.H, PM);
     prm.a_rows_per_expert = d.H;
+    prm.live_halves = ceil_div(d.H, CM);
     prm.out_slots = (__nv_bfloat16 *)out_slots;
     prm.perm = perm;
     prm.topk_w = topk_w;
