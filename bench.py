@@ -93,6 +93,23 @@ def roofline_entry(work, ms, peaks, source, dtype):
     return out
 
 
+# ------------------------------------------------------------------ ranks
+def slowest_rank_ms(ms, dist, device):
+    """The step time of the slowest rank (every rank gets the same value); `dist` is None
+    for a single process."""
+    if dist is None:
+        return ms
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms):
+    """Whole-job throughput: every rank processes its own batch (weak scaling), the job
+    takes as long as the slowest rank."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ measured DRAM traffic
 TRAFFIC_SOURCES = ("grouped_gemm_pair.cu", "sm100.cuh", "common.cuh")
 
@@ -385,12 +402,8 @@ def main():
     if flags:
         raise RuntimeError(f"device status flags {flags} after the timed steps")
 
-    ms_step = ms_total / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * shape.N / (ms_step / 1e3)
+    ms_step = slowest_rank_ms(ms_total / args.steps, dist, dev)
+    value = job_tokens_per_s(shape.N, world, ms_step)
 
     # end to end through the C ABI: every step copies its input from pinned host memory
     # to the device and reads its output back. Copies run on their own streams, double
@@ -433,13 +446,9 @@ def main():
         run_pipeline(K)
         s1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = s0.elapsed_time(s1) / K
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = slowest_rank_ms(s0.elapsed_time(s1) / K, dist, dev)
         nbytes = x.numel() * x.element_size()
-        e2e = dict(value=round(world * shape.N / (e2e_ms / 1e3), 1), unit="tokens/s",
+        e2e = dict(value=round(job_tokens_per_s(shape.N, world, e2e_ms), 1), unit="tokens/s",
                    ms_per_step=round(e2e_ms, 4), h2d_bytes_per_step=nbytes,
                    d2h_bytes_per_step=out.numel() * out.element_size(),
                    overlap="uploads and downloads on their own streams, double buffered")
