@@ -63,8 +63,9 @@ def stage_work(shape, counts):
     return {
         "route": dict(bytes=N * H * s + E * H * s + bias + N * k * 8 + nseg * E * 4,
                       flops=2 * N * H * E),
-        "scan": dict(bytes=3 * nseg * E * 4 + 4 * E * 4, flops=0),
-        "assign": dict(bytes=N * k * 8 + A * 4 + nseg * E * 4, flops=0),
+        # counts, offsets and slots in one kernel (the assign stage is empty)
+        "scan": dict(bytes=nseg * E * 4 + N * k * 8 + A * 4 + 4 * E * 4, flops=0),
+        "assign": dict(bytes=0, flops=0),
         "permute": dict(bytes=N * H * s + A * H * s + N * k * 4, flops=0),
         "gate_up": dict(bytes=touched * 2 * I * H * s + A * H * s + A * I * s,
                         flops=4 * A * H * I),
@@ -467,7 +468,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_from_device(shape, inp)
 
-    launches_per_step = 7   # route, scan, assign, permute, gate_up, down, combine
+    launches_per_step = 6   # route, scan/assign, permute, gate_up, down, combine
     if rank == 0:
         line = dict(metric=METRIC, value=round(value, 1), unit="tokens/s", n_gpus=world,
                     steps=args.steps, warmup=args.warmup, ms_per_step=round(ms_step, 4),

@@ -122,12 +122,11 @@ cudaError_t launch_update_selection_bias(const LayerDims &d, const int32_t *rout
 
 cudaError_t launch_histogram(const LayerDims &d, const int32_t *topk_idx, int32_t *seg_hist,
                              int32_t *status, cudaStream_t s);
-cudaError_t launch_scan(const LayerDims &d, const int32_t *seg_hist, int32_t *seg_base,
-                        int32_t *routed_counts, int32_t *counts, int32_t *expert_offsets,
-                        int32_t *part_offsets, cudaStream_t s);
-cudaError_t launch_assign(const LayerDims &d, const int32_t *topk_idx, const int32_t *seg_base,
-                          const int32_t *expert_offsets, int32_t *slot_pos, int32_t *perm,
-                          int32_t *status, cudaStream_t s);
+// scan + assign in one kernel (the scan's segment bases are not materialised)
+cudaError_t launch_scan_assign(const LayerDims &d, const int32_t *topk_idx, const int32_t *seg_hist,
+                               int32_t *routed_counts, int32_t *counts, int32_t *expert_offsets,
+                               int32_t *part_offsets, int32_t *slot_pos, int32_t *perm,
+                               int32_t *status, cudaStream_t s);
 cudaError_t launch_permute(const LayerDims &d, const void *x, const int32_t *slot_pos,
                            void *send, cudaStream_t s);
 

@@ -9,11 +9,12 @@
 // is expert_offsets[e] + rank. The rank is computed without atomics on values:
 //   1. per segment of kSegTokens tokens, a histogram of expert ids (fused into routing
 //      for the whole layer, or histogram_kernel here);
-//   2. one CTA scans the [segments x E] histogram: exclusive per-expert segment bases,
-//      routed counts, kept counts, expert and partition offsets;
-//   3. one warp per segment walks its pairs in order 32 at a time; lanes holding the
-//      same expert find each other with __match_any_sync, so a pair's rank is its
-//      segment base plus the number of earlier pairs of that expert.
+//   2. one warp per segment (8 per CTA): each CTA sums the [segments x E] histogram
+//      into the routed totals (hence kept counts, expert and partition offsets) and its
+//      segments' bases (pairs of earlier segments per expert); the warp then walks its
+//      pairs in order 32 at a time, and lanes holding the same expert find each other
+//      with __match_any_sync, so a pair's rank is its segment base plus the number of
+//      earlier pairs of that expert.
 // Every step is deterministic, so counts, offsets, perm and slot_pos are bit-exact.
 #include <limits.h>
 
@@ -21,8 +22,6 @@
 
 namespace moe {
 namespace {
-
-constexpr int kScanThreads = 1024;
 
 __global__ void histogram_kernel(const int32_t *__restrict__ idx, int N, int k, int E,
                                  int32_t *__restrict__ seg_hist, int32_t *status) {
@@ -44,78 +43,116 @@ __global__ void histogram_kernel(const int32_t *__restrict__ idx, int N, int k, 
     for (int e = threadIdx.x; e < E; e += blockDim.x) seg_hist[(size_t)blockIdx.x * E + e] = hs[e];
 }
 
-// Single CTA. Thread (e, c) = (tid % E, tid / E) owns a contiguous chunk of segments
-// for expert e; G = 1024 / E chunks per expert.
-__global__ void __launch_bounds__(kScanThreads)
-scan_kernel(const int32_t *__restrict__ seg_hist, int nseg, int E, int P, int capacity,
-            int32_t *__restrict__ seg_base, int32_t *__restrict__ routed_counts,
-            int32_t *__restrict__ counts, int32_t *__restrict__ expert_offsets,
-            int32_t *__restrict__ part_offsets) {
-    grid_dep_wait();
-    grid_dep_trigger();
-    __shared__ int part[kScanThreads];        // [G][E] chunk sums, then exclusive bases
-    __shared__ int kept_s[kMaxExperts + 1];
-    const int tid = threadIdx.x;
-    const int G = kScanThreads / E;
-    const int e = tid % E, c = tid / E;
-    const bool active = c < G;
-    const int per = (nseg + G - 1) / G;
-    const int b0 = min(c * per, nseg), b1 = min(b0 + per, nseg);
-    if (active) {
-        int s = 0;
-        for (int b = b0; b < b1; ++b) s += seg_hist[(size_t)b * E + e];
-        part[c * E + e] = s;
-    }
-    __syncthreads();
-    if (tid < E) {   // exclusive scan over chunks of expert tid
-        int run = 0;
-        for (int cc = 0; cc < G; ++cc) {
-            const int v = part[cc * E + tid];
-            part[cc * E + tid] = run;
-            run += v;
-        }
-        routed_counts[tid] = run;
-        const int kept = run < capacity ? run : capacity;
-        counts[tid] = kept;
-        kept_s[tid] = kept;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int ee = 0; ee < E; ++ee) {
-            const int v = kept_s[ee];
-            kept_s[ee] = run;
-            expert_offsets[ee] = run;
-            run += v;
-        }
-        kept_s[E] = run;
-        expert_offsets[E] = run;
-    }
-    __syncthreads();
-    if (tid <= P) part_offsets[tid] = kept_s[tid * (E / P)];
-    if (active) {
-        int run = part[c * E + e];
-        for (int b = b0; b < b1; ++b) {
-            seg_base[(size_t)b * E + e] = run;
-            run += seg_hist[(size_t)b * E + e];
-        }
-    }
-}
-
-// One warp per segment; 8 warps per CTA.
+// Counts, offsets and stable slots in one kernel: one warp per 64-token segment, 8 per
+// CTA. Every CTA sums all segments' histograms (at most 256 x nseg ints, read from L2)
+// into the experts' routed totals and its own segments' rank bases, derives the kept
+// counts and the exclusive expert offsets, and assigns its segments' pairs exactly as
+// the separate scan and assign kernels do; CTA 0 writes the counts and offsets.
 __global__ void __launch_bounds__(256)
-assign_kernel(const int32_t *__restrict__ idx, int N, int k, int E, int capacity,
-              const int32_t *__restrict__ seg_base, const int32_t *__restrict__ expert_offsets,
-              int32_t *__restrict__ slot_pos, int32_t *__restrict__ perm, int32_t *status) {
+scan_assign_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ seg_hist, int N,
+                   int k, int E, int P, int capacity, int32_t *__restrict__ routed_counts,
+                   int32_t *__restrict__ counts, int32_t *__restrict__ expert_offsets,
+                   int32_t *__restrict__ part_offsets, int32_t *__restrict__ slot_pos,
+                   int32_t *__restrict__ perm, int32_t *status) {
     grid_dep_wait();
     grid_dep_trigger();
+    __shared__ int tot_s[kMaxExperts], before_s[kMaxExperts], off_s[kMaxExperts + 1];
     __shared__ int base_s[8][kMaxExperts];
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int seg = blockIdx.x * 8 + warp;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int nseg = (N + kSegTokens - 1) / kSegTokens;
+    const int seg0 = blockIdx.x * 8;
+    // routed totals and the counts of segments before this CTA's, per expert
+    for (int e = tid; e < E; e += 256) {
+        tot_s[e] = 0;
+        before_s[e] = 0;
+    }
+    __syncthreads();
+    if (E % 4 == 0) {
+        // 16-byte loads of 4 experts; G threads per group of 4 experts, each with 8
+        // rows in flight
+        const int Q = E / 4, G = 256 / Q;
+        const int q = tid % Q, g = tid / Q;
+        if (g < G) {
+            int4 tot = make_int4(0, 0, 0, 0), before = make_int4(0, 0, 0, 0);
+            const int4 *h4 = reinterpret_cast<const int4 *>(seg_hist) + q;
+            for (int b0 = g; b0 < nseg; b0 += 8 * G) {
+                int4 h[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int b = b0 + u * G;
+                    h[u] = b < nseg ? h4[(size_t)b * Q] : make_int4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    tot.x += h[u].x; tot.y += h[u].y; tot.z += h[u].z; tot.w += h[u].w;
+                    if (b0 + u * G < seg0) {
+                        before.x += h[u].x; before.y += h[u].y;
+                        before.z += h[u].z; before.w += h[u].w;
+                    }
+                }
+            }
+            atomicAdd(&tot_s[4 * q], tot.x);
+            atomicAdd(&tot_s[4 * q + 1], tot.y);
+            atomicAdd(&tot_s[4 * q + 2], tot.z);
+            atomicAdd(&tot_s[4 * q + 3], tot.w);
+            atomicAdd(&before_s[4 * q], before.x);
+            atomicAdd(&before_s[4 * q + 1], before.y);
+            atomicAdd(&before_s[4 * q + 2], before.z);
+            atomicAdd(&before_s[4 * q + 3], before.w);
+        }
+    } else {
+        const int G = 256 / E > 0 ? 256 / E : 1;   // threads per expert
+        const int e = tid % E, g = tid / E;
+        if (g < G && tid < G * E) {
+            int tot = 0, before = 0;
+            for (int b = g; b < nseg; b += G) {
+                const int h = seg_hist[(size_t)b * E + e];
+                tot += h;
+                if (b < seg0) before += h;
+            }
+            atomicAdd(&tot_s[e], tot);
+            atomicAdd(&before_s[e], before);
+        }
+    }
+    __syncthreads();
+    // exclusive scan of the kept counts over experts (one warp, E/32 experts per lane)
+    if (warp == 0) {
+        const int per = (E + 31) / 32;
+        const int e0 = lane * per, e1 = min(e0 + per, E);
+        int local = 0;
+        for (int e = e0; e < e1; ++e) local += min(tot_s[e], capacity);
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int e = e0; e < e1; ++e) {
+            off_s[e] = run;
+            run += min(tot_s[e], capacity);
+        }
+        if (lane == 31) off_s[E] = incl;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int e = tid; e < E; e += 256) {
+            routed_counts[e] = tot_s[e];
+            counts[e] = min(tot_s[e], capacity);
+            expert_offsets[e] = off_s[e];
+        }
+        if (tid == 0) expert_offsets[E] = off_s[E];
+        if (tid <= P) part_offsets[tid] = off_s[tid * (E / P)];
+    }
+    // this warp's segment: rank base = pairs of earlier segments per expert
+    const int seg = seg0 + warp;
     if (seg >= nseg) return;   // warp-uniform; no block-wide barrier follows
     int *base = base_s[warp];
-    for (int e = lane; e < E; e += 32) base[e] = seg_base[(size_t)seg * E + e];
+    for (int e = lane; e < E; e += 32) {
+        int b = before_s[e];
+        for (int s2 = seg0; s2 < seg; ++s2) b += seg_hist[(size_t)s2 * E + e];
+        base[e] = b;
+    }
     __syncwarp();
     const int64_t p0 = (int64_t)seg * kSegTokens * k;
     const int64_t p1 = min(p0 + (int64_t)kSegTokens * k, (int64_t)N * k);
@@ -137,7 +174,7 @@ assign_kernel(const int32_t *__restrict__ idx, int N, int k, int E, int capacity
         if (live) {
             int slot = -1;
             if (valid && rank < capacity) {
-                slot = expert_offsets[e] + rank;
+                slot = off_s[e] + rank;
                 perm[slot] = (int32_t)p;
             }
             slot_pos[p] = slot;
@@ -209,20 +246,14 @@ cudaError_t launch_histogram(const LayerDims &d, const int32_t *topk_idx, int32_
                       seg_hist, status);
 }
 
-cudaError_t launch_scan(const LayerDims &d, const int32_t *seg_hist, int32_t *seg_base,
-                        int32_t *routed_counts, int32_t *counts, int32_t *expert_offsets,
-                        int32_t *part_offsets, cudaStream_t s) {
+cudaError_t launch_scan_assign(const LayerDims &d, const int32_t *topk_idx, const int32_t *seg_hist,
+                               int32_t *routed_counts, int32_t *counts, int32_t *expert_offsets,
+                               int32_t *part_offsets, int32_t *slot_pos, int32_t *perm,
+                               int32_t *status, cudaStream_t s) {
     const int nseg = ceil_div(d.N, kSegTokens);
-    return launch_pdl(scan_kernel, dim3(1), dim3(kScanThreads), 0, s, seg_hist, nseg, d.E, d.P,
-                      d.capacity, seg_base, routed_counts, counts, expert_offsets, part_offsets);
-}
-
-cudaError_t launch_assign(const LayerDims &d, const int32_t *topk_idx, const int32_t *seg_base,
-                          const int32_t *expert_offsets, int32_t *slot_pos, int32_t *perm,
-                          int32_t *status, cudaStream_t s) {
-    const int nseg = ceil_div(d.N, kSegTokens);
-    return launch_pdl(assign_kernel, dim3(ceil_div(nseg, 8)), dim3(256), 0, s, topk_idx, d.N, d.k,
-                      d.E, d.capacity, seg_base, expert_offsets, slot_pos, perm, status);
+    return launch_pdl(scan_assign_kernel, dim3(ceil_div(nseg, 8)), dim3(256), 0, s, topk_idx,
+                      seg_hist, d.N, d.k, d.E, d.P, d.capacity, routed_counts, counts,
+                      expert_offsets, part_offsets, slot_pos, perm, status);
 }
 
 cudaError_t launch_permute(const LayerDims &d, const void *x, const int32_t *slot_pos,

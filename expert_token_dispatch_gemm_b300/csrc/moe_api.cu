@@ -111,7 +111,6 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 struct Workspace {
     int32_t *status;       // [8]
     int32_t *seg_hist;     // [nseg, E]
-    int32_t *seg_base;     // [nseg, E]
     int32_t *topk_idx;     // [N*k]
     float *topk_w;         // [N*k]
     int32_t *routed;       // [E]
@@ -139,7 +138,6 @@ Workspace carve(const LayerDims &d, int mode, void *base) {
     const size_t pairs = (size_t)d.N * d.k;
     w.status = (int32_t *)take(8 * sizeof(int32_t));
     w.seg_hist = (int32_t *)take(nseg * d.E * sizeof(int32_t));
-    w.seg_base = (int32_t *)take(nseg * d.E * sizeof(int32_t));
     w.topk_idx = (int32_t *)take(pairs * sizeof(int32_t));
     w.topk_w = (float *)take(pairs * sizeof(float));
     w.routed = (int32_t *)take(d.E * sizeof(int32_t));
@@ -203,8 +201,9 @@ moe_status_t run_dispatch_from_hist(const LayerDims &d, const int32_t *idx, cons
                                     const Workspace &w, int32_t *routed, int32_t *counts,
                                     int32_t *eoff, int32_t *poff, int32_t *perm, int32_t *slot_pos,
                                     void *send, cudaStream_t s) {
-    MOE_CUDA(launch_scan(d, w.seg_hist, w.seg_base, routed, counts, eoff, poff, s), "scan kernel");
-    MOE_CUDA(launch_assign(d, idx, w.seg_base, eoff, slot_pos, perm, w.status, s), "assign kernel");
+    MOE_CUDA(launch_scan_assign(d, idx, w.seg_hist, routed, counts, eoff, poff, slot_pos, perm,
+                                w.status, s),
+             "scan/assign kernel");
     MOE_CUDA(launch_permute(d, x, slot_pos, send, s), "permute kernel");
     return MOE_OK;
 }
@@ -254,12 +253,11 @@ moe_status_t run_combine(const LayerDims &d, int mode, const void *slots, const 
 
 // ---------------------------------------------------------------- no-allocation dispatch
 // Scratch of moe_dispatch_noalloc: a status word (padded to 256 bytes), then the
-// per-segment histograms and the per-segment rank bases, each up to
-// kNoAllocMaxSegExperts ints. Every GPU that loads the library holds these 2 MiB until
-// the process exits.
+// per-segment histograms, up to kNoAllocMaxSegExperts ints. Every GPU that loads the
+// library holds this 1 MiB until the process exits.
 constexpr int kNoAllocMaxSegExperts = 1 << 18;
 constexpr int kNoAllocStatusInts = 64;
-__device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocStatusInts + 2 * kNoAllocMaxSegExperts];
+__device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocStatusInts + kNoAllocMaxSegExperts];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
@@ -497,9 +495,10 @@ moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void 
                    w.status, s);
     if (st != MOE_OK) return st;
     MOE_MARK(MOE_STAGE_SCAN);
-    MOE_CUDA(launch_scan(d, w.seg_hist, w.seg_base, routed, counts, eoff, poff, s), "scan kernel");
-    MOE_MARK(MOE_STAGE_ASSIGN);
-    MOE_CUDA(launch_assign(d, idx, w.seg_base, eoff, slot_pos, perm, w.status, s), "assign kernel");
+    MOE_CUDA(launch_scan_assign(d, idx, w.seg_hist, routed, counts, eoff, poff, slot_pos, perm,
+                                w.status, s),
+             "scan/assign kernel");
+    MOE_MARK(MOE_STAGE_ASSIGN);   // fused into the scan stage's kernel
     MOE_MARK(MOE_STAGE_PERMUTE);
     MOE_CUDA(launch_permute(d, x, slot_pos, w.send, s), "permute kernel");
     MOE_MARK(MOE_STAGE_GATE_UP);
@@ -578,13 +577,12 @@ moe_status_t moe_dispatch_noalloc(const moe_config *cfg, const int32_t *topk_idx
         MOE_CUDA(cudaMemsetAsync(part_offsets, 0, (d.P + 1) * sizeof(int32_t), s), "memset");
         return MOE_OK;
     }
-    // The histogram kernel writes every [segment, expert] entry and the scan every base,
-    // so only the status word carries over from the previous call: clear it.
+    // The histogram kernel writes every [segment, expert] entry, so only the status word
+    // carries over from the previous call: clear it.
     int32_t *status = scratch;
     Workspace w = {};
     w.status = status;
     w.seg_hist = scratch + kNoAllocStatusInts;
-    w.seg_base = w.seg_hist + seg_experts;
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t), s), "status reset");
     MOE_CUDA(launch_histogram(d, topk_idx, w.seg_hist, w.status, s), "histogram kernel");
     return run_dispatch_from_hist(d, topk_idx, x, w, routed_counts, counts, expert_offsets,

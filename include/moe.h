@@ -118,8 +118,8 @@ typedef struct moe_config {
  * MOE_NUM_STAGES after the last one. */
 enum {
     MOE_STAGE_ROUTE = 0,     /* router + top-k + softmax + segment histogram: 1 kernel */
-    MOE_STAGE_SCAN = 1,      /* counts, offsets, segment bases: 1 kernel */
-    MOE_STAGE_ASSIGN = 2,    /* stable slot of every pair: 1 kernel */
+    MOE_STAGE_SCAN = 1,      /* counts, offsets and the stable slot of every pair: 1 kernel */
+    MOE_STAGE_ASSIGN = 2,    /* empty: the slots are assigned in MOE_STAGE_SCAN's kernel */
     MOE_STAGE_PERMUTE = 3,   /* hidden-state rows into the send buffer: 1 kernel */
     MOE_STAGE_GATE_UP = 4,   /* grouped GEMM gate/up + SwiGLU: 1 kernel */
     MOE_STAGE_DOWN = 5,      /* grouped GEMM down + weighted un-permute: 1 kernel */
@@ -231,8 +231,8 @@ moe_status_t moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const 
  * outputs) and therefore cannot provide moe_dispatch's workspace.
  *
  * Same arguments, results and errors as moe_dispatch, minus workspace and its size. The
- * per-segment histograms and rank bases live instead in a fixed array of device memory
- * inside the library (2 MiB, plus 256 bytes for a status word), which every GPU that
+ * per-segment histograms live instead in a fixed array of device memory inside the
+ * library (1 MiB, plus 256 bytes for a status word), which every GPU that
  * loads the library keeps until the process exits. Limit: ceil(num_tokens / 64) *
  * num_experts must not exceed 262144 (for example 65536 tokens with 256 experts);
  * larger calls return MOE_ERR_UNSUPPORTED and enqueue nothing.
