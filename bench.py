@@ -75,12 +75,26 @@ def stage_work(shape, counts):
     }
 
 
+def fp32_alu_tflops(peaks):
+    """FFMA peak of the fp32 path: 148 SMs x 128 fp32 lanes x 2 flops per clock at the
+    measured maximum SM clock."""
+    return 148 * 128 * 2 * float(peaks.get("sm_max_mhz", 2032.0)) * 1e6 / 1e12
+
+
 def roofline_entry(work, ms, peaks, source, dtype):
     t = ms / 1e3
     hbm = peaks["hbm_gbs"]
     tf = peaks["bf16_tflops"] if dtype == "bf16" else None
     t_mem = work["bytes"] / (hbm * 1e9)
     t_flop = work["flops"] / (tf * 1e12) if tf else 0.0
+    if dtype != "bf16" and work["flops"]:
+        alu = fp32_alu_tflops(peaks)
+        if work["flops"] / (alu * 1e12) >= t_mem:
+            ach = work["flops"] / t / 1e12
+            return dict(bound="alu", achieved=round(ach, 2), peak=round(alu, 1),
+                        unit="TFLOP/s", frac=round(ach / alu, 4),
+                        peak_source="148 SMs x 128 fp32 lanes x 2 flop x max SM clock",
+                        hbm_frac=round(work["bytes"] / t / 1e9 / hbm, 4))
     if tf and t_flop >= t_mem:
         ach = work["flops"] / t / 1e12
         return dict(bound="tensor", achieved=round(ach, 2), peak=tf, unit="TFLOP/s",
