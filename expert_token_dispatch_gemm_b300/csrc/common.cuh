@@ -23,7 +23,7 @@ constexpr int kIpadAlign = 128;
 
 // Rows per M tile of the grouped GEMMs (tensor-core path and fp32 path).
 constexpr int kTcBlockM = 128;
-constexpr int kSimtBlockM = 64;
+constexpr int kSimtBlockM = 128;
 
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
