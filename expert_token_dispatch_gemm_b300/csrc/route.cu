@@ -18,7 +18,9 @@ namespace moe {
 namespace {
 
 constexpr int kRouteThreads = 256;
-constexpr int kRouteKChunk = 32;
+// Hidden columns staged per step: wide for few experts (fewer load/barrier round trips),
+// narrow for many (the expert tile grows with E).
+__host__ __device__ constexpr int route_k_chunk(int ep) { return ep <= 16 ? 128 : 32; }
 
 template <typename T, int RE, int EG>
 __global__ void __launch_bounds__(kRouteThreads)
@@ -29,7 +31,7 @@ route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__r
     grid_dep_wait();
     grid_dep_trigger();
     constexpr int TB = kSegTokens;
-    constexpr int KC = kRouteKChunk;
+    constexpr int KC = route_k_chunk(RE * EG);
     constexpr int EP = RE * EG;               // experts padded to the thread layout
     constexpr int TGN = kRouteThreads / EG;   // token groups
     constexpr int RT = TB / TGN;              // tokens per thread
@@ -209,7 +211,7 @@ template <typename T, int RE, int EG>
 cudaError_t launch_route_t(const LayerDims &d, const T *x, const T *wr, const float *b,
                            int32_t *idx, float *w, int32_t *hist, cudaStream_t s) {
     constexpr int EP = RE * EG;
-    const size_t stage = (size_t)(kSegTokens + EP) * (kRouteKChunk + 1) * sizeof(float);
+    const size_t stage = (size_t)(kSegTokens + EP) * (route_k_chunk(EP) + 1) * sizeof(float);
     const size_t logits = (size_t)kSegTokens * (EP + 1) * sizeof(float);
     const size_t smem = stage > logits ? stage : logits;
     auto kern = route_kernel<T, RE, EG>;
