@@ -9,5 +9,6 @@ from .moe import (  # noqa: F401
     expert_partition, load_counts, expert_capacity, dispatch_layout, permute,
     silu, swiglu_expert, expert_outputs, combine_dispatch, combine_mask_sum,
     layer_forward, token_outputs, selection_scores, group_limited_top_k, route_variant,
-    update_selection_bias,
+    update_selection_bias, silu_grad, layer_backward, balance_stats, tp_slices,
+    tp_row_split_forward,
 )

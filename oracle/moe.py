@@ -169,7 +169,7 @@ def expert_capacity(capacity_factor, num_tokens, k, num_experts):
     return math.ceil(cf * num_tokens * k / num_experts)
 
 
-def dispatch_layout(idx, num_experts, ep_size, capacity=None):
+def dispatch_layout(idx, num_experts, ep_size, capacity=None, priority="token"):
     """[HF-EP] "Token dispatch": every (token, expert) pair is sent to the partition that
     owns the expert; [UL-EP] step 2. On one device the send buffer is grouped by expert,
     so each partition's rows are contiguous (experts are split contiguously).
@@ -178,6 +178,11 @@ def dispatch_layout(idx, num_experts, ep_size, capacity=None):
     to the same expert. With a capacity C, a pair is kept iff rank < C ([UL-EP] "Load
     balancing and capacity": overflow pairs skip that expert; reading: the first C in
     token order are kept).
+
+    priority="slot" is the GShard-style variant: pairs are ranked slot-major -- every
+    token's first choice before any token's second choice, then by token -- so p's
+    priority key is j*N + t instead of t*k + j. The rank, the capacity test and the row
+    order inside an expert's segment all follow that key.
 
     Returns dict of int64 arrays:
       routed_counts [E]    pairs routed to each expert before capacity
@@ -192,8 +197,14 @@ def dispatch_layout(idx, num_experts, ep_size, capacity=None):
     E = num_experts
     flat = idx.reshape(-1).astype(np.int64)
     routed = np.bincount(flat, minlength=E).astype(np.int64)
-    # pairs grouped by expert; the stable sort keeps pair (= token) order inside a group
-    by_expert = np.argsort(flat, kind="stable")
+    if priority == "token":
+        order = np.arange(N * k)                       # pairs in priority order
+    elif priority == "slot":
+        order = np.arange(N * k).reshape(N, k).T.reshape(-1)
+    else:
+        raise ValueError(priority)
+    # pairs grouped by expert; the stable sort keeps priority order inside a group
+    by_expert = order[np.argsort(flat[order], kind="stable")]
     group_start = np.concatenate([[0], np.cumsum(routed)[:-1]])
     rank = np.empty(N * k, dtype=np.int64)
     rank[by_expert] = np.arange(N * k) - group_start[flat[by_expert]]
@@ -292,7 +303,7 @@ def combine_mask_sum(y_send, slot_pos, topk_idx, topk_w, num_experts, ep_size):
 # ---------------------------------------------------------------- the whole layer
 def layer_forward(x, w_router, b_router, w_gate, w_up, w_down, top_k, ep_size,
                   capacity_factor=None, mode="dispatch", selection_bias=None,
-                  group_limit=None):
+                  group_limit=None, capacity_priority="token"):
     """Route -> dispatch -> local experts -> weighted combine, all in fp64.
     Returns a dict with every intermediate (logits, topk_idx, topk_w, the dispatch
     layout, send, y_send, out and, in mask mode, partials)."""
@@ -302,7 +313,7 @@ def layer_forward(x, w_router, b_router, w_gate, w_up, w_down, top_k, ep_size,
     logits, idx, w = route_variant(x, w_router, b_router, top_k, selection_bias, ep_size,
                                    group_limit)
     C = expert_capacity(capacity_factor, N, top_k, E)
-    lay = dispatch_layout(idx, E, ep_size, C)
+    lay = dispatch_layout(idx, E, ep_size, C, capacity_priority)
     send = permute(x, lay["perm"], top_k)
     y_send = expert_outputs(send, lay["expert_offsets"], w_gate, w_up, w_down)
     res = dict(logits=logits, topk_idx=idx, topk_w=w, capacity=C, send=send,
@@ -315,6 +326,62 @@ def layer_forward(x, w_router, b_router, w_gate, w_up, w_down, top_k, ep_size,
     else:
         raise ValueError(mode)
     return res
+
+
+def balance_stats(logits, routed_counts, num_tokens, k):
+    """Router load statistics ([UL-EP] "Load balancing and capacity": an auxiliary loss
+    term pushes the router towards an even spread of tokens; the pages name no formula,
+    so only its two usual ingredients are computed, not a loss):
+      load_frac[e] = routed_counts[e] / (N * k), the share of the step's routed pairs
+                     that chose expert e (before capacity);
+      prob_mean[e] = mean over tokens of softmax(logits[t])[e], the router's average
+                     probability for e over all E experts.
+    logits are the raw router logits (bias included, selection bias not)."""
+    lg = _f64(logits)
+    N = lg.shape[0]
+    load = _f64(routed_counts) / float(num_tokens * k) if num_tokens * k else \
+        np.zeros(np.shape(routed_counts))
+    if N == 0:
+        return dict(load_frac=load, prob_mean=np.zeros(lg.shape[1]))
+    m = lg.max(axis=1, keepdims=True)
+    ex = np.exp(lg - m)
+    prob = ex / ex.sum(axis=1, keepdims=True)
+    return dict(load_frac=load, prob_mean=prob.sum(axis=0) / N)
+
+
+def tp_slices(num_tokens, tp_size):
+    """[HF-EP] "With tensor parallelism": the ranks of a TP group hold the same batch
+    and each dispatches a disjoint 1/tp_size of its tokens; slices may be uneven or
+    empty. Reading: contiguous slices, the first N mod tp one token longer
+    (numpy.array_split's rule). Returns [(begin, end)] per TP rank."""
+    q, r = divmod(num_tokens, tp_size)
+    out, b = [], 0
+    for s in range(tp_size):
+        n = q + (1 if s < r else 0)
+        out.append((b, b + n))
+        b += n
+    return out
+
+
+def tp_row_split_forward(x, w_router, b_router, w_gate, w_up, w_down, top_k, ep_size,
+                         tp_size, capacity_factor=None, mode="dispatch"):
+    """[HF-EP] "With tensor parallelism": TP rank s dispatches only its slice of the
+    shared batch, its results come back to it, and an all-reduce over the TP group of
+    the zero-padded slice outputs restores the full output. Each slice is a layer call
+    of its own over its tokens (reading: a capacity limit is therefore taken over the
+    slice's tokens). padded[s] holds slice s's rows and zeros elsewhere;
+    out = padded[0] + padded[1] + ... in rank order. Returns (padded, out)."""
+    x = _f64(x)
+    N, H = x.shape
+    padded = np.zeros((tp_size, N, H))
+    for s, (b, e) in enumerate(tp_slices(N, tp_size)):
+        if e > b:
+            padded[s, b:e] = layer_forward(x[b:e], w_router, b_router, w_gate, w_up, w_down,
+                                           top_k, ep_size, capacity_factor, mode)["out"]
+    out = np.zeros((N, H))
+    for s in range(tp_size):
+        out += padded[s]
+    return padded, out
 
 
 def token_outputs(x_rows, idx_rows, w_rows, keep_rows, expert_weights):
@@ -341,3 +408,74 @@ def token_outputs(x_rows, idx_rows, w_rows, keep_rows, expert_weights):
             if keep_rows[i][j]:
                 out[i] += float(w_rows[i][j]) * y[(i, j)]
     return out
+
+
+# ---------------------------------------------------------------- backward of the layer
+def silu_grad(z):
+    """d silu(z) / dz = sigmoid(z) * (1 + z * (1 - sigmoid(z)))."""
+    z = _f64(z)
+    with np.errstate(over="ignore"):
+        sig = 1.0 / (1.0 + np.exp(-z))
+    return sig * (1.0 + z * (1.0 - sig))
+
+
+def layer_backward(x, w_router, b_router, w_gate, w_up, w_down, top_k, ep_size, dout,
+                   capacity_factor=None, selection_bias=None, group_limit=None,
+                   capacity_priority="token"):
+    """Gradients of the layer output (dispatch rule; the mask-and-sum rule computes the
+    same output) with respect to its inputs and weights, for the upstream gradient dout
+    [N, H]: the chain rule through each step of layer_forward, in fp64. The expert
+    selection and the capacity drops are piecewise constant and carry no gradient; a
+    dropped pair's output is zero but its routing weight stays in the softmax, so the
+    weights' Jacobian still couples it ([UL-EP] "Load balancing and capacity": no
+    renormalisation). An expert's weight gradient sums over every token it received, as
+    the pages sum an expert's gradient over the batches of its group ([HF-EP] "How the
+    sizes combine").
+
+    out[t] = sum_j keep[t,j] * w[t,j] * y_{e_tj}(x_t),
+    y_e(x) = Wd_e (silu(Wg_e x) * (Wu_e x)),  w = softmax over the k chosen logits.
+    Returns dict dx [N,H], dw_router [E,H], db_router [E], dw_gate / dw_up [E,I,H],
+    dw_down [E,H,I]."""
+    x = _f64(x)
+    dout = _f64(dout)
+    N, H = x.shape
+    E = np.shape(w_router)[0]
+    k = top_k
+    fwd = layer_forward(x, w_router, b_router, w_gate, w_up, w_down, k, ep_size,
+                        capacity_factor, "dispatch", selection_bias, group_limit,
+                        capacity_priority)
+    idx, w, sp = fwd["topk_idx"], fwd["topk_w"], np.asarray(fwd["slot_pos"]).reshape(N, k)
+    dx = np.zeros_like(x)
+    dwg = np.zeros(np.shape(w_gate))
+    dwu = np.zeros(np.shape(w_up))
+    dwd = np.zeros(np.shape(w_down))
+    dweight = np.zeros((N, k))          # d out / d w[t, j] contracted with dout
+    for e in range(E):
+        pairs = [(t, j) for t in range(N) for j in range(k) if idx[t, j] == e and sp[t, j] >= 0]
+        if not pairs:
+            continue
+        ts = np.array([t for t, _ in pairs])
+        js = np.array([j for _, j in pairs])
+        xe = x[ts]                                   # [n, H]
+        g = xe @ _f64(w_gate[e]).T                   # [n, I]
+        u = xe @ _f64(w_up[e]).T
+        a = silu(g) * u
+        y = a @ _f64(w_down[e]).T                    # [n, H]
+        dy = w[ts, js][:, None] * dout[ts]           # d loss / d y
+        dweight[ts, js] = np.sum(dout[ts] * y, axis=1)
+        da = dy @ _f64(w_down[e])                    # [n, I]
+        dwd[e] += dy.T @ a
+        dg = da * u * silu_grad(g)
+        du = da * silu(g)
+        dwg[e] += dg.T @ xe
+        dwu[e] += du.T @ xe
+        np.add.at(dx, ts, dg @ _f64(w_gate[e]) + du @ _f64(w_up[e]))
+    # softmax over the chosen logits: dl_c = w_c (dweight_c - sum_c' w_c' dweight_c')
+    dl_chosen = w * (dweight - np.sum(w * dweight, axis=1, keepdims=True))
+    dlogits = np.zeros((N, E))
+    np.put_along_axis(dlogits, idx, dl_chosen, axis=1)
+    dx += dlogits @ _f64(w_router)
+    dwr = dlogits.T @ x
+    dbr = dlogits.sum(axis=0)
+    return dict(dx=dx, dw_router=dwr, db_router=dbr, dw_gate=dwg, dw_up=dwu, dw_down=dwd,
+                dlogits=dlogits, forward=fwd)

@@ -389,8 +389,8 @@ def test_planted_oracle_mistake_is_caught(name, monkeypatch):
 def test_planted_drop_order_mistake_is_caught(monkeypatch):
     real = om.dispatch_layout
 
-    def keep_last(idx, E, P, capacity=None):
-        lay = real(idx, E, P, capacity)
+    def keep_last(idx, E, P, capacity=None, priority="token"):
+        lay = real(idx, E, P, capacity, priority)
         flat = np.asarray(idx).reshape(-1)
         sp = np.full(flat.size, -1, dtype=np.int64)
         for e in range(E):
