@@ -19,6 +19,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUD
     MOE_ERR_TIMEOUT = range(6)
 MOE_DTYPE_BF16, MOE_DTYPE_FP32 = 0, 1
 MOE_MODE_DISPATCH, MOE_MODE_MASK_SUM = 0, 1
+MOE_PRIORITY_TOKEN, MOE_PRIORITY_SLOT = 0, 1
 MOE_DEV_TIMEOUT, MOE_DEV_BAD_EXPERT_ID = 1, 2
 
 _DTYPES = {MOE_DTYPE_BF16: torch.bfloat16, MOE_DTYPE_FP32: torch.float32}
@@ -37,7 +38,8 @@ class MoeConfig(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("ep_size", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("mode", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("has_bias", ctypes.c_int32),
-                ("group_limit", ctypes.c_int32), ("selection_bias", ctypes.c_void_p)]
+                ("group_limit", ctypes.c_int32), ("selection_bias", ctypes.c_void_p),
+                ("capacity_priority", ctypes.c_int32)]
 
     @property
     def torch_dtype(self):
@@ -48,7 +50,9 @@ class MoeDiagnostics(ctypes.Structure):
     """struct moe_diagnostics."""
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "topk_idx", "topk_w", "routed_counts", "counts", "expert_offsets", "part_offsets",
-        "perm", "slot_pos", "stage_events")]
+        "perm", "slot_pos", "stage_events", "router_logits")]
+    _ARRAYS = ("topk_idx", "topk_w", "routed_counts", "counts", "expert_offsets",
+               "part_offsets", "perm", "slot_pos", "router_logits")
 
 
 MOE_NUM_STAGES = 7
@@ -77,6 +81,10 @@ def _load():
         "moe_layer_forward": (ctypes.c_int, [cfgp, P, P, P, P, P, P,
                                              ctypes.POINTER(MoeDiagnostics), P, S, P]),
         "moe_read_device_status": (ctypes.c_int, [cfgp, P, S, ctypes.POINTER(I32), I32, P]),
+        "moe_balance_stats": (ctypes.c_int, [cfgp, P, P, P, P, P, S, P]),
+        "moe_tp_slice": (ctypes.c_int, [ctypes.c_int64, I32, I32, ctypes.POINTER(ctypes.c_int64),
+                                        ctypes.POINTER(ctypes.c_int64)]),
+        "moe_tp_reduce": (ctypes.c_int, [cfgp, I32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -89,16 +97,21 @@ lib = _load()
 
 
 def config(N, H, I, E, top_k, ep_size, capacity_factor=None, mode="dispatch",
-           dtype="bf16", has_bias=False, group_limit=0, selection_bias=None) -> MoeConfig:
+           dtype="bf16", has_bias=False, group_limit=0, selection_bias=None,
+           capacity_priority="token") -> MoeConfig:
     """struct moe_config. selection_bias: None or an fp32 [E] CUDA tensor, which the
-    caller keeps alive while the config is in use."""
+    caller keeps alive while the config is in use. capacity_priority: "token" or
+    "slot"."""
+    if capacity_priority not in ("token", "slot"):
+        raise ValueError(f"capacity_priority must be 'token' or 'slot', not {capacity_priority!r}")
     return MoeConfig(int(N), int(H), int(I), int(E), int(top_k), int(ep_size),
                      float(capacity_factor) if capacity_factor else 0.0,
                      MOE_MODE_DISPATCH if mode == "dispatch" else MOE_MODE_MASK_SUM,
                      MOE_DTYPE_BF16 if dtype == "bf16" else MOE_DTYPE_FP32, int(bool(has_bias)),
                      int(group_limit or 0),
                      None if selection_bias is None
-                     else _ptr(selection_bias, "selection_bias", torch.float32).value)
+                     else _ptr(selection_bias, "selection_bias", torch.float32).value,
+                     MOE_PRIORITY_SLOT if capacity_priority == "slot" else MOE_PRIORITY_TOKEN)
 
 
 def _check(status: int, func: str):
@@ -232,9 +245,9 @@ def moe_layer_forward(cfg, x, w_router, b_router, w_gate_up_packed, w_down, out,
                 raise ValueError("stage_events needs MOE_NUM_STAGES + 1 events")
             keep = (ctypes.c_void_p * len(stage_events))(*[e.cuda_event for e in stage_events])
             dg.stage_events = ctypes.cast(keep, ctypes.c_void_p).value
-        for name, _ in MoeDiagnostics._fields_[:-1]:
+        for name in MoeDiagnostics._ARRAYS:
             if diag and diag.get(name) is not None:
-                want = torch.float32 if name == "topk_w" else torch.int32
+                want = torch.float32 if name in ("topk_w", "router_logits") else torch.int32
                 setattr(dg, name, _ptr(diag[name], name, want).value)
     _check(lib.moe_layer_forward(ctypes.byref(cfg), _ptr(x, "x", dt),
                                  _ptr(w_router, "w_router", dt),
@@ -254,3 +267,28 @@ def moe_read_device_status(cfg, workspace, reset=True) -> int:
     if st not in (MOE_OK, MOE_ERR_TIMEOUT):
         _check(st, "moe_read_device_status")
     return flags.value
+
+
+def moe_balance_stats(cfg, router_logits, routed_counts, load_frac, prob_mean, workspace):
+    """Per-expert load share and mean router probability (moe.h)."""
+    f32 = torch.float32
+    _check(lib.moe_balance_stats(ctypes.byref(cfg), _ptr(router_logits, "router_logits", f32),
+                                 _ptr(routed_counts, "routed_counts", torch.int32),
+                                 _ptr(load_frac, "load_frac", f32),
+                                 _ptr(prob_mean, "prob_mean", f32), _ptr(workspace, "workspace"),
+                                 workspace.numel(), _stream()), "moe_balance_stats")
+
+
+def moe_tp_slice(num_tokens, tp_size, tp_rank):
+    """Token rows (begin, end) that TP rank tp_rank dispatches."""
+    b, e = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib.moe_tp_slice(int(num_tokens), int(tp_size), int(tp_rank), ctypes.byref(b),
+                            ctypes.byref(e)), "moe_tp_slice")
+    return b.value, e.value
+
+
+def moe_tp_reduce(cfg, tp_size, padded, out):
+    """out = sum over TP ranks, in order, of the zero-padded slice outputs padded[s]."""
+    dt = cfg.torch_dtype
+    _check(lib.moe_tp_reduce(ctypes.byref(cfg), int(tp_size), _ptr(padded, "padded", dt),
+                             _ptr(out, "out", dt), _stream()), "moe_tp_reduce")

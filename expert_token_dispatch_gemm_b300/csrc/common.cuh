@@ -108,13 +108,18 @@ struct LayerDims {
     int dtype;         // MOE_DTYPE_*
     int group_limit;   // partitions a token may use; 0 when unlimited
     const float *sel_bias;   // [E] selection-only bias or nullptr
+    int slot_priority;       // 1: capacity ranks pairs slot-major (j*N + t)
 };
+// Histogram segments of the dispatch scan: ceil(N/64) token segments, or in slot-major
+// priority k slots x ceil(N / 64k) token spans.
+int num_segments(const LayerDims &d);
 // Largest group limit and partition count of the group-limited routing.
 constexpr int kMaxGroupLimit = 8;
 constexpr int kMaxGroupPartitions = 64;
 
 cudaError_t launch_route(const LayerDims &d, const void *x, const void *w_router,
                          const float *b_router, int32_t *topk_idx, float *topk_w,
+                         float *logits /* [N, E] or nullptr */,
                          int32_t *seg_hist /* [nseg, E] or nullptr */, cudaStream_t s);
 
 cudaError_t launch_update_selection_bias(const LayerDims &d, const int32_t *routed_counts,
@@ -146,7 +151,18 @@ cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *exp
 // seg_hist and status may be null.
 cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_router,
                             const float *bias, int32_t *topk_idx, float *topk_w,
-                            int32_t *seg_hist, int32_t *status, int num_sms, cudaStream_t s);
+                            float *logits, int32_t *seg_hist, int32_t *status, int num_sms,
+                            cudaStream_t s);
+
+// Router load statistics: per-block partial sums of the token softmax [kStatsBlocks, E]
+// in `partials`, then load_frac / prob_mean. TP row split: ordered sum of tp padded
+// outputs.
+constexpr int kStatsBlocks = 256;
+cudaError_t launch_balance_stats(const LayerDims &d, const float *logits,
+                                 const int32_t *routed_counts, float *partials, float *load_frac,
+                                 float *prob_mean, cudaStream_t s);
+cudaError_t launch_tp_reduce(const LayerDims &d, int tp_size, const void *padded, void *out,
+                             cudaStream_t s);
 
 // fp32 FFMA grouped FFN.
 cudaError_t launch_simt_gate_up(const LayerDims &d, const float *send,

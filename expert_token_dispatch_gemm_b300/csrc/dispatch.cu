@@ -16,6 +16,12 @@
 //      with __match_any_sync, so a pair's rank is its segment base plus the number of
 //      earlier pairs of that expert.
 // Every step is deterministic, so counts, offsets, perm and slot_pos are bit-exact.
+//
+// Slot-major priority (GShard-style capacity, template SLOT): the pairs are ranked in
+// the order j*N + t -- every token's first choice, then every token's second choice --
+// and the same machinery runs over "virtual segments" of that order: segment v covers
+// slot j = v / S of the tokens [s*64k, (s+1)*64k), s = v mod S, S = ceil(N / 64k), so
+// a segment still holds at most 64k pairs. Its histograms come from histogram_kernel.
 #include <limits.h>
 
 #include "common.cuh"
@@ -23,6 +29,29 @@
 namespace moe {
 namespace {
 
+// The pairs of segment v in priority order: count() of them, the i-th is pair(i).
+template <bool SLOT>
+struct SegWalk {
+    int64_t p0;      // token order: first pair; slot order: first token
+    int count;
+    int k, j;
+    __device__ SegWalk(int v, int N, int k_) : k(k_) {
+        const int span = kSegTokens * k;
+        if (SLOT) {
+            const int S = (N + span - 1) / span;
+            j = v / S;
+            p0 = (int64_t)(v - j * S) * span;
+            count = (int)min((int64_t)span, (int64_t)N - p0);
+        } else {
+            j = 0;
+            p0 = (int64_t)v * span;
+            count = (int)min((int64_t)span, (int64_t)N * k - p0);
+        }
+    }
+    __device__ int64_t pair(int i) const { return SLOT ? (p0 + i) * k + j : p0 + i; }
+};
+
+template <bool SLOT>
 __global__ void histogram_kernel(const int32_t *__restrict__ idx, int N, int k, int E,
                                  int32_t *__restrict__ seg_hist, int32_t *status) {
     grid_dep_wait();
@@ -30,10 +59,9 @@ __global__ void histogram_kernel(const int32_t *__restrict__ idx, int N, int k, 
     __shared__ int hs[kMaxExperts];
     for (int e = threadIdx.x; e < E; e += blockDim.x) hs[e] = 0;
     __syncthreads();
-    const int64_t p0 = (int64_t)blockIdx.x * kSegTokens * k;
-    const int64_t p1 = min(p0 + (int64_t)kSegTokens * k, (int64_t)N * k);
-    for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-        const int e = idx[p];
+    const SegWalk<SLOT> w(blockIdx.x, N, k);
+    for (int i = threadIdx.x; i < w.count; i += blockDim.x) {
+        const int e = idx[w.pair(i)];
         if (e >= 0 && e < E)
             atomicAdd(&hs[e], 1);
         else
@@ -48,9 +76,10 @@ __global__ void histogram_kernel(const int32_t *__restrict__ idx, int N, int k, 
 // into the experts' routed totals and its own segments' rank bases, derives the kept
 // counts and the exclusive expert offsets, and assigns its segments' pairs exactly as
 // the separate scan and assign kernels do; CTA 0 writes the counts and offsets.
+template <bool SLOT>
 __global__ void __launch_bounds__(256)
 scan_assign_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ seg_hist, int N,
-                   int k, int E, int P, int capacity, int32_t *__restrict__ routed_counts,
+                   int nseg, int k, int E, int P, int capacity, int32_t *__restrict__ routed_counts,
                    int32_t *__restrict__ counts, int32_t *__restrict__ expert_offsets,
                    int32_t *__restrict__ part_offsets, int32_t *__restrict__ slot_pos,
                    int32_t *__restrict__ perm, int32_t *status) {
@@ -59,7 +88,6 @@ scan_assign_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ 
     __shared__ int tot_s[kMaxExperts], before_s[kMaxExperts], off_s[kMaxExperts + 1];
     __shared__ int base_s[8][kMaxExperts];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int nseg = (N + kSegTokens - 1) / kSegTokens;
     const int seg0 = blockIdx.x * 8;
     // routed totals and the counts of segments before this CTA's, per expert
     for (int e = tid; e < E; e += 256) {
@@ -154,12 +182,11 @@ scan_assign_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ 
         base[e] = b;
     }
     __syncwarp();
-    const int64_t p0 = (int64_t)seg * kSegTokens * k;
-    const int64_t p1 = min(p0 + (int64_t)kSegTokens * k, (int64_t)N * k);
+    const SegWalk<SLOT> walk(seg, N, k);
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int64_t pc = p0; pc < p1; pc += 32) {
-        const int64_t p = pc + lane;
-        const bool live = p < p1;
+    for (int ic = 0; ic < walk.count; ic += 32) {
+        const bool live = ic + lane < walk.count;
+        const int64_t p = live ? walk.pair(ic + lane) : 0;
         int e = live ? idx[p] : -1;
         const bool valid = live && e >= 0 && e < E;
         if (live && !valid) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
@@ -239,20 +266,27 @@ cudaError_t launch_update_selection_bias(const LayerDims &d, const int32_t *rout
                       (long long)d.N * d.k, routed_counts, selection_bias, gamma);
 }
 
+int num_segments(const LayerDims &d) {
+    if (d.slot_priority) return d.k * ceil_div(d.N, kSegTokens * d.k);
+    return ceil_div(d.N, kSegTokens);
+}
+
 cudaError_t launch_histogram(const LayerDims &d, const int32_t *topk_idx, int32_t *seg_hist,
                              int32_t *status, cudaStream_t s) {
-    const int nseg = ceil_div(d.N, kSegTokens);
-    return launch_pdl(histogram_kernel, dim3(nseg), dim3(256), 0, s, topk_idx, d.N, d.k, d.E,
-                      seg_hist, status);
+    const int nseg = num_segments(d);
+    if (nseg == 0) return cudaSuccess;
+    auto kern = d.slot_priority ? histogram_kernel<true> : histogram_kernel<false>;
+    return launch_pdl(kern, dim3(nseg), dim3(256), 0, s, topk_idx, d.N, d.k, d.E, seg_hist, status);
 }
 
 cudaError_t launch_scan_assign(const LayerDims &d, const int32_t *topk_idx, const int32_t *seg_hist,
                                int32_t *routed_counts, int32_t *counts, int32_t *expert_offsets,
                                int32_t *part_offsets, int32_t *slot_pos, int32_t *perm,
                                int32_t *status, cudaStream_t s) {
-    const int nseg = ceil_div(d.N, kSegTokens);
-    return launch_pdl(scan_assign_kernel, dim3(ceil_div(nseg, 8)), dim3(256), 0, s, topk_idx,
-                      seg_hist, d.N, d.k, d.E, d.P, d.capacity, routed_counts, counts,
+    const int nseg = num_segments(d);
+    auto kern = d.slot_priority ? scan_assign_kernel<true> : scan_assign_kernel<false>;
+    return launch_pdl(kern, dim3(std::max(1, ceil_div(nseg, 8))), dim3(256), 0, s, topk_idx,
+                      seg_hist, d.N, nseg, d.k, d.E, d.P, d.capacity, routed_counts, counts,
                       expert_offsets, part_offsets, slot_pos, perm, status);
 }
 

@@ -92,6 +92,9 @@ moe_status_t check_config(const moe_config *cfg, LayerDims *d) {
     if (cfg->selection_bias != nullptr && (reinterpret_cast<uintptr_t>(cfg->selection_bias) & 3u))
         return fail(MOE_ERR_INVALID_ARG, "selection_bias must be 4-byte aligned");
     d->sel_bias = cfg->selection_bias;
+    if (cfg->capacity_priority != MOE_PRIORITY_TOKEN && cfg->capacity_priority != MOE_PRIORITY_SLOT)
+        return fail(MOE_ERR_INVALID_ARG, "unknown capacity_priority %d", cfg->capacity_priority);
+    d->slot_priority = cfg->capacity_priority == MOE_PRIORITY_SLOT;
     if (cfg->capacity_factor > 0.f) {
         // cf * N * k is exact in double (24-bit cf times an integer below 2^29); if the
         // exact quotient by E is an integer the division returns it exactly, otherwise it
@@ -110,7 +113,8 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // Workspace layout, every region 256-byte aligned.
 struct Workspace {
     int32_t *status;       // [8]
-    int32_t *seg_hist;     // [nseg, E]
+    int32_t *seg_hist;     // [num_segments, E]
+    float *stats;          // [kStatsBlocks, E]
     int32_t *topk_idx;     // [N*k]
     float *topk_w;         // [N*k]
     int32_t *routed;       // [E]
@@ -134,10 +138,11 @@ Workspace carve(const LayerDims &d, int mode, void *base) {
         off += align256(bytes);
         return r;
     };
-    const size_t nseg = (size_t)ceil_div(d.N, kSegTokens);
+    const size_t nseg = (size_t)num_segments(d);
     const size_t pairs = (size_t)d.N * d.k;
     w.status = (int32_t *)take(8 * sizeof(int32_t));
     w.seg_hist = (int32_t *)take(nseg * d.E * sizeof(int32_t));
+    w.stats = (float *)take((size_t)kStatsBlocks * d.E * sizeof(float));
     w.topk_idx = (int32_t *)take(pairs * sizeof(int32_t));
     w.topk_w = (float *)take(pairs * sizeof(float));
     w.routed = (int32_t *)take(d.E * sizeof(int32_t));
@@ -186,14 +191,16 @@ int num_sms() {
 // --------------------------------------------------------------- step bodies
 // bf16 layers route on the tensor cores; fp32 layers on the FFMA router (single-pass
 // TF32 would round the fp32 inputs). `hist` (may be null) receives the segment
-// histogram; `status` (may be null) the device status bits.
+// histogram, `logits` (may be null) the logits, `status` (may be null) the device
+// status bits.
 moe_status_t run_route(const LayerDims &d, const void *x, const void *wr, const float *b,
-                       int32_t *idx, float *w, int32_t *hist, int32_t *status, cudaStream_t s) {
+                       int32_t *idx, float *w, float *logits, int32_t *hist, int32_t *status,
+                       cudaStream_t s) {
     if (d.dtype == MOE_DTYPE_BF16)
-        MOE_CUDA(launch_tc_route(d, x, wr, b, idx, w, hist, status, num_sms(), s),
+        MOE_CUDA(launch_tc_route(d, x, wr, b, idx, w, logits, hist, status, num_sms(), s),
                  "tensor-core route kernel");
     else
-        MOE_CUDA(launch_route(d, x, wr, b, idx, w, hist, s), "route kernel");
+        MOE_CUDA(launch_route(d, x, wr, b, idx, w, logits, hist, s), "route kernel");
     return MOE_OK;
 }
 
@@ -347,7 +354,7 @@ moe_status_t moe_route(const moe_config *cfg, const void *x, const void *w_route
     NEED(topk_w, false);
     g_last_error.clear();
     return run_route(d, x, w_router, cfg->has_bias ? b_router : nullptr, topk_idx, topk_w, nullptr,
-                     nullptr, (cudaStream_t)stream);
+                     nullptr, nullptr, (cudaStream_t)stream);
 }
 
 moe_status_t moe_update_selection_bias(const moe_config *cfg, const int32_t *routed_counts,
@@ -490,11 +497,16 @@ moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void 
         if (st != MOE_OK) return st; \
     } while (0)
 
+    if (g.router_logits) NEED(g.router_logits, true);
     MOE_MARK(MOE_STAGE_ROUTE);
-    st = run_route(d, x, w_router, cfg->has_bias ? b_router : nullptr, idx, tw, w.seg_hist,
-                   w.status, s);
+    // slot-major priority ranks pairs in another order than the router's per-token
+    // segment histogram: its histograms come from the histogram kernel instead
+    st = run_route(d, x, w_router, cfg->has_bias ? b_router : nullptr, idx, tw, g.router_logits,
+                   d.slot_priority ? nullptr : w.seg_hist, w.status, s);
     if (st != MOE_OK) return st;
     MOE_MARK(MOE_STAGE_SCAN);
+    if (d.slot_priority)
+        MOE_CUDA(launch_histogram(d, idx, w.seg_hist, w.status, s), "histogram kernel");
     MOE_CUDA(launch_scan_assign(d, idx, w.seg_hist, routed, counts, eoff, poff, slot_pos, perm,
                                 w.status, s),
              "scan/assign kernel");
@@ -548,12 +560,12 @@ moe_status_t moe_dispatch_noalloc(const moe_config *cfg, const int32_t *topk_idx
     LayerDims d;
     moe_status_t st = check_config(cfg, &d);
     if (st != MOE_OK) return st;
-    const int64_t seg_experts = (int64_t)ceil_div(d.N, kSegTokens) * d.E;
+    const int64_t seg_experts = (int64_t)num_segments(d) * d.E;
     if (seg_experts > kNoAllocMaxSegExperts)
         return fail(MOE_ERR_UNSUPPORTED,
-                    "moe_dispatch_noalloc: ceil(num_tokens/%d) * num_experts = %lld exceeds its "
-                    "fixed scratch of %d; use moe_dispatch with a workspace",
-                    kSegTokens, (long long)seg_experts, kNoAllocMaxSegExperts);
+                    "moe_dispatch_noalloc: %lld histogram segments x num_experts = %lld exceeds "
+                    "its fixed scratch of %d; use moe_dispatch with a workspace",
+                    (long long)num_segments(d), (long long)seg_experts, kNoAllocMaxSegExperts);
     NEED(routed_counts, false);
     NEED(counts, false);
     NEED(expert_offsets, false);
@@ -587,6 +599,59 @@ moe_status_t moe_dispatch_noalloc(const moe_config *cfg, const int32_t *topk_idx
     MOE_CUDA(launch_histogram(d, topk_idx, w.seg_hist, w.status, s), "histogram kernel");
     return run_dispatch_from_hist(d, topk_idx, x, w, routed_counts, counts, expert_offsets,
                                   part_offsets, perm, slot_pos, send, s);
+}
+
+moe_status_t moe_balance_stats(const moe_config *cfg, const float *router_logits,
+                               const int32_t *routed_counts, float *load_frac, float *prob_mean,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    Workspace w;
+    st = check_workspace(d, cfg->mode, workspace, workspace_bytes, &w);
+    if (st != MOE_OK) return st;
+    NEED(routed_counts, false);
+    NEED(load_frac, false);
+    NEED(prob_mean, false);
+    cudaStream_t s = (cudaStream_t)stream;
+    g_last_error.clear();
+    if (d.N == 0) {   // no tokens: both statistics are zero
+        MOE_CUDA(cudaMemsetAsync(load_frac, 0, d.E * sizeof(float), s), "memset");
+        MOE_CUDA(cudaMemsetAsync(prob_mean, 0, d.E * sizeof(float), s), "memset");
+        return MOE_OK;
+    }
+    NEED(router_logits, false);
+    MOE_CUDA(launch_balance_stats(d, router_logits, routed_counts, w.stats, load_frac, prob_mean, s),
+             "balance statistics kernels");
+    return MOE_OK;
+}
+
+moe_status_t moe_tp_slice(int64_t num_tokens, int32_t tp_size, int32_t tp_rank, int64_t *begin,
+                          int64_t *end) {
+    if (num_tokens < 0) return fail(MOE_ERR_INVALID_ARG, "num_tokens must be >= 0");
+    if (tp_size < 1) return fail(MOE_ERR_INVALID_ARG, "tp_size must be >= 1 (got %d)", tp_size);
+    if (tp_rank < 0 || tp_rank >= tp_size)
+        return fail(MOE_ERR_INVALID_ARG, "tp_rank %d not in [0, %d)", tp_rank, tp_size);
+    if (begin == nullptr || end == nullptr) return fail(MOE_ERR_INVALID_ARG, "begin/end is NULL");
+    const int64_t q = num_tokens / tp_size, r = num_tokens % tp_size;
+    *begin = tp_rank * q + std::min<int64_t>(tp_rank, r);
+    *end = *begin + q + (tp_rank < r ? 1 : 0);
+    g_last_error.clear();
+    return MOE_OK;
+}
+
+moe_status_t moe_tp_reduce(const moe_config *cfg, int32_t tp_size, const void *padded, void *out,
+                           void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    if (tp_size < 1) return fail(MOE_ERR_INVALID_ARG, "tp_size must be >= 1 (got %d)", tp_size);
+    if (d.N == 0) return MOE_OK;
+    NEED(padded, true);
+    NEED(out, true);
+    g_last_error.clear();
+    MOE_CUDA(launch_tp_reduce(d, tp_size, padded, out, (cudaStream_t)stream), "TP reduce kernel");
+    return MOE_OK;
 }
 
 }  // extern "C"

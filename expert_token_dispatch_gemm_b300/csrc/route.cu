@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__restrict__ bias,
              const float *__restrict__ sel_bias, int group_limit, int P, int N, int H, int E,
              int k, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
-             int32_t *__restrict__ seg_hist) {
+             int32_t *__restrict__ seg_hist, float *__restrict__ logits_out) {
     grid_dep_wait();
     grid_dep_trigger();
     constexpr int TB = kSegTokens;
@@ -89,6 +89,11 @@ route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__r
             lg[(tg + r * TGN) * (EP + 1) + e] = v;
         }
     __syncthreads();
+    if (logits_out != nullptr)   // optional copy for load statistics, coalesced
+        for (int i = tid; i < TB * E; i += kRouteThreads) {
+            const int r = i / E, e = i - r * E;
+            if (t0 + r < N) logits_out[(size_t)(t0 + r) * E + e] = lg[r * (EP + 1) + e];
+        }
 
     // top-k: one warp per token. Selection on logit + selection bias (a NaN ranks
     // last), optionally among the experts of the group_limit best partitions; the
@@ -209,7 +214,7 @@ route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__r
 
 template <typename T, int RE, int EG>
 cudaError_t launch_route_t(const LayerDims &d, const T *x, const T *wr, const float *b,
-                           int32_t *idx, float *w, int32_t *hist, cudaStream_t s) {
+                           int32_t *idx, float *w, int32_t *hist, float *lgo, cudaStream_t s) {
     constexpr int EP = RE * EG;
     const size_t stage = (size_t)(kSegTokens + EP) * (route_k_chunk(EP) + 1) * sizeof(float);
     const size_t logits = (size_t)kSegTokens * (EP + 1) * sizeof(float);
@@ -222,33 +227,33 @@ cudaError_t launch_route_t(const LayerDims &d, const T *x, const T *wr, const fl
     }
     const int grid = ceil_div(d.N, kSegTokens);
     return launch_pdl(kern, dim3(grid), dim3(kRouteThreads), smem, s, x, wr, b, d.sel_bias,
-                      d.group_limit, d.P, d.N, d.H, d.E, d.k, idx, w, hist);
+                      d.group_limit, d.P, d.N, d.H, d.E, d.k, idx, w, hist, lgo);
 }
 
 template <typename T>
 cudaError_t launch_route_dt(const LayerDims &d, const T *x, const T *wr, const float *b,
-                            int32_t *idx, float *w, int32_t *hist, cudaStream_t s) {
+                            int32_t *idx, float *w, int32_t *hist, float *lgo, cudaStream_t s) {
     // experts per thread RE and expert groups EG, EP = RE*EG >= E
-    if (d.E <= 4) return launch_route_t<T, 1, 4>(d, x, wr, b, idx, w, hist, s);
-    if (d.E <= 8) return launch_route_t<T, 1, 8>(d, x, wr, b, idx, w, hist, s);
-    if (d.E <= 16) return launch_route_t<T, 1, 16>(d, x, wr, b, idx, w, hist, s);
-    if (d.E <= 32) return launch_route_t<T, 2, 16>(d, x, wr, b, idx, w, hist, s);
-    if (d.E <= 64) return launch_route_t<T, 4, 16>(d, x, wr, b, idx, w, hist, s);
-    if (d.E <= 128) return launch_route_t<T, 8, 16>(d, x, wr, b, idx, w, hist, s);
-    return launch_route_t<T, 16, 16>(d, x, wr, b, idx, w, hist, s);
+    if (d.E <= 4) return launch_route_t<T, 1, 4>(d, x, wr, b, idx, w, hist, lgo, s);
+    if (d.E <= 8) return launch_route_t<T, 1, 8>(d, x, wr, b, idx, w, hist, lgo, s);
+    if (d.E <= 16) return launch_route_t<T, 1, 16>(d, x, wr, b, idx, w, hist, lgo, s);
+    if (d.E <= 32) return launch_route_t<T, 2, 16>(d, x, wr, b, idx, w, hist, lgo, s);
+    if (d.E <= 64) return launch_route_t<T, 4, 16>(d, x, wr, b, idx, w, hist, lgo, s);
+    if (d.E <= 128) return launch_route_t<T, 8, 16>(d, x, wr, b, idx, w, hist, lgo, s);
+    return launch_route_t<T, 16, 16>(d, x, wr, b, idx, w, hist, lgo, s);
 }
 
 }  // namespace
 
 cudaError_t launch_route(const LayerDims &d, const void *x, const void *w_router,
                          const float *b_router, int32_t *topk_idx, float *topk_w,
-                         int32_t *seg_hist, cudaStream_t s) {
+                         float *logits, int32_t *seg_hist, cudaStream_t s) {
     if (d.dtype == MOE_DTYPE_BF16)
         return launch_route_dt<__nv_bfloat16>(d, (const __nv_bfloat16 *)x,
                                               (const __nv_bfloat16 *)w_router, b_router,
-                                              topk_idx, topk_w, seg_hist, s);
+                                              topk_idx, topk_w, seg_hist, logits, s);
     return launch_route_dt<float>(d, (const float *)x, (const float *)w_router, b_router,
-                                  topk_idx, topk_w, seg_hist, s);
+                                  topk_idx, topk_w, seg_hist, logits, s);
 }
 
 }  // namespace moe

@@ -55,6 +55,7 @@ struct RouteParams {
     int32_t *route_idx;      // [N, k] out
     float *route_w;          // [N, k] out
     int32_t *seg_hist;       // [nseg, E] or nullptr
+    float *logits;           // [N, E] out (logit + router bias) or nullptr
     int32_t *status;         // or nullptr
 };
 
@@ -249,6 +250,20 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                     isnan(l) ? -INFINITY : l, e);
             }
         };
+        // optional copy of the token's logits (with the router bias) for load statistics
+        auto store_logits = [&](const float (&v)[32], int c) {
+            if (p.logits == nullptr || tok >= p.rows) return;
+            float *dst = p.logits + (size_t)tok * p.E + c;
+            if (c + 32 <= p.E && (p.E & 3) == 0) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) =
+                        make_float4(v[j] + bias_s[c + j], v[j + 1] + bias_s[c + j + 1],
+                                    v[j + 2] + bias_s[c + j + 2], v[j + 3] + bias_s[c + j + 3]);
+            } else {
+                for (int j = 0; j < 32 && c + j < p.E; ++j) dst[j] = v[j] + bias_s[c + j];
+            }
+        };
         if (ok) {
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
             if (MODE == ROUTE_GROUP) {
@@ -295,6 +310,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                         const int e = c + j;
                         if (e < p.E && ((allowed >> (e / p.per_part)) & 1ull)) push(v[j], e);
                     }
+                    store_logits(v, c);
                 }
             } else {
                 const int cps = (p.bn + 32 * SLICES - 1) / (32 * SLICES) * 32;   // columns per slice
@@ -307,6 +323,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                         const int e = c + j;
                         if (e < p.E) push(v[j], e);
                     }
+                    store_logits(v, c);
                 }
             }
             if (SLICES > 1) {
@@ -464,7 +481,8 @@ cudaError_t tc::make_map(CUtensorMap *map, const void *base, uint64_t rows, uint
 
 cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_router,
                             const float *bias, int32_t *topk_idx, float *topk_w,
-                            int32_t *seg_hist, int32_t *status, int num_sms, cudaStream_t s) {
+                            float *logits, int32_t *seg_hist, int32_t *status, int num_sms,
+                            cudaStream_t s) {
     const int bn = (d.E + 15) / 16 * 16;
     CUtensorMap mx, mw;
     cudaError_t e = tc::make_map(&mx, x, d.N, d.H, d.H, BM);
@@ -488,6 +506,7 @@ cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_rou
     prm.route_idx = topk_idx;
     prm.route_w = topk_w;
     prm.seg_hist = seg_hist;
+    prm.logits = logits;
     prm.status = status;
     const int tiles = ceil_div(d.N, BM);
     // the register list holds k rounded up to a power of two

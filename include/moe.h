@@ -55,6 +55,8 @@ typedef enum moe_status_t {
 
 enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP32 = 1 };
 enum { MOE_MODE_DISPATCH = 0, MOE_MODE_MASK_SUM = 1 };
+/* Order in which a capacity limit ranks an expert's pairs (moe_config.capacity_priority). */
+enum { MOE_PRIORITY_TOKEN = 0, MOE_PRIORITY_SLOT = 1 };
 
 /* Device status word bits (moe_read_device_status). */
 enum {
@@ -97,6 +99,15 @@ enum {
  *  selection_bias   NULL, or fp32 [E] device array added to the logits for choosing
  *                   experts only; the routing weights remain the softmax of the chosen
  *                   experts' own logits. moe_update_selection_bias adjusts it.
+ *
+ * Capacity priority (Ultralytics page, "Load balancing and capacity"; the order in which
+ * an over-full expert keeps pairs is left open there):
+ *  capacity_priority  MOE_PRIORITY_TOKEN (0): an expert's pairs are ranked by token
+ *                   index. MOE_PRIORITY_SLOT (1), GShard-style: ranked slot-major --
+ *                   every token's first choice before any token's second choice, then by
+ *                   token -- so pair (t, j) has priority j*N + t. The rank decides which
+ *                   pairs the capacity keeps and orders the rows of the expert's segment
+ *                   in the send layout.
  */
 typedef struct moe_config {
     int64_t num_tokens;
@@ -111,6 +122,7 @@ typedef struct moe_config {
     int32_t has_bias;
     int32_t group_limit;
     const float *selection_bias;
+    int32_t capacity_priority;
 } moe_config;
 
 /* Stage boundaries recorded by moe_layer_forward when moe_diagnostics.stage_events is
@@ -141,6 +153,9 @@ typedef struct moe_diagnostics {
     /* NULL, or MOE_NUM_STAGES + 1 cudaEvent_t handles (created by the caller) to record
      * at the stage boundaries, for per-kernel timing on the caller's stream. */
     void *const *stage_events;
+    /* NULL, or fp32 [N, E], 16-byte aligned: the router logits with the router bias
+     * (without the selection bias), for moe_balance_stats. */
+    float *router_logits;
 } moe_diagnostics;
 
 /* Human-readable name of a status code (static string). */
@@ -312,6 +327,42 @@ moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void 
 moe_status_t moe_read_device_status(const moe_config *cfg, void *workspace,
                                     size_t workspace_bytes, int32_t *flags, int32_t reset,
                                     void *stream);
+
+/*
+ * Router load statistics (Ultralytics page, "Load balancing and capacity": an auxiliary
+ * loss term encourages the router to spread tokens evenly; the page gives no formula,
+ * so this computes the two per-expert quantities such a term is built from, not a
+ * loss):
+ *   load_frac[e] = routed_counts[e] / (N * k)    share of the step's routed pairs
+ *   prob_mean[e] = mean over the N tokens of softmax(router_logits[t])[e]
+ *   router_logits  [N, E] fp32 (moe_diagnostics.router_logits of moe_layer_forward)
+ *   routed_counts  [E] int32 (before capacity)
+ *   load_frac, prob_mean  [E] fp32 out
+ * Deterministic (fixed summation order). N = 0 gives zeros. Uses the workspace.
+ */
+moe_status_t moe_balance_stats(const moe_config *cfg, const float *router_logits,
+                               const int32_t *routed_counts, float *load_frac, float *prob_mean,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * TP row split (Hugging Face page, "With tensor parallelism"): the tp_size ranks of a TP
+ * group hold the same batch; each dispatches a disjoint slice of its tokens, and an
+ * all-reduce over the group of the zero-padded slice outputs restores the full output.
+ *
+ * moe_tp_slice: the token rows [*begin, *end) of rank tp_rank: contiguous slices, the
+ * first num_tokens mod tp_size ranks one token longer; slices may be empty (for
+ * example a single decode token with tp_size 2). Host only; enqueues nothing.
+ *
+ * moe_tp_reduce: out = padded[0] + padded[1] + ... + padded[tp_size-1] (fp32
+ * accumulation in rank order, rounded once to dtype), the single-device stand-in for
+ * the all-reduce. padded is [tp_size, N, H] dtype, slice s's output at its rows and
+ * zeros elsewhere (each slice is one moe_layer_forward over its rows, whose output
+ * pointer is padded + (s*N + begin_s)*H); out is [N, H] dtype. Both 16-byte aligned.
+ */
+moe_status_t moe_tp_slice(int64_t num_tokens, int32_t tp_size, int32_t tp_rank, int64_t *begin,
+                          int64_t *end);
+moe_status_t moe_tp_reduce(const moe_config *cfg, int32_t tp_size, const void *padded, void *out,
+                           void *stream);
 
 #ifdef __cplusplus
 }

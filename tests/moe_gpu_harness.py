@@ -17,11 +17,13 @@ def tol_for(shape) -> float:
     return BF16_TOL if shape.dtype == "bf16" else FP32_TOL
 
 
-def make_cfg(shape, mode="dispatch", N=None, group_limit=0, selection_bias=None):
+def make_cfg(shape, mode="dispatch", N=None, group_limit=0, selection_bias=None,
+             capacity_priority="token"):
     return moe.config(shape.N if N is None else N, shape.H, shape.I, shape.E, shape.top_k,
                       shape.ep_size, shape.capacity_factor, mode, shape.dtype,
                       has_bias=shape.bias or shape.zipf_s is not None,
-                      group_limit=group_limit, selection_bias=selection_bias)
+                      group_limit=group_limit, selection_bias=selection_bias,
+                      capacity_priority=capacity_priority)
 
 
 def f64(t):
@@ -31,13 +33,15 @@ def f64(t):
 class Layer:
     """Device copies of one layer's inputs plus packed weights and a workspace."""
 
-    def __init__(self, shape, inputs, mode="dispatch", group_limit=0, selection_bias=None):
+    def __init__(self, shape, inputs, mode="dispatch", group_limit=0, selection_bias=None,
+                 capacity_priority="token"):
         self.shape, self.mode = shape, mode
         dev = "cuda"
         # the config holds the selection bias' device address: keep the tensor alive
         self.sel_bias = (None if selection_bias is None
                          else torch.as_tensor(selection_bias, dtype=torch.float32).to(dev))
-        self.cfg = make_cfg(shape, mode, group_limit=group_limit, selection_bias=self.sel_bias)
+        self.cfg = make_cfg(shape, mode, group_limit=group_limit, selection_bias=self.sel_bias,
+                            capacity_priority=capacity_priority)
         self.x = inputs["x"].to(dev).contiguous()
         self.w_router = inputs["w_router"].to(dev).contiguous()
         b = inputs["b_router"]
@@ -95,7 +99,8 @@ class Layer:
         return moe.moe_read_device_status(self.cfg, self.ws, reset=True)
 
 
-def oracle_layer(shape, inputs, mode="dispatch", group_limit=None, selection_bias=None):
+def oracle_layer(shape, inputs, mode="dispatch", group_limit=None, selection_bias=None,
+                 capacity_priority="token"):
     b = inputs["b_router"]
     return oracle.layer_forward(f64(inputs["x"]), f64(inputs["w_router"]),
                                 None if b is None else f64(b), f64(inputs["w_gate"]),
@@ -103,7 +108,8 @@ def oracle_layer(shape, inputs, mode="dispatch", group_limit=None, selection_bia
                                 shape.ep_size, shape.capacity_factor, mode,
                                 selection_bias=(None if selection_bias is None
                                                 else np.asarray(selection_bias, np.float64)),
-                                group_limit=group_limit or None)
+                                group_limit=group_limit or None,
+                                capacity_priority=capacity_priority)
 
 
 def assert_routing_and_layout_exact(diag, ref, shape):

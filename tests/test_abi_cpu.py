@@ -83,6 +83,7 @@ def status_of(moe, c):
     (dict(group_limit=4), 0),                      # >= ep_size: no limit
     (dict(E=128, ep_size=16, group_limit=9), 2),   # beyond the supported group limit
     (dict(E=128, ep_size=128, group_limit=2), 2),  # beyond the supported partition count
+    (dict(capacity_priority="slot"), 0),
 ])
 def test_config_validation(moe, kw, status):
     c = cfg(moe, **kw)
@@ -173,3 +174,46 @@ def test_misaligned_selection_bias_is_rejected_before_any_access(moe):
     c.selection_bias = 0x1002     # never dereferenced: validation comes first
     st, _ = status_of(moe, c)
     assert st == 1 and b"selection_bias" in moe.lib.moe_last_error()
+
+
+def test_unknown_capacity_priority_is_rejected(moe):
+    c = cfg(moe)
+    c.capacity_priority = 2
+    st, _ = status_of(moe, c)
+    assert st == 1 and b"capacity_priority" in moe.lib.moe_last_error()
+    with pytest.raises(ValueError):
+        moe.config(N=8, H=64, I=32, E=8, top_k=2, ep_size=4, capacity_priority="expert")
+
+
+def test_slot_priority_workspace_holds_its_histograms(moe):
+    # k slots x ceil(N / 64k) spans of histograms instead of ceil(N / 64) segments
+    _, tok = status_of(moe, cfg(moe, N=4096, E=64, top_k=8, ep_size=8))
+    _, slot = status_of(moe, cfg(moe, N=4096, E=64, top_k=8, ep_size=8, capacity_priority="slot"))
+    assert slot >= tok
+
+
+@pytest.mark.parametrize("N,tp", [(0, 1), (0, 3), (1, 2), (1, 4), (7, 3), (8, 2), (5, 8),
+                                  (100, 3), (32768, 7)])
+def test_tp_slice_matches_the_oracle_rule(moe, N, tp):
+    import oracle
+    got = [moe.moe_tp_slice(N, tp, r) for r in range(tp)]
+    assert got == oracle.tp_slices(N, tp)
+
+
+@pytest.mark.parametrize("args", [(-1, 2, 0), (4, 0, 0), (4, 2, 2), (4, 2, -1)])
+def test_tp_slice_rejects_bad_arguments(moe, args):
+    with pytest.raises(moe.MoeError):
+        moe.moe_tp_slice(*args)
+
+
+def test_balance_stats_and_tp_reduce_validate_before_any_access(moe):
+    c = cfg(moe)
+    ws = ctypes.c_void_p(1 << 20)
+    st = moe.lib.moe_balance_stats(ctypes.byref(c), FAKE, None, FAKE, FAKE, ws, 1 << 30, None)
+    assert st == 1 and b"routed_counts" in moe.lib.moe_last_error()
+    st = moe.lib.moe_balance_stats(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, ws, 16, None)
+    assert st == 3                                           # workspace too small
+    st = moe.lib.moe_tp_reduce(ctypes.byref(c), 0, FAKE, FAKE, None)
+    assert st == 1
+    st = moe.lib.moe_tp_reduce(ctypes.byref(c), 2, ctypes.c_void_p((1 << 20) + 4), FAKE, None)
+    assert st == 1 and b"aligned" in moe.lib.moe_last_error()
