@@ -39,7 +39,7 @@ class MoeConfig(ctypes.Structure):
                 ("capacity_factor", ctypes.c_float), ("mode", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("has_bias", ctypes.c_int32),
                 ("group_limit", ctypes.c_int32), ("selection_bias", ctypes.c_void_p),
-                ("capacity_priority", ctypes.c_int32)]
+                ("capacity_priority", ctypes.c_int32), ("training", ctypes.c_int32)]
 
     @property
     def torch_dtype(self):
@@ -82,6 +82,7 @@ def _load():
                                              ctypes.POINTER(MoeDiagnostics), P, S, P]),
         "moe_read_device_status": (ctypes.c_int, [cfgp, P, S, ctypes.POINTER(I32), I32, P]),
         "moe_balance_stats": (ctypes.c_int, [cfgp, P, P, P, P, P, S, P]),
+        "moe_layer_backward": (ctypes.c_int, [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
         "moe_tp_slice": (ctypes.c_int, [ctypes.c_int64, I32, I32, ctypes.POINTER(ctypes.c_int64),
                                         ctypes.POINTER(ctypes.c_int64)]),
         "moe_tp_reduce": (ctypes.c_int, [cfgp, I32, P, P, P]),
@@ -98,7 +99,7 @@ lib = _load()
 
 def config(N, H, I, E, top_k, ep_size, capacity_factor=None, mode="dispatch",
            dtype="bf16", has_bias=False, group_limit=0, selection_bias=None,
-           capacity_priority="token") -> MoeConfig:
+           capacity_priority="token", training=False) -> MoeConfig:
     """struct moe_config. selection_bias: None or an fp32 [E] CUDA tensor, which the
     caller keeps alive while the config is in use. capacity_priority: "token" or
     "slot"."""
@@ -111,7 +112,8 @@ def config(N, H, I, E, top_k, ep_size, capacity_factor=None, mode="dispatch",
                      int(group_limit or 0),
                      None if selection_bias is None
                      else _ptr(selection_bias, "selection_bias", torch.float32).value,
-                     MOE_PRIORITY_SLOT if capacity_priority == "slot" else MOE_PRIORITY_TOKEN)
+                     MOE_PRIORITY_SLOT if capacity_priority == "slot" else MOE_PRIORITY_TOKEN,
+                     int(bool(training)))
 
 
 def _check(status: int, func: str):
@@ -292,3 +294,18 @@ def moe_tp_reduce(cfg, tp_size, padded, out):
     dt = cfg.torch_dtype
     _check(lib.moe_tp_reduce(ctypes.byref(cfg), int(tp_size), _ptr(padded, "padded", dt),
                              _ptr(out, "out", dt), _stream()), "moe_tp_reduce")
+
+
+def moe_layer_backward(cfg, x, w_router, w_gate_up_packed, w_down, dout, dx, dw_router, db_router,
+                       dw_gate, dw_up, dw_down, workspace):
+    """Gradients of the layer (moe.h); after moe_layer_forward with cfg.training = 1 and
+    the same workspace."""
+    dt = cfg.torch_dtype
+    f32 = torch.float32
+    _check(lib.moe_layer_backward(
+        ctypes.byref(cfg), _ptr(x, "x", dt), _ptr(w_router, "w_router", dt),
+        _ptr(w_gate_up_packed, "w_gate_up_packed", dt), _ptr(w_down, "w_down", dt),
+        _ptr(dout, "dout", dt), _ptr(dx, "dx", dt), _ptr(dw_router, "dw_router", f32),
+        _ptr(db_router, "db_router", f32), _ptr(dw_gate, "dw_gate", dt), _ptr(dw_up, "dw_up", dt),
+        _ptr(dw_down, "dw_down", dt), _ptr(workspace, "workspace"), workspace.numel(), _stream()),
+        "moe_layer_backward")

@@ -1,0 +1,173 @@
+// Backward of the router and of the combine step (the chain rule through step 1 and
+// step 4 of the Ultralytics glossary "Expert Parallelism": the output is the routing-
+// weighted sum of the experts' outputs, the weights a softmax over the chosen logits).
+//
+//   dweight[t, j] = <dout_t, y_tj> for a kept pair (summed from the per-M-tile partials
+//                   of the dgrad-down epilogue, in tile order), 0 for a dropped one;
+//   dl[t, j]      = w_tj (dweight_tj - sum_j' w_tj' dweight_tj')   (softmax Jacobian;
+//                   a dropped pair's weight still enters the softmax, so it still gets
+//                   a logit gradient);
+//   dx[t]         = sum_j over kept pairs of dx_slots[t k + j] + sum_j dl_tj W_r[e_tj]
+//                   (fp32, in slot order, then the router rows in slot order);
+//   dW_r[e]       = sum over the pairs routed to e, in token order, of dl x_t;
+//   db_r[e]       = sum of the same dl.
+// The selection is piecewise constant, so the selection bias gets no gradient.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(256)
+router_dl_kernel(int N, int k, int m_tiles, int rows, const float *__restrict__ dweight_part,
+                 const int32_t *__restrict__ slot_pos, const float *__restrict__ topk_w,
+                 float *__restrict__ dl) {
+    grid_dep_wait();
+    grid_dep_trigger();
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= N) return;
+    float s = 0.f;
+    for (int j = 0; j < k; ++j) {
+        const size_t pr = (size_t)t * k + j;
+        const int slot = slot_pos[pr];
+        float dw = 0.f;
+        if (slot >= 0)
+            for (int f = 0; f < m_tiles; ++f) dw += dweight_part[(size_t)f * rows + slot];
+        dl[pr] = dw;
+        s = fmaf(topk_w[pr], dw, s);
+    }
+    for (int j = 0; j < k; ++j) {
+        const size_t pr = (size_t)t * k + j;
+        dl[pr] = topk_w[pr] * (dl[pr] - s);
+    }
+}
+
+// One warp per token, 16-byte vectors of 8 bf16.
+__global__ void __launch_bounds__(256)
+dx_combine_kernel(const __nv_bfloat16 *__restrict__ dx_slots, const int32_t *__restrict__ slot_pos,
+                  const int32_t *__restrict__ topk_idx, const float *__restrict__ dl,
+                  const __nv_bfloat16 *__restrict__ w_router, int N, int H, int k,
+                  __nv_bfloat16 *__restrict__ dx) {
+    grid_dep_wait();
+    grid_dep_trigger();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= N) return;
+    const int my_slot = lane < k ? slot_pos[(size_t)t * k + lane] : -1;
+    const int my_e = lane < k ? topk_idx[(size_t)t * k + lane] : 0;
+    const float my_dl = lane < k ? dl[(size_t)t * k + lane] : 0.f;
+    const int nvec = H / 8;
+    for (int v = lane; v < nvec; v += 32) {
+        float acc[8] = {};
+        for (int j = 0; j < k; ++j) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+            if (slot < 0) continue;
+            float f[8];
+            Vec16<__nv_bfloat16>::to_float(
+                __ldg(reinterpret_cast<const uint4 *>(dx_slots + ((size_t)t * k + j) * H) + v), f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] += f[c];
+        }
+        for (int j = 0; j < k; ++j) {
+            const int e = __shfl_sync(0xffffffffu, my_e, j);
+            const float c0 = __shfl_sync(0xffffffffu, my_dl, j);
+            float f[8];
+            Vec16<__nv_bfloat16>::to_float(
+                __ldg(reinterpret_cast<const uint4 *>(w_router + (size_t)e * H) + v), f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] = fmaf(c0, f[c], acc[c]);
+        }
+        reinterpret_cast<uint4 *>(dx + (size_t)t * H)[v] = Vec16<__nv_bfloat16>::from_float(acc);
+    }
+}
+
+// Block (expert e, column chunk of 2048, split z): the z-th contiguous part of e's
+// routed pairs, in order; partial [Z, E, H] fp32, and the part's sum of dl.
+__global__ void __launch_bounds__(256)
+router_wgrad_partial_kernel(const int32_t *__restrict__ eoff_all, const int32_t *__restrict__ perm_all,
+                            const float *__restrict__ dl, const __nv_bfloat16 *__restrict__ x,
+                            int H, int E, int k, float *__restrict__ partial,
+                            float *__restrict__ partial_db) {
+    grid_dep_wait();
+    grid_dep_trigger();
+    const int e = blockIdx.x, z = blockIdx.z, Z = gridDim.z;
+    const int r0 = eoff_all[e], n = eoff_all[e + 1] - r0;
+    const int a = r0 + (int)((int64_t)n * z / Z), b = r0 + (int)((int64_t)n * (z + 1) / Z);
+    const int col = (blockIdx.y * 256 + threadIdx.x) * 8;
+    float acc[8] = {};
+    float db = 0.f;
+    if (col < H) {
+        for (int r = a; r < b; ++r) {
+            const int pr = perm_all[r];
+            const float c0 = dl[pr];
+            float f[8];
+            Vec16<__nv_bfloat16>::to_float(
+                __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(pr / k) * H + col)), f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] = fmaf(c0, f[c], acc[c]);
+            db += c0;
+        }
+        float *dst = partial + ((size_t)z * E + e) * H + col;
+        *reinterpret_cast<float4 *>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4 *>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    if (blockIdx.y == 0 && threadIdx.x == 0) partial_db[(size_t)z * E + e] = db;
+}
+
+__global__ void __launch_bounds__(256)
+router_wgrad_reduce_kernel(const float *__restrict__ partial, const float *__restrict__ partial_db,
+                           int Z, int E, int H, float *__restrict__ dw_router,
+                           float *__restrict__ db_router) {
+    grid_dep_wait();
+    grid_dep_trigger();
+    const size_t n = (size_t)E * H;
+    for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
+        float s = 0.f;
+        for (int z = 0; z < Z; ++z) s += partial[(size_t)z * n + i];
+        dw_router[i] = s;
+    }
+    if (db_router != nullptr && blockIdx.x == 0)
+        for (int e = threadIdx.x; e < E; e += 256) {
+            float s = 0.f;
+            for (int z = 0; z < Z; ++z) s += partial_db[(size_t)z * E + e];
+            db_router[e] = s;
+        }
+}
+
+}  // namespace
+
+int router_wgrad_splits(const LayerDims &d) {
+    const int chunks = ceil_div(d.H, 2048);
+    const int z = (148 * 4) / std::max(1, d.E * chunks);
+    return std::max(1, std::min(z, 64));
+}
+
+cudaError_t launch_router_dl(const LayerDims &d, const float *dweight_part, int m_tiles,
+                             const int32_t *slot_pos, const float *topk_w, float *dl,
+                             cudaStream_t s) {
+    return launch_pdl(router_dl_kernel, dim3(ceil_div(d.N, 256)), dim3(256), 0, s, d.N, d.k, m_tiles,
+                      d.N * d.k, dweight_part, slot_pos, topk_w, dl);
+}
+
+cudaError_t launch_dx_combine(const LayerDims &d, const void *dx_slots, const int32_t *slot_pos,
+                              const int32_t *topk_idx, const float *dl, const void *w_router,
+                              void *dx, cudaStream_t s) {
+    return launch_pdl(dx_combine_kernel, dim3(ceil_div(d.N, 8)), dim3(256), 0, s,
+                      (const __nv_bfloat16 *)dx_slots, slot_pos, topk_idx, dl,
+                      (const __nv_bfloat16 *)w_router, d.N, d.H, d.k, (__nv_bfloat16 *)dx);
+}
+
+cudaError_t launch_router_wgrad(const LayerDims &d, const int32_t *eoff_all, const int32_t *perm_all,
+                                const float *dl, const void *x, float *partial, float *partial_db,
+                                float *dw_router, float *db_router, cudaStream_t s) {
+    const int Z = router_wgrad_splits(d);
+    cudaError_t e = launch_pdl(router_wgrad_partial_kernel, dim3(d.E, ceil_div(d.H, 2048), Z),
+                               dim3(256), 0, s, eoff_all, perm_all, dl, (const __nv_bfloat16 *)x, d.H,
+                               d.E, d.k, partial, partial_db);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)std::min<int64_t>(ceil_div64((int64_t)d.E * d.H, 256), 148 * 4);
+    return launch_pdl(router_wgrad_reduce_kernel, dim3(grid), dim3(256), 0, s,
+                      (const float *)partial, (const float *)partial_db, Z, d.E, d.H, dw_router,
+                      db_router);
+}
+
+}  // namespace moe

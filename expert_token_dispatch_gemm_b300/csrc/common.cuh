@@ -109,6 +109,7 @@ struct LayerDims {
     int group_limit;   // partitions a token may use; 0 when unlimited
     const float *sel_bias;   // [E] selection-only bias or nullptr
     int slot_priority;       // 1: capacity ranks pairs slot-major (j*N + t)
+    int training;            // 1: the forward keeps what the backward needs
 };
 // Histogram segments of the dispatch scan: ceil(N/64) token segments, or in slot-major
 // priority k slots x ceil(N / 64k) token spans.
@@ -141,7 +142,8 @@ cudaError_t launch_pack_gate_up(const LayerDims &d, const void *w_gate, const vo
 // Tensor-core (bf16) grouped GEMMs. h has row stride Ipad.
 cudaError_t launch_tc_gate_up(const LayerDims &d, const void *send, const int32_t *expert_offsets,
                               int e_begin, int e_end, const void *packed, void *h,
-                              int32_t *status, int num_sms, cudaStream_t s);
+                              void *gu /* [N*k, 2 Ipad] or nullptr */, int32_t *status,
+                              int num_sms, cudaStream_t s);
 cudaError_t launch_tc_down(const LayerDims &d, const void *h, const int32_t *expert_offsets,
                            int e_begin, int e_end, const void *w_down, const int32_t *perm,
                            const float *topk_w, void *out_slots, int32_t *status, int num_sms,
@@ -158,6 +160,31 @@ cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_rou
 // in `partials`, then load_frac / prob_mean. TP row split: ordered sum of tp padded
 // outputs.
 constexpr int kStatsBlocks = 256;
+
+// Backward (bf16): tensor-core grouped GEMMs, then the router / combine kernels.
+cudaError_t launch_tc_dgrad_down(const LayerDims &d, const void *dout_send, const int32_t *eoff,
+                                 const void *w_down, const void *gu, const int32_t *perm,
+                                 const float *topk_w, void *dgu, void *wa, float *dweight_part,
+                                 int32_t *status, cudaStream_t s);
+cudaError_t launch_tc_dgrad_gate_up(const LayerDims &d, const void *dgu, const int32_t *eoff,
+                                    const void *packed, const int32_t *perm, void *dx_slots,
+                                    int32_t *status, cudaStream_t s);
+cudaError_t launch_tc_wgrad_gate_up(const LayerDims &d, const void *dgu, const void *send,
+                                    const int32_t *eoff, void *dw_gate, void *dw_up,
+                                    int32_t *status, cudaStream_t s);
+cudaError_t launch_tc_wgrad_down(const LayerDims &d, const void *dout_send, const void *wa,
+                                 const int32_t *eoff, void *dw_down, int32_t *status,
+                                 cudaStream_t s);
+int router_wgrad_splits(const LayerDims &d);
+cudaError_t launch_router_dl(const LayerDims &d, const float *dweight_part, int m_tiles,
+                             const int32_t *slot_pos, const float *topk_w, float *dl,
+                             cudaStream_t s);
+cudaError_t launch_dx_combine(const LayerDims &d, const void *dx_slots, const int32_t *slot_pos,
+                              const int32_t *topk_idx, const float *dl, const void *w_router,
+                              void *dx, cudaStream_t s);
+cudaError_t launch_router_wgrad(const LayerDims &d, const int32_t *eoff_all, const int32_t *perm_all,
+                                const float *dl, const void *x, float *partial, float *partial_db,
+                                float *dw_router, float *db_router, cudaStream_t s);
 cudaError_t launch_balance_stats(const LayerDims &d, const float *logits,
                                  const int32_t *routed_counts, float *partials, float *load_frac,
                                  float *prob_mean, cudaStream_t s);

@@ -1,0 +1,630 @@
+// Backward of the local experts as grouped GEMMs on the tensor cores. The chain rule
+// through y = W_d (silu(g) * u), g = W_g x, u = W_u x of every kept (token, expert) pair
+// (Ultralytics glossary "Expert Parallelism", step 3; an expert's weight gradient sums
+// over every row it received -- Hugging Face "Expert parallelism" docs, "How the sizes
+// combine"). Per send row r (pair of token t, weight w) with upstream gradient dout_t:
+//   dgrad_down : da_u[i, r] = sum_h W_d[h, i] dout_t[h]       (tokens on N, K = H)
+//                epilogue: a = silu(g) u, dweight_r += da_u . a (the routing weight's
+//                gradient), dg = w da_u u silu'(g), du = w da_u silu(g), wa = w a
+//   dgrad_gu   : dx_r[h] = sum_f W_gu[f, h] dgu_r[f]           (tokens on N, K = 2 Ipad)
+//   wgrad      : dW_gu[f, h] = sum_r dgu_r[f] x_r[h]           (K = the expert's rows)
+//                dW_d[h, i]  = sum_r dout_t[h] wa_r[i]
+// The weights stay in their forward layouts: the dgrad GEMMs read them as MN-major A
+// operands (M = the weight's column index), and the weight-gradient GEMMs read both
+// token-major activations as MN-major operands (K = token rows), so nothing is
+// transposed in memory.
+//
+// One CTA per SM (192 threads, persistent over its tiles), tcgen05.mma cta_group::1,
+// M = 128 TMEM lanes, N <= 256:
+//   warp 0      TMA producer, 4-stage ring (A: 128 x 64, B: up to 256 x 64; 128-byte
+//               swizzle). MN-major tiles are 64-element boxes: one 128-byte row per K.
+//   warp 1      TMEM (two 128 x 256 fp32 accumulators); lane 0 issues the MMAs. In the
+//               weight-gradient GEMMs the warp first zeroes the rows of the last K block
+//               that lie past the expert's segment, in both operands (they hold another
+//               expert's rows, or unwritten memory past the kept rows).
+//   warps 2..5  epilogue (tcgen05.ld, 32 columns at a time).
+// Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
+// MOE_DEV_TIMEOUT in the status word, stops issuing work, waits (bounded) for its own
+// copies and MMAs, frees TMEM and returns.
+#include "sm100.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128;                 // M rows per tile (TMEM lanes)
+constexpr int BN = 256;                 // max N per tile
+constexpr int STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
+constexpr uint32_t MN_BOX = 64 * BK * 2;    // one 64-element x 64-row MN-major box: 8 KB
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int CHUNK = 32;
+
+enum { BWD_DGRAD_DOWN = 0, BWD_DGRAD_GU = 1, BWD_WGRAD = 2 };
+
+// Shared-memory descriptor of an MN-major tile written by TMA in 64-element boxes with
+// 128-byte swizzle: one 128-byte row per K index, 8-row groups 1024 bytes apart (stride
+// byte offset), 64-element groups along M / N `lbo` bytes apart (leading byte offset).
+// Advancing K by 16 adds 16 rows = 2048 bytes to the start address.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Token maps with box heights 32, 64, 128 and 256 rows (K-major B of the dgrad GEMMs).
+struct BwdMaps {
+    CUtensorMap a;       // MN-major A: box 64 x 64
+    CUtensorMap b[4];    // dgrad: token rows (K-major); wgrad: b[0] MN-major box 64 x 64
+};
+__host__ __device__ constexpr int box_index(int rows) {
+    return rows <= 32 ? 0 : rows <= 64 ? 1 : rows <= 128 ? 2 : 3;
+}
+
+struct BwdParams {
+    const int32_t *expert_offsets;
+    int ne;                  // experts (all of the layer)
+    int num_kb;              // dgrad: K blocks of BK
+    int m_tiles, n_tiles;    // M tiles of BM; wgrad: N tiles of BN
+    int a_rows_per_expert;   // dgrad: rows between experts in A's map (K rows)
+    uint32_t lbo, sbo;       // MN-major descriptor strides
+    int I, Ipad, H;
+    // dgrad_down
+    const __nv_bfloat16 *gu;      // [rows, 2 Ipad] saved gate / up pre-activations
+    __nv_bfloat16 *dgu;           // [rows, 2 Ipad] out
+    __nv_bfloat16 *wa;            // [rows, Ipad] out: w * silu(g) * u
+    float *dweight_part;          // [m_tiles, rows] out
+    int rows;                     // send rows of the buffers (N * k)
+    // dgrad_down / dgrad_gu
+    const int32_t *perm;
+    const float *topk_w;
+    __nv_bfloat16 *dx_slots;      // dgrad_gu: [N*k, H] out (row = pair id)
+    // wgrad outputs: gate/up rows (packed order) or down rows
+    __nv_bfloat16 *out0, *out1;
+    int wgrad_gu;                 // 1: M = packed gate/up rows -> out0 = dW_gate, out1 = dW_up
+    int32_t *status;
+};
+
+struct Smem {
+    static constexpr uint32_t a_off = 0;
+    static constexpr uint32_t b_off = STAGES * A_BYTES;
+    static constexpr uint32_t epi_off = b_off + STAGES * B_BYTES;     // 16 KB staging
+    static constexpr uint32_t epi_bytes = CHUNK * BM * 4;
+    static constexpr uint32_t pairs_off = epi_off + epi_bytes;       // [BN] int + [BN] float
+    static constexpr uint32_t bar_off = pairs_off + 2 * BN * 4;
+    static constexpr uint32_t misc_off = bar_off + 24 * 8;
+    static constexpr uint32_t tables_off = misc_off + 16;
+    static constexpr uint32_t end = tables_off + 2 * (kMaxExperts + 1) * 4;
+    static constexpr uint32_t alloc = end + 1024;
+};
+static_assert(Smem::alloc <= 227 * 1024, "shared memory per CTA");
+
+// Tile of a dgrad GEMM: expert i, M tile f, token tile m; tokens fastest.
+struct DTile {
+    int i, f, m, tok0, ntok, nmma;
+};
+__device__ __forceinline__ DTile dtile_at(int t, const int *mtp, const int *eo, int ne, int m_tiles) {
+    DTile r;
+    decode_tile(t, mtp, ne, m_tiles, r.i, r.m, r.f);
+    const int seg = eo[r.i + 1] - eo[r.i];
+    r.tok0 = eo[r.i] + r.m * BN;
+    r.ntok = min(BN, seg - r.m * BN);
+    r.nmma = (r.ntok + 31) & ~31;
+    return r;
+}
+// Tile of a weight-gradient GEMM: expert e, M tile mt, N tile nt; K = the expert's rows.
+struct WTile {
+    int e, mt, nt, row0, nrows, nkb;
+};
+__device__ __forceinline__ WTile wtile_at(int t, const int *eo, int m_tiles, int n_tiles) {
+    WTile r;
+    const int per = m_tiles * n_tiles;
+    r.e = t / per;
+    const int l = t - r.e * per;
+    r.mt = l / n_tiles;          // N fastest: concurrent tiles share the A rows in L2
+    r.nt = l - r.mt * n_tiles;
+    r.row0 = eo[r.e];
+    r.nrows = eo[r.e + 1] - r.row0;
+    r.nkb = (r.nrows + BK - 1) / BK;
+    return r;
+}
+
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16 *p, float *f) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(p);
+    Vec16<__nv_bfloat16>::to_float(v, f);
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
+    constexpr bool WG = KIND == BWD_WGRAD;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::bar_off);
+    uint64_t *full = bars;                  // [STAGES]
+    uint64_t *empty = bars + STAGES;        // [STAGES]
+    uint64_t *tfull = bars + 2 * STAGES;    // [2]
+    uint64_t *tempty = tfull + 2;           // [2] (4 epilogue warps)
+    uint64_t *mma_done = tempty + 2;        // [1]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::misc_off);
+    volatile int *abort_s = reinterpret_cast<volatile int *>(smem + Smem::misc_off + 4);
+    int *eo = reinterpret_cast<int *>(smem + Smem::tables_off);
+    int *mtp = eo + (kMaxExperts + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (warp == 0) {
+        if (lane < 5) tma_prefetch_desc(lane == 0 ? &maps.a : &maps.b[lane - 1]);
+    } else if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else if (warp == 2 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4);
+        }
+        mbar_init(mma_done, 1);
+        *abort_s = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    grid_dep_wait();
+    grid_dep_trigger();
+    if (warp == 0) {
+        if (WG) {
+            for (int e = lane; e <= p.ne; e += 32) eo[e] = p.expert_offsets[e];
+        } else {
+            build_tile_tables(p.expert_offsets, 0, p.ne, BN, eo, mtp);
+        }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = WG ? p.ne * p.m_tiles * p.n_tiles : mtp[p.ne] * p.m_tiles;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, armed_parity = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                int nkb, a_x, a_y0, b_x, b_y0, bsel;
+                uint32_t tx;
+                if (WG) {
+                    const WTile tl = wtile_at(t, eo, p.m_tiles, p.n_tiles);
+                    nkb = tl.nkb;
+                    a_x = tl.mt * BM;
+                    b_x = tl.nt * BN;
+                    a_y0 = b_y0 = tl.row0;
+                    bsel = 0;
+                    tx = A_BYTES + B_BYTES;
+                } else {
+                    const DTile tl = dtile_at(t, mtp, eo, p.ne, p.m_tiles);
+                    nkb = p.num_kb;
+                    a_x = tl.f * BM;
+                    a_y0 = tl.i * p.a_rows_per_expert;
+                    b_y0 = tl.tok0;
+                    bsel = box_index(tl.nmma);
+                    b_x = 0;
+                    tx = A_BYTES + (uint32_t)(32 << bsel) * BK * 2;
+                }
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_s, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], tx);
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    const uint32_t a_dst = smem_u32(smem + Smem::a_off + stage * A_BYTES);
+                    const uint32_t b_dst = smem_u32(smem + Smem::b_off + stage * B_BYTES);
+                    tma_load_2d(a_dst, &maps.a, fb, a_x, a_y0 + kb * BK);
+                    tma_load_2d(a_dst + MN_BOX, &maps.a, fb, a_x + 64, a_y0 + kb * BK);
+                    if (WG) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            tma_load_2d(b_dst + q * MN_BOX, &maps.b[0], fb, b_x + 64 * q,
+                                        b_y0 + kb * BK);
+                    } else {
+                        tma_load_2d(b_dst, &maps.b[bsel], fb, kb * BK, b_y0);
+                    }
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < STAGES; ++s)
+                if ((armed >> s) & 1u) {
+                    volatile int no_abort = 0;
+                    mbar_wait(&full[s], (armed_parity >> s) & 1u, &no_abort, p.status);
+                }
+        }
+    } else if (warp == 1) {   // ------------------------------------- MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        const uint32_t idesc_mn = (1u << 15) | (WG ? (1u << 16) : 0u);
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            int nkb, nmma, tail;
+            if (WG) {
+                const WTile tl = wtile_at(t, eo, p.m_tiles, p.n_tiles);
+                nkb = tl.nkb;
+                nmma = BN;
+                tail = tl.nrows - (tl.nkb - 1) * BK;   // valid rows of the last K block
+            } else {
+                const DTile tl = dtile_at(t, mtp, eo, p.ne, p.m_tiles);
+                nkb = p.num_kb;
+                nmma = tl.nmma;
+                tail = BK;
+            }
+            const uint32_t idesc = make_idesc(BM, nmma) | idesc_mn;
+            if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_s, p.status))) break;
+            fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_s, p.status))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *a_tile = smem + Smem::a_off + stage * A_BYTES;
+                uint8_t *b_tile = smem + Smem::b_off + stage * B_BYTES;
+                if (WG && kb == nkb - 1 && tail < BK) {
+                    // rows tail..63 of every box of both operands read as zero
+                    const int zr = BK - tail;
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    for (int c = lane; c < 6 * zr * 8; c += 32) {
+                        const int box = c / (zr * 8), rem = c - box * zr * 8;
+                        const int row = tail + rem / 8, ch = rem % 8;
+                        uint8_t *base = box < 2 ? a_tile + box * MN_BOX : b_tile + (box - 2) * MN_BOX;
+                        *reinterpret_cast<uint4 *>(base + row * 128 + ch * 16) = z;
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    fence_after();
+                    const uint32_t a_addr = smem_u32(a_tile);
+                    const uint32_t b_addr = smem_u32(b_tile);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = smem_desc_mn_sw128(a_addr + kk * 2048, p.lbo, p.sbo);
+                        const uint64_t bd = WG ? smem_desc_mn_sw128(b_addr + kk * 2048, p.lbo, p.sbo)
+                                               : smem_desc_sw128(b_addr + kk * 32);
+                        mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                    }
+                    commit(&empty[stage]);
+                }
+                __syncwarp();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) commit(&tfull[acc]);   // after no K block: arrives at once
+            __syncwarp();
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (lane == 0) {
+            commit(mma_done);   // every MMA done before TMEM is freed
+            volatile int no_abort = 0;
+            mbar_wait(mma_done, 0, &no_abort, p.status);
+        }
+    } else {   // ------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int etid = threadIdx.x - 64;
+        float *stage_f = reinterpret_cast<float *>(smem + Smem::epi_off);
+        __nv_bfloat16 *stage_h = reinterpret_cast<__nv_bfloat16 *>(smem + Smem::epi_off);
+        int *pair_s = reinterpret_cast<int *>(smem + Smem::pairs_off);
+        float *wgt_s = reinterpret_cast<float *>(pair_s + BN);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            DTile dt = {};
+            WTile wt = {};
+            if (WG) {
+                wt = wtile_at(t, eo, p.m_tiles, p.n_tiles);
+            } else {
+                dt = dtile_at(t, mtp, eo, p.ne, p.m_tiles);
+                for (int j = etid; j < dt.nmma; j += 128) {
+                    const bool tv = j < dt.ntok;
+                    const int pr = tv ? p.perm[dt.tok0 + j] : -1;
+                    pair_s[j] = pr;
+                    wgt_s[j] = tv && p.topk_w != nullptr ? p.topk_w[pr] : 1.f;
+                }
+            }
+            const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_s, p.status);
+            if (!epilogue_all(ok)) break;
+            fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            if (WG) {
+                // row m of the tile -> output row; 32 columns per step, written directly
+                const int m = wt.mt * BM + q * 32 + lane;
+                __nv_bfloat16 *row = nullptr;
+                int ncols;
+                if (p.wgrad_gu) {
+                    const int blk = m / 128, r128 = m % 128;
+                    const int i = blk * 64 + (r128 & 63);
+                    if (i < p.I)
+                        row = (r128 < 64 ? p.out0 : p.out1) + ((size_t)wt.e * p.I + i) * p.H;
+                    ncols = p.H;
+                } else {
+                    if (m < p.H) row = p.out0 + ((size_t)wt.e * p.H + m) * p.I;
+                    ncols = p.I;
+                }
+                for (int c = 0; c < BN; c += CHUNK) {
+                    const int col0 = wt.nt * BN + c;
+                    if (col0 >= ncols) break;   // uniform over the CTA
+                    float v[32];
+                    if (wt.nkb > 0) {
+                        tmem_ld32(taddr + c, v);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0.f;   // an expert with no rows
+                    }
+                    if (row != nullptr)
+#pragma unroll
+                        for (int j8 = 0; j8 < 32; j8 += 8)
+                            if (col0 + j8 < ncols)
+                                *reinterpret_cast<uint4 *>(row + col0 + j8) = pack8_bf16(v + j8);
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+            } else {
+                for (int c = 0; c < dt.nmma; c += CHUNK) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+                    if (c + CHUNK >= dt.nmma) {
+                        fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[acc]);
+                    }
+                    if (KIND == BWD_DGRAD_DOWN) {
+                        // stage [32 tokens][128 features] fp32, then 8 features per item
+                        const int f = q * 32 + lane;
+#pragma unroll
+                        for (int j = 0; j < CHUNK; ++j) stage_f[j * BM + f] = v[j];
+                        epilogue_sync();
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const int item = etid + 128 * s;
+                            const int j = item >> 4, f8 = (item & 15) * 8;
+                            const int i = dt.f * BM + f8;             // intermediate feature
+                            const bool tv = c + j < dt.ntok;
+                            float part = 0.f;
+                            if (tv) {
+                                const size_t r = (size_t)dt.tok0 + c + j;
+                                const int gcol = (i / 64) * 128 + (i % 64);   // packed column
+                                uint4 dg_v = make_uint4(0u, 0u, 0u, 0u), du_v = dg_v, wa_v = dg_v;
+                                if (i < p.I) {
+                                    const float w = wgt_s[c + j];
+                                    float g[8], u[8], da[8], dg[8], du[8], wa[8];
+                                    load8_bf16(p.gu + r * 2 * p.Ipad + gcol, g);
+                                    load8_bf16(p.gu + r * 2 * p.Ipad + gcol + 64, u);
+                                    const float4 d0 = *reinterpret_cast<const float4 *>(stage_f + j * BM + f8);
+                                    const float4 d1 = *reinterpret_cast<const float4 *>(stage_f + j * BM + f8 + 4);
+                                    da[0] = d0.x; da[1] = d0.y; da[2] = d0.z; da[3] = d0.w;
+                                    da[4] = d1.x; da[5] = d1.y; da[6] = d1.z; da[7] = d1.w;
+#pragma unroll
+                                    for (int x = 0; x < 8; ++x) {
+                                        const float sg = 1.0f / (1.0f + __expf(-g[x]));
+                                        const float sl = g[x] * sg;
+                                        const float a = sl * u[x];
+                                        part += da[x] * a;
+                                        const float dw = w * da[x];
+                                        dg[x] = dw * u[x] * (sg * (1.0f + g[x] * (1.0f - sg)));
+                                        du[x] = dw * sl;
+                                        wa[x] = w * a;
+                                    }
+                                    dg_v = pack8_bf16(dg);
+                                    du_v = pack8_bf16(du);
+                                    wa_v = pack8_bf16(wa);
+                                }
+                                *reinterpret_cast<uint4 *>(p.dgu + r * 2 * p.Ipad + gcol) = dg_v;
+                                *reinterpret_cast<uint4 *>(p.dgu + r * 2 * p.Ipad + gcol + 64) = du_v;
+                                *reinterpret_cast<uint4 *>(p.wa + r * p.Ipad + i) = wa_v;
+                            }
+                            // the 16 items of token j are 16 consecutive lanes
+#pragma unroll
+                            for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                            if (tv && (item & 15) == 0)
+                                p.dweight_part[(size_t)dt.f * p.rows + dt.tok0 + c + j] = part;
+                        }
+                        epilogue_sync();
+                    } else {   // BWD_DGRAD_GU: dx of the pair, unweighted, into its slot
+                        const int f = q * 32 + lane;
+#pragma unroll
+                        for (int j = 0; j < CHUNK; ++j) stage_h[j * BM + f] = __float2bfloat16_rn(v[j]);
+                        epilogue_sync();
+                        const int col0 = dt.f * BM;
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const int item = etid + 128 * s;
+                            const int j = item >> 4, f8 = (item & 15) * 8;
+                            const int prj = c + j < dt.ntok ? pair_s[c + j] : -1;
+                            if (prj >= 0 && col0 + f8 < p.H)
+                                *reinterpret_cast<uint4 *>(p.dx_slots + (size_t)prj * p.H + col0 + f8) =
+                                    *reinterpret_cast<const uint4 *>(stage_h + j * BM + f8);
+                        }
+                        epilogue_sync();
+                    }
+                }
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+template <int KIND>
+cudaError_t launch_bwd(const BwdMaps &maps, BwdParams prm, int64_t max_tiles, cudaStream_t s) {
+    if (max_tiles <= 0) return cudaSuccess;
+    // MN-major descriptor strides: 64-element groups are one 8 KB box apart, 8-row K
+    // groups one 1024-byte swizzle atom apart
+    prm.lbo = MN_BOX;
+    prm.sbo = 1024;
+    auto kern = grouped_gemm_bwd_kernel<KIND>;
+    static int sms_dev[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (sms_dev[dev] == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::alloc);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        sms_dev[dev] = n > 0 ? n : 148;
+    }
+    const int grid = (int)std::min<int64_t>(max_tiles, sms_dev[dev]);
+    return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), Smem::alloc, s, maps, prm);
+}
+
+cudaError_t token_maps(BwdMaps *m, const void *t, uint64_t rows, uint64_t cols, uint64_t ld) {
+    cudaError_t e = cudaSuccess;
+    for (int b = 0; b < 4 && e == cudaSuccess; ++b) e = make_map(&m->b[b], t, rows, cols, ld, 32u << b);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_dgrad_down(const LayerDims &d, const void *dout_send, const int32_t *eoff,
+                                 const void *w_down, const void *gu, const int32_t *perm,
+                                 const float *topk_w, void *dgu, void *wa, float *dweight_part,
+                                 int32_t *status, cudaStream_t s) {
+    const int64_t rows = (int64_t)d.N * d.k;
+    BwdMaps maps;
+    // A = W_d [E*H rows (K = h), I columns (M = i)]
+    cudaError_t e = make_map(&maps.a, w_down, (uint64_t)d.E * d.H, d.I, d.I, 64);
+    if (e == cudaSuccess) e = token_maps(&maps, dout_send, rows, d.H, d.H);
+    if (e != cudaSuccess) return e;
+    BwdParams prm = {};
+    prm.expert_offsets = eoff;
+    prm.ne = d.E;
+    prm.num_kb = ceil_div(d.H, BK);
+    prm.m_tiles = d.Ipad / BM;
+    prm.a_rows_per_expert = d.H;
+    prm.I = d.I;
+    prm.Ipad = d.Ipad;
+    prm.H = d.H;
+    prm.gu = (const __nv_bfloat16 *)gu;
+    prm.dgu = (__nv_bfloat16 *)dgu;
+    prm.wa = (__nv_bfloat16 *)wa;
+    prm.dweight_part = dweight_part;
+    prm.rows = (int)rows;
+    prm.perm = perm;
+    prm.topk_w = topk_w;
+    prm.status = status;
+    return launch_bwd<BWD_DGRAD_DOWN>(maps, prm, (ceil_div64(rows, BN) + d.E) * prm.m_tiles, s);
+}
+
+cudaError_t launch_tc_dgrad_gate_up(const LayerDims &d, const void *dgu, const int32_t *eoff,
+                                    const void *packed, const int32_t *perm, void *dx_slots,
+                                    int32_t *status, cudaStream_t s) {
+    const int64_t rows = (int64_t)d.N * d.k;
+    BwdMaps maps;
+    // A = packed W_gu [E*2Ipad rows (K = f), H columns (M = h)]
+    cudaError_t e = make_map(&maps.a, packed, (uint64_t)d.E * 2 * d.Ipad, d.H, d.H, 64);
+    if (e == cudaSuccess) e = token_maps(&maps, dgu, rows, 2 * d.Ipad, 2 * d.Ipad);
+    if (e != cudaSuccess) return e;
+    BwdParams prm = {};
+    prm.expert_offsets = eoff;
+    prm.ne = d.E;
+    prm.num_kb = 2 * d.Ipad / BK;
+    prm.m_tiles = ceil_div(d.H, BM);
+    prm.a_rows_per_expert = 2 * d.Ipad;
+    prm.I = d.I;
+    prm.Ipad = d.Ipad;
+    prm.H = d.H;
+    prm.rows = (int)rows;
+    prm.perm = perm;
+    prm.topk_w = nullptr;
+    prm.dx_slots = (__nv_bfloat16 *)dx_slots;
+    prm.status = status;
+    return launch_bwd<BWD_DGRAD_GU>(maps, prm, (ceil_div64(rows, BN) + d.E) * prm.m_tiles, s);
+}
+
+cudaError_t launch_tc_wgrad_gate_up(const LayerDims &d, const void *dgu, const void *send,
+                                    const int32_t *eoff, void *dw_gate, void *dw_up,
+                                    int32_t *status, cudaStream_t s) {
+    const int64_t rows = (int64_t)d.N * d.k;
+    BwdMaps maps = {};
+    cudaError_t e = make_map(&maps.a, dgu, rows, 2 * d.Ipad, 2 * d.Ipad, 64);
+    if (e == cudaSuccess) e = make_map(&maps.b[0], send, rows, d.H, d.H, 64);
+    for (int b = 1; b < 4 && e == cudaSuccess; ++b) maps.b[b] = maps.b[0];
+    if (e != cudaSuccess) return e;
+    BwdParams prm = {};
+    prm.expert_offsets = eoff;
+    prm.ne = d.E;
+    prm.m_tiles = 2 * d.Ipad / BM;
+    prm.n_tiles = ceil_div(d.H, BN);
+    prm.I = d.I;
+    prm.Ipad = d.Ipad;
+    prm.H = d.H;
+    prm.rows = (int)rows;
+    prm.out0 = (__nv_bfloat16 *)dw_gate;
+    prm.out1 = (__nv_bfloat16 *)dw_up;
+    prm.wgrad_gu = 1;
+    prm.status = status;
+    return launch_bwd<BWD_WGRAD>(maps, prm, (int64_t)d.E * prm.m_tiles * prm.n_tiles, s);
+}
+
+cudaError_t launch_tc_wgrad_down(const LayerDims &d, const void *dout_send, const void *wa,
+                                 const int32_t *eoff, void *dw_down, int32_t *status,
+                                 cudaStream_t s) {
+    const int64_t rows = (int64_t)d.N * d.k;
+    BwdMaps maps = {};
+    cudaError_t e = make_map(&maps.a, dout_send, rows, d.H, d.H, 64);
+    if (e == cudaSuccess) e = make_map(&maps.b[0], wa, rows, d.Ipad, d.Ipad, 64);
+    for (int b = 1; b < 4 && e == cudaSuccess; ++b) maps.b[b] = maps.b[0];
+    if (e != cudaSuccess) return e;
+    BwdParams prm = {};
+    prm.expert_offsets = eoff;
+    prm.ne = d.E;
+    prm.m_tiles = ceil_div(d.H, BM);
+    prm.n_tiles = ceil_div(d.I, BN);
+    prm.I = d.I;
+    prm.Ipad = d.Ipad;
+    prm.H = d.H;
+    prm.rows = (int)rows;
+    prm.out0 = (__nv_bfloat16 *)dw_down;
+    prm.wgrad_gu = 0;
+    prm.status = status;
+    return launch_bwd<BWD_WGRAD>(maps, prm, (int64_t)d.E * prm.m_tiles * prm.n_tiles, s);
+}
+
+}  // namespace moe

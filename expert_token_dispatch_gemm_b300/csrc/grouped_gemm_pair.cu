@@ -72,6 +72,8 @@ struct PairParams {
                              // past I / H: its loads, and gate_up's stores)
     __nv_bfloat16 *h;        // EPI_SWIGLU output [pairs, h_ld]
     int h_ld;
+    __nv_bfloat16 *gu;       // EPI_SWIGLU, training: gate / up pre-activations
+                             // [pairs, 2 h_ld] in packed column order, or nullptr
     __nv_bfloat16 *out_slots;   // EPI_DOWN output [pairs, H]
     const int32_t *perm;
     const float *topk_w;
@@ -319,6 +321,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const PairParams
                             __nv_bfloat16 *out = p.h + (size_t)(tl.tok0 + c + j) * p.h_ld +
                                                  tl.f * (2 * GU_FEATS) + cta * GU_FEATS + f8;
                             *reinterpret_cast<uint4 *>(out) = pack8_bf16(hv);
+                            if (p.gu != nullptr) {
+                                const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                                const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                                __nv_bfloat16 *gd = p.gu + (size_t)(tl.tok0 + c + j) * 2 * p.h_ld +
+                                                    (2 * tl.f + cta) * CM + f8;
+                                *reinterpret_cast<uint4 *>(gd) = pack8_bf16(gv);
+                                *reinterpret_cast<uint4 *>(gd + GU_FEATS) = pack8_bf16(uv);
+                            }
                         }
                     }
                     epilogue_sync();
@@ -423,7 +433,7 @@ cudaError_t launch_pair(const PairMaps &maps, const PairParams &prm, int64_t max
 }  // namespace
 
 cudaError_t launch_tc_gate_up(const LayerDims &d, const void *send, const int32_t *expert_offsets,
-                              int e_begin, int e_end, const void *packed, void *h,
+                              int e_begin, int e_end, const void *packed, void *h, void *gu,
                               int32_t *status, int /*num_sms*/, cudaStream_t s) {
     const int64_t rows = (int64_t)d.N * d.k;
     PairMaps maps;
@@ -440,6 +450,7 @@ cudaError_t launch_tc_gate_up(const LayerDims &d, const void *send, const int32_
     prm.live_halves = ceil_div(d.I, GU_FEATS);
     prm.h = (__nv_bfloat16 *)h;
     prm.h_ld = d.Ipad;
+    prm.gu = (__nv_bfloat16 *)gu;
     prm.H = d.H;
     prm.status = status;
     const int64_t max_tiles = (ceil_div64(rows, PN) + prm.ne) * prm.f_tiles;

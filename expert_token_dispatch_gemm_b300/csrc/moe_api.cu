@@ -95,6 +95,10 @@ moe_status_t check_config(const moe_config *cfg, LayerDims *d) {
     if (cfg->capacity_priority != MOE_PRIORITY_TOKEN && cfg->capacity_priority != MOE_PRIORITY_SLOT)
         return fail(MOE_ERR_INVALID_ARG, "unknown capacity_priority %d", cfg->capacity_priority);
     d->slot_priority = cfg->capacity_priority == MOE_PRIORITY_SLOT;
+    if (cfg->training != 0 && cfg->training != 1) return fail(MOE_ERR_INVALID_ARG, "training must be 0 or 1");
+    if (cfg->training && cfg->dtype != MOE_DTYPE_BF16)
+        return fail(MOE_ERR_UNSUPPORTED, "the backward is implemented for bf16 layers");
+    d->training = cfg->training;
     if (cfg->capacity_factor > 0.f) {
         // cf * N * k is exact in double (24-bit cf times an integer below 2^29); if the
         // exact quotient by E is an integer the division returns it exactly, otherwise it
@@ -125,7 +129,16 @@ struct Workspace {
     int32_t *slot_pos;     // [N*k]
     void *send;            // [N*k, H]
     void *h;               // [N*k, Ipad]
-    void *slots;           // [N*k, H]
+    void *slots;           // [N*k, H]; the backward's dx slots
+    // training only: state kept by the forward, buffers of the backward
+    void *gu;              // [N*k, 2 Ipad] gate / up pre-activations
+    void *dout_send;       // [N*k, H]
+    void *dgu;             // [N*k, 2 Ipad]
+    float *dweight_part;   // [Ipad / 128, N*k]
+    float *dl;             // [N*k]
+    int32_t *routed_all, *counts_all, *eoff_all, *poff_all, *slot_all, *perm_all;
+    float *rw_partial;     // [Z, E, H]
+    float *rw_partial_db;  // [Z, E]
     size_t bytes;
 };
 
@@ -154,6 +167,22 @@ Workspace carve(const LayerDims &d, int mode, void *base) {
     w.send = take(pairs * d.H * esize(d));
     w.h = take(pairs * d.Ipad * esize(d));
     w.slots = take(pairs * d.H * esize(d));
+    if (d.training) {
+        const size_t Z = (size_t)router_wgrad_splits(d);
+        w.gu = take(pairs * 2 * d.Ipad * esize(d));
+        w.dout_send = take(pairs * d.H * esize(d));
+        w.dgu = take(pairs * 2 * d.Ipad * esize(d));
+        w.dweight_part = (float *)take((size_t)(d.Ipad / 128) * pairs * sizeof(float));
+        w.dl = (float *)take(pairs * sizeof(float));
+        w.routed_all = (int32_t *)take(d.E * sizeof(int32_t));
+        w.counts_all = (int32_t *)take(d.E * sizeof(int32_t));
+        w.eoff_all = (int32_t *)take((d.E + 1) * sizeof(int32_t));
+        w.poff_all = (int32_t *)take((d.P + 1) * sizeof(int32_t));
+        w.slot_all = (int32_t *)take(pairs * sizeof(int32_t));
+        w.perm_all = (int32_t *)take(pairs * sizeof(int32_t));
+        w.rw_partial = (float *)take(Z * d.E * d.H * sizeof(float));
+        w.rw_partial_db = (float *)take(Z * d.E * sizeof(float));
+    }
     w.bytes = off;
     return w;
 }
@@ -216,9 +245,9 @@ moe_status_t run_dispatch_from_hist(const LayerDims &d, const int32_t *idx, cons
 }
 
 moe_status_t run_gate_up(const LayerDims &d, const void *send, const int32_t *eoff, int e0, int e1,
-                         const void *packed, const Workspace &w, cudaStream_t s) {
+                         const void *packed, const Workspace &w, cudaStream_t s, void *gu = nullptr) {
     if (d.dtype == MOE_DTYPE_BF16)
-        MOE_CUDA(launch_tc_gate_up(d, send, eoff, e0, e1, packed, w.h, w.status, num_sms(), s),
+        MOE_CUDA(launch_tc_gate_up(d, send, eoff, e0, e1, packed, w.h, gu, w.status, num_sms(), s),
                  "tensor-core gate/up kernel");
     else
         MOE_CUDA(launch_simt_gate_up(d, (const float *)send, eoff, e0, e1, (const float *)packed,
@@ -462,20 +491,23 @@ moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void 
     cudaStream_t s = (cudaStream_t)stream;
     moe_diagnostics none = {};
     const moe_diagnostics &g = diag ? *diag : none;
-    int32_t *idx = g.topk_idx ? g.topk_idx : w.topk_idx;
-    float *tw = g.topk_w ? g.topk_w : w.topk_w;
-    int32_t *routed = g.routed_counts ? g.routed_counts : w.routed;
-    int32_t *counts = g.counts ? g.counts : w.counts;
-    int32_t *eoff = g.expert_offsets ? g.expert_offsets : w.eoff;
-    int32_t *poff = g.part_offsets ? g.part_offsets : w.poff;
-    int32_t *perm = g.perm ? g.perm : w.perm;
-    int32_t *slot_pos = g.slot_pos ? g.slot_pos : w.slot_pos;
+    // training: the routing state stays in the workspace for the backward and is copied
+    // to the requested diagnostic buffers at the end
+    const bool own = !d.training;
+    int32_t *idx = own && g.topk_idx ? g.topk_idx : w.topk_idx;
+    float *tw = own && g.topk_w ? g.topk_w : w.topk_w;
+    int32_t *routed = own && g.routed_counts ? g.routed_counts : w.routed;
+    int32_t *counts = own && g.counts ? g.counts : w.counts;
+    int32_t *eoff = own && g.expert_offsets ? g.expert_offsets : w.eoff;
+    int32_t *poff = own && g.part_offsets ? g.part_offsets : w.poff;
+    int32_t *perm = own && g.perm ? g.perm : w.perm;
+    int32_t *slot_pos = own && g.slot_pos ? g.slot_pos : w.slot_pos;
     if (d.N == 0) {
         g_last_error.clear();
-        if (g.routed_counts) MOE_CUDA(cudaMemsetAsync(routed, 0, d.E * 4, s), "memset");
-        if (g.counts) MOE_CUDA(cudaMemsetAsync(counts, 0, d.E * 4, s), "memset");
-        if (g.expert_offsets) MOE_CUDA(cudaMemsetAsync(eoff, 0, (d.E + 1) * 4, s), "memset");
-        if (g.part_offsets) MOE_CUDA(cudaMemsetAsync(poff, 0, (d.P + 1) * 4, s), "memset");
+        if (g.routed_counts) MOE_CUDA(cudaMemsetAsync(g.routed_counts, 0, d.E * 4, s), "memset");
+        if (g.counts) MOE_CUDA(cudaMemsetAsync(g.counts, 0, d.E * 4, s), "memset");
+        if (g.expert_offsets) MOE_CUDA(cudaMemsetAsync(g.expert_offsets, 0, (d.E + 1) * 4, s), "memset");
+        if (g.part_offsets) MOE_CUDA(cudaMemsetAsync(g.part_offsets, 0, (d.P + 1) * 4, s), "memset");
         return MOE_OK;
     }
     NEED(x, true);
@@ -517,7 +549,7 @@ moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void 
     // Both forward rules run every partition's experts in one launch per GEMM: an
     // expert's rows never share a tile with another expert's, so its outputs are the
     // same as if its partition ran it alone.
-    st = run_gate_up(d, w.send, eoff, 0, d.E, w_gate_up_packed, w, s);
+    st = run_gate_up(d, w.send, eoff, 0, d.E, w_gate_up_packed, w, s, d.training ? w.gu : nullptr);
     if (st != MOE_OK) return st;
     MOE_MARK(MOE_STAGE_DOWN);
     st = run_down(d, eoff, 0, d.E, w_down, perm, tw, w.slots, w, s);
@@ -527,6 +559,21 @@ moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void 
     if (st != MOE_OK) return st;
     MOE_MARK(MOE_NUM_STAGES);
 #undef MOE_MARK
+    if (d.training) {
+        const size_t pairs = (size_t)d.N * d.k;
+        auto copy = [&](void *dst, const void *src, size_t bytes) -> moe_status_t {
+            if (dst != nullptr)
+                MOE_CUDA(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s), "diagnostic copy");
+            return MOE_OK;
+        };
+        const moe_status_t c[8] = {
+            copy(g.topk_idx, idx, pairs * 4), copy(g.topk_w, tw, pairs * 4),
+            copy(g.routed_counts, routed, d.E * 4), copy(g.counts, counts, d.E * 4),
+            copy(g.expert_offsets, eoff, (d.E + 1) * 4), copy(g.part_offsets, poff, (d.P + 1) * 4),
+            copy(g.perm, perm, pairs * 4), copy(g.slot_pos, slot_pos, pairs * 4)};
+        for (moe_status_t x : c)
+            if (x != MOE_OK) return x;
+    }
     return MOE_OK;
 }
 
@@ -599,6 +646,75 @@ moe_status_t moe_dispatch_noalloc(const moe_config *cfg, const int32_t *topk_idx
     MOE_CUDA(launch_histogram(d, topk_idx, w.seg_hist, w.status, s), "histogram kernel");
     return run_dispatch_from_hist(d, topk_idx, x, w, routed_counts, counts, expert_offsets,
                                   part_offsets, perm, slot_pos, send, s);
+}
+
+moe_status_t moe_layer_backward(const moe_config *cfg, const void *x, const void *w_router,
+                                const void *w_gate_up_packed, const void *w_down,
+                                const void *dout, void *dx, float *dw_router, float *db_router,
+                                void *dw_gate, void *dw_up, void *dw_down, void *workspace,
+                                size_t workspace_bytes, void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    if (!d.training)
+        return fail(MOE_ERR_INVALID_ARG, "moe_layer_backward needs a config with training = 1");
+    Workspace w;
+    st = check_workspace(d, cfg->mode, workspace, workspace_bytes, &w);
+    if (st != MOE_OK) return st;
+    NEED(dw_router, true);
+    NEED(dw_gate, true);
+    NEED(dw_up, true);
+    NEED(dw_down, true);
+    cudaStream_t s = (cudaStream_t)stream;
+    g_last_error.clear();
+    if (d.N == 0) {   // no tokens: every gradient is zero
+        const size_t es = esize(d);
+        MOE_CUDA(cudaMemsetAsync(dw_router, 0, (size_t)d.E * d.H * 4, s), "memset");
+        if (db_router) MOE_CUDA(cudaMemsetAsync(db_router, 0, (size_t)d.E * 4, s), "memset");
+        MOE_CUDA(cudaMemsetAsync(dw_gate, 0, (size_t)d.E * d.I * d.H * es, s), "memset");
+        MOE_CUDA(cudaMemsetAsync(dw_up, 0, (size_t)d.E * d.I * d.H * es, s), "memset");
+        MOE_CUDA(cudaMemsetAsync(dw_down, 0, (size_t)d.E * d.H * d.I * es, s), "memset");
+        return MOE_OK;
+    }
+    NEED(x, true);
+    NEED(w_router, true);
+    NEED(w_gate_up_packed, true);
+    NEED(w_down, true);
+    NEED(dout, true);
+    NEED(dx, true);
+    // 1. the upstream gradient of every kept pair, in the send layout
+    MOE_CUDA(launch_permute(d, dout, w.slot_pos, w.dout_send, s), "permute kernel");
+    // 2. dgrad of the down projection with the SwiGLU backward: dgu, w*a, dweight parts
+    MOE_CUDA(launch_tc_dgrad_down(d, w.dout_send, w.eoff, w_down, w.gu, w.perm, w.topk_w, w.dgu,
+                                  w.h, w.dweight_part, w.status, s),
+             "tensor-core dgrad-down kernel");
+    // 3. dgrad of gate / up: every kept pair's dx into its slot
+    MOE_CUDA(launch_tc_dgrad_gate_up(d, w.dgu, w.eoff, w_gate_up_packed, w.perm, w.slots, w.status,
+                                     s),
+             "tensor-core dgrad-gate/up kernel");
+    // 4. weight gradients of the experts
+    MOE_CUDA(launch_tc_wgrad_gate_up(d, w.dgu, w.send, w.eoff, dw_gate, dw_up, w.status, s),
+             "tensor-core wgrad-gate/up kernel");
+    MOE_CUDA(launch_tc_wgrad_down(d, w.dout_send, w.h, w.eoff, dw_down, w.status, s),
+             "tensor-core wgrad-down kernel");
+    // 5. routing-weight and logit gradients, dx
+    MOE_CUDA(launch_router_dl(d, w.dweight_part, d.Ipad / 128, w.slot_pos, w.topk_w, w.dl, s),
+             "router logit-gradient kernel");
+    MOE_CUDA(launch_dx_combine(d, w.slots, w.slot_pos, w.topk_idx, w.dl, w_router, dx, s),
+             "dx combine kernel");
+    // 6. router weight gradient over every routed pair (dropped ones too), grouped by
+    //    expert in token order: the dispatch scan without a capacity
+    LayerDims all = d;
+    all.capacity = INT_MAX;
+    all.slot_priority = 0;
+    MOE_CUDA(launch_histogram(all, w.topk_idx, w.seg_hist, w.status, s), "histogram kernel");
+    MOE_CUDA(launch_scan_assign(all, w.topk_idx, w.seg_hist, w.routed_all, w.counts_all, w.eoff_all,
+                                w.poff_all, w.slot_all, w.perm_all, w.status, s),
+             "scan/assign kernel");
+    MOE_CUDA(launch_router_wgrad(d, w.eoff_all, w.perm_all, w.dl, x, w.rw_partial, w.rw_partial_db,
+                                 dw_router, db_router, s),
+             "router wgrad kernels");
+    return MOE_OK;
 }
 
 moe_status_t moe_balance_stats(const moe_config *cfg, const float *router_logits,

@@ -108,6 +108,13 @@ enum {
  *                   token -- so pair (t, j) has priority j*N + t. The rank decides which
  *                   pairs the capacity keeps and orders the rows of the expert's segment
  *                   in the send layout.
+ *
+ * Training:
+ *  training         0: inference. 1: moe_layer_forward also keeps, in the workspace, what
+ *                   moe_layer_backward needs (the routing, the send layout and the gate /
+ *                   up pre-activations; the workspace grows accordingly), and copies the
+ *                   routing arrays it keeps to any moe_diagnostics buffers given.
+ *                   bf16 layers only (MOE_ERR_UNSUPPORTED for fp32).
  */
 typedef struct moe_config {
     int64_t num_tokens;
@@ -123,6 +130,7 @@ typedef struct moe_config {
     int32_t group_limit;
     const float *selection_bias;
     int32_t capacity_priority;
+    int32_t training;
 } moe_config;
 
 /* Stage boundaries recorded by moe_layer_forward when moe_diagnostics.stage_events is
@@ -327,6 +335,29 @@ moe_status_t moe_layer_forward(const moe_config *cfg, const void *x, const void 
 moe_status_t moe_read_device_status(const moe_config *cfg, void *workspace,
                                     size_t workspace_bytes, int32_t *flags, int32_t reset,
                                     void *stream);
+
+/*
+ * Backward of the whole layer (the chain rule through moe_layer_forward; an expert's
+ * weight gradient sums over every row it received -- Hugging Face page, "How the sizes
+ * combine"). Call it after moe_layer_forward with the same cfg (training = 1), inputs
+ * and workspace, on the same stream; the forward's state in the workspace must not be
+ * overwritten in between.
+ *   dout       [N, H] dtype     gradient of the layer output
+ *   dx         [N, H] dtype out (expert paths plus the router's)
+ *   dw_router  [E, H] fp32 out
+ *   db_router  [E] fp32 out, or NULL
+ *   dw_gate, dw_up [E, I, H] dtype out; dw_down [E, H, I] dtype out (nn.Linear layouts)
+ * The expert selection and the capacity drops are piecewise constant and carry no
+ * gradient; a dropped pair contributes no expert gradient but its routing weight still
+ * gets a logit gradient through the softmax. All products accumulate in fp32; the
+ * experts' weight gradients are one fp32 sum per expert over its rows, rounded once.
+ * Deterministic: no atomics on values.
+ */
+moe_status_t moe_layer_backward(const moe_config *cfg, const void *x, const void *w_router,
+                                const void *w_gate_up_packed, const void *w_down,
+                                const void *dout, void *dx, float *dw_router, float *db_router,
+                                void *dw_gate, void *dw_up, void *dw_down, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /*
  * Router load statistics (Ultralytics page, "Load balancing and capacity": an auxiliary

@@ -217,3 +217,24 @@ def test_balance_stats_and_tp_reduce_validate_before_any_access(moe):
     assert st == 1
     st = moe.lib.moe_tp_reduce(ctypes.byref(c), 2, ctypes.c_void_p((1 << 20) + 4), FAKE, None)
     assert st == 1 and b"aligned" in moe.lib.moe_last_error()
+
+
+def test_training_needs_bf16_and_grows_the_workspace(moe):
+    c = cfg(moe)
+    _, base = status_of(moe, c)
+    c.training = 1
+    st, grown = status_of(moe, c)
+    assert st == 0 and grown > base
+    c = cfg(moe, dtype="fp32")
+    c.training = 1
+    assert status_of(moe, c)[0] == 2
+    c = cfg(moe)
+    c.training = 3
+    assert status_of(moe, c)[0] == 1
+
+
+def test_backward_needs_a_training_config(moe):
+    c = cfg(moe)
+    st = moe.lib.moe_layer_backward(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                    FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert st == 1 and b"training" in moe.lib.moe_last_error()

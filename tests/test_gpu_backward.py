@@ -1,0 +1,137 @@
+"""Backward of the layer on the GPU (moe_layer_backward, bf16), through the C ABI,
+against the fp64 oracle's chain rule (oracle.layer_backward) on the same seeded inputs.
+
+Bar: every gradient within 2e-2 * max|ref| (the bf16 rule of the forward: the
+operands and the intermediate gradients are bf16, every product accumulates in fp32).
+Routing is exact on the dyadic input variant, so both sides differentiate the same
+selection. The shapes span several M / N / K tiles with ragged tails (H and I not
+multiples of 64 or 128), capacity drops, slot-major priority, mask-and-sum mode, a
+single token, experts that receive no rows, and a 256-row expert segment boundary.
+"""
+import numpy as np
+import pytest
+import torch
+
+import expert_token_dispatch_gemm_b300 as moe
+import oracle
+import workloads
+from moe_gpu_harness import BF16_TOL, assert_close, f64, make_cfg
+
+pytestmark = pytest.mark.gpu
+
+S = workloads.LayerShape
+SHAPES = [
+    S("b_e8_k2", N=600, H=256, I=192, E=8, top_k=2, ep_size=4, bias=True),
+    S("b_ragged", N=777, H=200, I=136, E=16, top_k=4, ep_size=4),
+    S("b_cap", N=900, H=128, I=256, E=8, top_k=2, ep_size=2, capacity_factor=0.6),
+    S("b_skew_cap", N=1024, H=256, I=128, E=32, top_k=8, ep_size=8, capacity_factor=1.25,
+      zipf_s=1.1),
+    S("b_sparse", N=20, H=128, I=64, E=32, top_k=2, ep_size=8),     # most experts get no rows
+    S("b_one", N=1, H=64, I=64, E=4, top_k=2, ep_size=2),
+    S("b_long_seg", N=1200, H=192, I=320, E=4, top_k=1, ep_size=2),  # segments > 256 rows
+]
+
+
+def _run(shape, inp, dout, mode="dispatch", capacity_priority="token"):
+    dev = "cuda"
+    cfg = make_cfg(shape, mode, capacity_priority=capacity_priority)
+    cfg.training = 1
+    x = inp["x"].to(dev).contiguous()
+    wr = inp["w_router"].to(dev).contiguous()
+    b = inp["b_router"]
+    br = None if b is None else b.to(dev, torch.float32).contiguous()
+    wg, wu, wd = (inp[n].to(dev).contiguous() for n in ("w_gate", "w_up", "w_down"))
+    packed = moe.moe_pack_weights(cfg, wg, wu)
+    ws = moe.alloc_workspace(cfg)
+    out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device=dev)
+    moe.moe_layer_forward(cfg, x, wr, br, packed, wd, out, ws)
+    g = dict(dx=torch.full_like(x, float("nan")),
+             dw_router=torch.full((shape.E, shape.H), float("nan"), device=dev),
+             db_router=torch.full((shape.E,), float("nan"), device=dev),
+             dw_gate=torch.full_like(wg, float("nan")), dw_up=torch.full_like(wu, float("nan")),
+             dw_down=torch.full_like(wd, float("nan")))
+    moe.moe_layer_backward(cfg, x, wr, packed, wd, dout.to(dev).contiguous(), g["dx"],
+                           g["dw_router"], g["db_router"], g["dw_gate"], g["dw_up"], g["dw_down"],
+                           ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(cfg, ws) == 0
+    return out, g
+
+
+def _dout(shape, seed):
+    gen = torch.Generator().manual_seed(seed)
+    return torch.randn((shape.N, shape.H), generator=gen).to(torch.bfloat16)
+
+
+def _oracle(shape, inp, dout, capacity_priority="token"):
+    b = inp["b_router"]
+    return oracle.layer_backward(f64(inp["x"]), f64(inp["w_router"]), None if b is None else f64(b),
+                                 f64(inp["w_gate"]), f64(inp["w_up"]), f64(inp["w_down"]),
+                                 shape.top_k, shape.ep_size, f64(dout), shape.capacity_factor,
+                                 capacity_priority=capacity_priority)
+
+
+def _compare(g, ref):
+    for key in ("dx", "dw_router", "db_router", "dw_gate", "dw_up", "dw_down"):
+        assert_close(g[key], ref[key], BF16_TOL, key)
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
+def test_layer_backward_matches_oracle(shape):
+    inp = workloads.layer_inputs(shape, seed=51, variant="exact")
+    dout = _dout(shape, 52)
+    _, g = _run(shape, inp, dout)
+    _compare(g, _oracle(shape, inp, dout))
+
+
+def test_backward_with_slot_priority_and_mask_mode():
+    shape = SHAPES[3]
+    inp = workloads.layer_inputs(shape, seed=53, variant="exact")
+    dout = _dout(shape, 54)
+    _, g = _run(shape, inp, dout, mode="mask_sum", capacity_priority="slot")
+    _compare(g, _oracle(shape, inp, dout, capacity_priority="slot"))
+
+
+def test_backward_is_deterministic():
+    shape = SHAPES[1]
+    inp = workloads.layer_inputs(shape, seed=55, variant="exact")
+    dout = _dout(shape, 56)
+    _, a = _run(shape, inp, dout)
+    _, b = _run(shape, inp, dout)
+    for key in a:
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_experts_without_rows_get_zero_weight_gradients():
+    shape = SHAPES[4]
+    inp = workloads.layer_inputs(shape, seed=57, variant="exact")
+    _, g = _run(shape, inp, _dout(shape, 58))
+    ref = _oracle(shape, inp, _dout(shape, 58))
+    empty = [e for e in range(shape.E) if not np.any(ref["dw_down"][e])]
+    assert empty, "the shape should leave experts without rows"
+    for e in empty:
+        assert not g["dw_gate"][e].any() and not g["dw_up"][e].any() and not g["dw_down"][e].any()
+
+
+def test_training_forward_output_and_diagnostics_are_unchanged():
+    shape = SHAPES[0]
+    inp = workloads.layer_inputs(shape, seed=59, variant="exact")
+    dev = "cuda"
+    outs = []
+    for training in (0, 1):
+        cfg = make_cfg(shape)
+        cfg.training = training
+        x = inp["x"].to(dev)
+        wg, wu, wd = (inp[n].to(dev).contiguous() for n in ("w_gate", "w_up", "w_down"))
+        packed = moe.moe_pack_weights(cfg, wg, wu)
+        ws = moe.alloc_workspace(cfg)
+        out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device=dev)
+        diag = dict(topk_idx=torch.empty((shape.N, shape.top_k), dtype=torch.int32, device=dev),
+                    slot_pos=torch.empty(shape.N * shape.top_k, dtype=torch.int32, device=dev))
+        moe.moe_layer_forward(cfg, x, inp["w_router"].to(dev), inp["b_router"].to(dev), packed, wd,
+                              out, ws, diag)
+        torch.cuda.synchronize()
+        outs.append((out, diag))
+    assert torch.equal(outs[0][0], outs[1][0])
+    for key in ("topk_idx", "slot_pos"):
+        assert torch.equal(outs[0][1][key], outs[1][1][key])
