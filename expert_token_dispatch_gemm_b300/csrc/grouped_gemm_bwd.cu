@@ -35,7 +35,6 @@ using namespace tc;
 
 constexpr int BM = 128;                 // M rows per tile (TMEM lanes)
 constexpr int BN = 256;                 // max N per tile
-constexpr int STAGES = 4;
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
 constexpr uint32_t MN_BOX = 64 * BK * 2;    // one 64-element x 64-row MN-major box: 8 KB
@@ -59,10 +58,29 @@ __device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t addr, uint32_t l
     return d;
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Token maps with box heights 32, 64, 128 and 256 rows (K-major B of the dgrad GEMMs).
 struct BwdMaps {
     CUtensorMap a;       // MN-major A: box 64 x 64
     CUtensorMap b[4];    // dgrad: token rows (K-major); wgrad: b[0] MN-major box 64 x 64
+    CUtensorMap out[2];  // wgrad: [E][rows][cols] outputs, box 64 x 32 (TMA stores)
 };
 __host__ __device__ constexpr int box_index(int rows) {
     return rows <= 32 ? 0 : rows <= 64 ? 1 : rows <= 128 ? 2 : 3;
@@ -86,25 +104,31 @@ struct BwdParams {
     const int32_t *perm;
     const float *topk_w;
     __nv_bfloat16 *dx_slots;      // dgrad_gu: [N*k, H] out (row = pair id)
-    // wgrad outputs: gate/up rows (packed order) or down rows
-    __nv_bfloat16 *out0, *out1;
-    int wgrad_gu;                 // 1: M = packed gate/up rows -> out0 = dW_gate, out1 = dW_up
+    int wgrad_gu;                 // wgrad: 1 = M is packed gate/up rows (outputs dW_gate,
+                                  // dW_up), 0 = M is down rows (output dW_down)
     int32_t *status;
 };
 
+// 4-stage ring. The dgrad GEMMs add a 16 KB staging block, the token tile's pair ids and
+// weights and two tile tables; the weight-gradient GEMMs 32 KB of TMA-store staging (4
+// warps x 2 buffers x 4 KB) and the expert offsets only.
+template <int KIND>
 struct Smem {
+    static constexpr bool WG = KIND == BWD_WGRAD;
+    static constexpr int STAGES = 4;
     static constexpr uint32_t a_off = 0;
     static constexpr uint32_t b_off = STAGES * A_BYTES;
-    static constexpr uint32_t epi_off = b_off + STAGES * B_BYTES;     // 16 KB staging
-    static constexpr uint32_t epi_bytes = CHUNK * BM * 4;
+    static constexpr uint32_t epi_off = b_off + STAGES * B_BYTES;
+    static constexpr uint32_t epi_bytes = WG ? 4 * 2 * 4096 : CHUNK * BM * 4;
     static constexpr uint32_t pairs_off = epi_off + epi_bytes;       // [BN] int + [BN] float
-    static constexpr uint32_t bar_off = pairs_off + 2 * BN * 4;
+    static constexpr uint32_t bar_off = pairs_off + (WG ? 0 : 2 * BN * 4);
     static constexpr uint32_t misc_off = bar_off + 24 * 8;
     static constexpr uint32_t tables_off = misc_off + 16;
-    static constexpr uint32_t end = tables_off + 2 * (kMaxExperts + 1) * 4;
+    static constexpr uint32_t end = tables_off + (WG ? 1 : 2) * (kMaxExperts + 1) * 4;
     static constexpr uint32_t alloc = end + 1024;
 };
-static_assert(Smem::alloc <= 227 * 1024, "shared memory per CTA");
+static_assert(Smem<BWD_WGRAD>::alloc <= 227 * 1024 && Smem<BWD_DGRAD_DOWN>::alloc <= 227 * 1024,
+              "shared memory per CTA");
 
 // Tile of a dgrad GEMM: expert i, M tile f, token tile m; tokens fastest.
 struct DTile {
@@ -136,6 +160,33 @@ __device__ __forceinline__ WTile wtile_at(int t, const int *eo, int m_tiles, int
     return r;
 }
 
+// 64 consecutive fp32 accumulator columns of this thread's TMEM lane (one load, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float *v) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
+          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
+          "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void load8_bf16(const __nv_bfloat16 *p, float *f) {
     const uint4 v = *reinterpret_cast<const uint4 *>(p);
     Vec16<__nv_bfloat16>::to_float(v, f);
@@ -145,18 +196,20 @@ template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     constexpr bool WG = KIND == BWD_WGRAD;
+    using L = Smem<KIND>;
+    constexpr int STAGES = L::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::bar_off);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
     uint64_t *full = bars;                  // [STAGES]
     uint64_t *empty = bars + STAGES;        // [STAGES]
     uint64_t *tfull = bars + 2 * STAGES;    // [2]
     uint64_t *tempty = tfull + 2;           // [2] (4 epilogue warps)
     uint64_t *mma_done = tempty + 2;        // [1]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::misc_off);
-    volatile int *abort_s = reinterpret_cast<volatile int *>(smem + Smem::misc_off + 4);
-    int *eo = reinterpret_cast<int *>(smem + Smem::tables_off);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
+    volatile int *abort_s = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
+    int *eo = reinterpret_cast<int *>(smem + L::tables_off);
     int *mtp = eo + (kMaxExperts + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -229,8 +282,8 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     }
                     mbar_arrive_expect_tx(&full[stage], tx);
                     const uint32_t fb = smem_u32(&full[stage]);
-                    const uint32_t a_dst = smem_u32(smem + Smem::a_off + stage * A_BYTES);
-                    const uint32_t b_dst = smem_u32(smem + Smem::b_off + stage * B_BYTES);
+                    const uint32_t a_dst = smem_u32(smem + L::a_off + stage * A_BYTES);
+                    const uint32_t b_dst = smem_u32(smem + L::b_off + stage * B_BYTES);
                     tma_load_2d(a_dst, &maps.a, fb, a_x, a_y0 + kb * BK);
                     tma_load_2d(a_dst + MN_BOX, &maps.a, fb, a_x + 64, a_y0 + kb * BK);
                     if (WG) {
@@ -284,27 +337,32 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     ok = false;
                     break;
                 }
-                uint8_t *a_tile = smem + Smem::a_off + stage * A_BYTES;
-                uint8_t *b_tile = smem + Smem::b_off + stage * B_BYTES;
+                uint8_t *a_tile = smem + L::a_off + stage * A_BYTES;
+                uint8_t *b_tile = smem + L::b_off + stage * B_BYTES;
+                // the last K block of a weight-gradient tile: only its 16-row slices
+                // that hold rows of the segment are multiplied, and the rows past the
+                // segment inside the last of them read as zero (both operands)
+                int kslices = BK / 16;
                 if (WG && kb == nkb - 1 && tail < BK) {
-                    // rows tail..63 of every box of both operands read as zero
-                    const int zr = BK - tail;
-                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                    for (int c = lane; c < 6 * zr * 8; c += 32) {
-                        const int box = c / (zr * 8), rem = c - box * zr * 8;
-                        const int row = tail + rem / 8, ch = rem % 8;
-                        uint8_t *base = box < 2 ? a_tile + box * MN_BOX : b_tile + (box - 2) * MN_BOX;
-                        *reinterpret_cast<uint4 *>(base + row * 128 + ch * 16) = z;
+                    kslices = (tail + 15) / 16;
+                    const int zr = kslices * 16 - tail;
+                    if (zr > 0) {
+                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                        for (int c = lane; c < 6 * zr * 8; c += 32) {
+                            const int box = c / (zr * 8), rem = c - box * zr * 8;
+                            const int row = tail + rem / 8, ch = rem % 8;
+                            uint8_t *base = box < 2 ? a_tile + box * MN_BOX : b_tile + (box - 2) * MN_BOX;
+                            *reinterpret_cast<uint4 *>(base + row * 128 + ch * 16) = z;
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
                 }
                 if (lane == 0) {
                     fence_after();
                     const uint32_t a_addr = smem_u32(a_tile);
                     const uint32_t b_addr = smem_u32(b_tile);
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
+                    for (int kk = 0; kk < kslices; ++kk) {
                         const uint64_t ad = smem_desc_mn_sw128(a_addr + kk * 2048, p.lbo, p.sbo);
                         const uint64_t bd = WG ? smem_desc_mn_sw128(b_addr + kk * 2048, p.lbo, p.sbo)
                                                : smem_desc_sw128(b_addr + kk * 32);
@@ -334,9 +392,9 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     } else {   // ------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int etid = threadIdx.x - 64;
-        float *stage_f = reinterpret_cast<float *>(smem + Smem::epi_off);
-        __nv_bfloat16 *stage_h = reinterpret_cast<__nv_bfloat16 *>(smem + Smem::epi_off);
-        int *pair_s = reinterpret_cast<int *>(smem + Smem::pairs_off);
+        float *stage_f = reinterpret_cast<float *>(smem + L::epi_off);
+        __nv_bfloat16 *stage_h = reinterpret_cast<__nv_bfloat16 *>(smem + L::epi_off);
+        int *pair_s = reinterpret_cast<int *>(smem + L::pairs_off);
         float *wgt_s = reinterpret_cast<float *>(pair_s + BN);
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -359,35 +417,41 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             if (WG) {
-                // row m of the tile -> output row; 32 columns per step, written directly
-                const int m = wt.mt * BM + q * 32 + lane;
-                __nv_bfloat16 *row = nullptr;
-                int ncols;
+                // The warp's 32 accumulator rows are 32 consecutive rows of one output:
+                // 64 columns at a time go through a 128-byte-swizzled staging block
+                // [32 rows][128 bytes] into a TMA store (rows past I / H and columns past
+                // the output's width are clipped by the 3-D map).
+                const int m0 = wt.mt * BM + q * 32;
+                int sel = 0, r0 = m0, ncols = p.I;
                 if (p.wgrad_gu) {
-                    const int blk = m / 128, r128 = m % 128;
-                    const int i = blk * 64 + (r128 & 63);
-                    if (i < p.I)
-                        row = (r128 < 64 ? p.out0 : p.out1) + ((size_t)wt.e * p.I + i) * p.H;
+                    sel = q >= 2 ? 1 : 0;                  // gate rows, then up rows
+                    r0 = wt.mt * 64 + (q & 1) * 32;
                     ncols = p.H;
-                } else {
-                    if (m < p.H) row = p.out0 + ((size_t)wt.e * p.H + m) * p.I;
-                    ncols = p.I;
                 }
-                for (int c = 0; c < BN; c += CHUNK) {
+                const bool live = r0 < (p.wgrad_gu ? p.I : p.H);
+                uint8_t *stage = smem + L::epi_off + q * 8192;   // 2 chunk buffers
+                for (int c = 0; c < BN; c += 64) {
                     const int col0 = wt.nt * BN + c;
                     if (col0 >= ncols) break;   // uniform over the CTA
-                    float v[32];
+                    float v[64];
                     if (wt.nkb > 0) {
-                        tmem_ld32(taddr + c, v);
+                        tmem_ld64(taddr + c, v);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = 0.f;   // an expert with no rows
+                        for (int j = 0; j < 64; ++j) v[j] = 0.f;   // an expert with no rows
                     }
-                    if (row != nullptr)
+                    if (!live) continue;
+                    uint8_t *buf = stage + ((c / 64) & 1) * 4096;
+                    // the store that last read this buffer (two stores ago) is done
+                    if (lane == 0) tma_store_wait_read1();
+                    __syncwarp();
 #pragma unroll
-                        for (int j8 = 0; j8 < 32; j8 += 8)
-                            if (col0 + j8 < ncols)
-                                *reinterpret_cast<uint4 *>(row + col0 + j8) = pack8_bf16(v + j8);
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4 *>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+                            pack8_bf16(v + 8 * j);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) tma_store_3d(&maps.out[sel], smem_u32(buf), col0, r0, wt.e);
                 }
                 fence_before();
                 __syncwarp();
@@ -407,6 +471,23 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 #pragma unroll
                         for (int j = 0; j < CHUNK; ++j) stage_f[j * BM + f] = v[j];
                         epilogue_sync();
+                        // the four items' gate / up vectors are loaded first, so their
+                        // latencies overlap
+                        const __nv_bfloat16 *__restrict__ gu = p.gu;
+                        uint4 graw[4], uraw[4];
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const int item = etid + 128 * s;
+                            const int j = item >> 4, f8 = (item & 15) * 8;
+                            const int i = dt.f * BM + f8;
+                            graw[s] = uraw[s] = make_uint4(0u, 0u, 0u, 0u);
+                            if (c + j < dt.ntok && i < p.I) {
+                                const size_t r = (size_t)dt.tok0 + c + j;
+                                const int gcol = (i / 64) * 128 + (i % 64);
+                                graw[s] = __ldg(reinterpret_cast<const uint4 *>(gu + r * 2 * p.Ipad + gcol));
+                                uraw[s] = __ldg(reinterpret_cast<const uint4 *>(gu + r * 2 * p.Ipad + gcol + 64));
+                            }
+                        }
 #pragma unroll
                         for (int s = 0; s < 4; ++s) {
                             const int item = etid + 128 * s;
@@ -421,15 +502,15 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                                 if (i < p.I) {
                                     const float w = wgt_s[c + j];
                                     float g[8], u[8], da[8], dg[8], du[8], wa[8];
-                                    load8_bf16(p.gu + r * 2 * p.Ipad + gcol, g);
-                                    load8_bf16(p.gu + r * 2 * p.Ipad + gcol + 64, u);
+                                    Vec16<__nv_bfloat16>::to_float(graw[s], g);
+                                    Vec16<__nv_bfloat16>::to_float(uraw[s], u);
                                     const float4 d0 = *reinterpret_cast<const float4 *>(stage_f + j * BM + f8);
                                     const float4 d1 = *reinterpret_cast<const float4 *>(stage_f + j * BM + f8 + 4);
                                     da[0] = d0.x; da[1] = d0.y; da[2] = d0.z; da[3] = d0.w;
                                     da[4] = d1.x; da[5] = d1.y; da[6] = d1.z; da[7] = d1.w;
 #pragma unroll
                                     for (int x = 0; x < 8; ++x) {
-                                        const float sg = 1.0f / (1.0f + __expf(-g[x]));
+                                        const float sg = __frcp_rn(1.0f + __expf(-g[x]));
                                         const float sl = g[x] * sg;
                                         const float a = sl * u[x];
                                         part += da[x] * a;
@@ -479,6 +560,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         }
     }
 
+    if (WG && warp >= 2 && lane == 0) tma_store_wait_all();   // stores done, staging free
     fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -503,7 +585,8 @@ cudaError_t launch_bwd(const BwdMaps &maps, BwdParams prm, int64_t max_tiles, cu
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (sms_dev[dev] == 0) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::alloc);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)Smem<KIND>::alloc);
         if (e != cudaSuccess) return e;
         int n = 0;
         e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
@@ -511,7 +594,7 @@ cudaError_t launch_bwd(const BwdMaps &maps, BwdParams prm, int64_t max_tiles, cu
         sms_dev[dev] = n > 0 ? n : 148;
     }
     const int grid = (int)std::min<int64_t>(max_tiles, sms_dev[dev]);
-    return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), Smem::alloc, s, maps, prm);
+    return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), Smem<KIND>::alloc, s, maps, prm);
 }
 
 cudaError_t token_maps(BwdMaps *m, const void *t, uint64_t rows, uint64_t cols, uint64_t ld) {
@@ -586,6 +669,8 @@ cudaError_t launch_tc_wgrad_gate_up(const LayerDims &d, const void *dgu, const v
     cudaError_t e = make_map(&maps.a, dgu, rows, 2 * d.Ipad, 2 * d.Ipad, 64);
     if (e == cudaSuccess) e = make_map(&maps.b[0], send, rows, d.H, d.H, 64);
     for (int b = 1; b < 4 && e == cudaSuccess; ++b) maps.b[b] = maps.b[0];
+    if (e == cudaSuccess) e = make_store_map_3d(&maps.out[0], dw_gate, d.H, d.I, d.E, 64, 32);
+    if (e == cudaSuccess) e = make_store_map_3d(&maps.out[1], dw_up, d.H, d.I, d.E, 64, 32);
     if (e != cudaSuccess) return e;
     BwdParams prm = {};
     prm.expert_offsets = eoff;
@@ -596,8 +681,6 @@ cudaError_t launch_tc_wgrad_gate_up(const LayerDims &d, const void *dgu, const v
     prm.Ipad = d.Ipad;
     prm.H = d.H;
     prm.rows = (int)rows;
-    prm.out0 = (__nv_bfloat16 *)dw_gate;
-    prm.out1 = (__nv_bfloat16 *)dw_up;
     prm.wgrad_gu = 1;
     prm.status = status;
     return launch_bwd<BWD_WGRAD>(maps, prm, (int64_t)d.E * prm.m_tiles * prm.n_tiles, s);
@@ -611,6 +694,8 @@ cudaError_t launch_tc_wgrad_down(const LayerDims &d, const void *dout_send, cons
     cudaError_t e = make_map(&maps.a, dout_send, rows, d.H, d.H, 64);
     if (e == cudaSuccess) e = make_map(&maps.b[0], wa, rows, d.Ipad, d.Ipad, 64);
     for (int b = 1; b < 4 && e == cudaSuccess; ++b) maps.b[b] = maps.b[0];
+    if (e == cudaSuccess) e = make_store_map_3d(&maps.out[0], dw_down, d.I, d.H, d.E, 64, 32);
+    if (e == cudaSuccess) maps.out[1] = maps.out[0];
     if (e != cudaSuccess) return e;
     BwdParams prm = {};
     prm.expert_offsets = eoff;
@@ -621,7 +706,6 @@ cudaError_t launch_tc_wgrad_down(const LayerDims &d, const void *dout_send, cons
     prm.Ipad = d.Ipad;
     prm.H = d.H;
     prm.rows = (int)rows;
-    prm.out0 = (__nv_bfloat16 *)dw_down;
     prm.wgrad_gu = 0;
     prm.status = status;
     return launch_bwd<BWD_WGRAD>(maps, prm, (int64_t)d.E * prm.m_tiles * prm.n_tiles, s);

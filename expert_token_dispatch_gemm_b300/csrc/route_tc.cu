@@ -479,6 +479,21 @@ cudaError_t tc::make_map(CUtensorMap *map, const void *base, uint64_t rows, uint
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t tc::make_store_map_3d(CUtensorMap *map, void *base, uint64_t d0, uint64_t d1,
+                                 uint64_t d2, uint32_t box0, uint32_t box1) {
+    EncodeTiledFn enc;
+    cudaError_t e = get_encoder(&enc);
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_router,
                             const float *bias, int32_t *topk_idx, float *topk_w,
                             float *logits, int32_t *seg_hist, int32_t *status, int num_sms,

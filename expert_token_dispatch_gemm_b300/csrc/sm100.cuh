@@ -242,6 +242,10 @@ __device__ __forceinline__ uint4 pack8_bf16(const float *f) {
 // box of box_rows x 64 columns, 128-byte swizzle, out-of-range elements read as zero.
 cudaError_t make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint64_t ld,
                      uint32_t box_rows);
+// 3-D bf16 tensor map of a dense [d2][d1][d0] array (d0 contiguous) for TMA stores of
+// box0 x box1 tiles with 128-byte swizzle; out-of-range rows / columns are not written.
+cudaError_t make_store_map_3d(CUtensorMap *map, void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                              uint32_t box0, uint32_t box1);
 
 }  // namespace tc
 }  // namespace moe
