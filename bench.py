@@ -323,6 +323,71 @@ def run_reference(args, shape):
     print(json.dumps(line), flush=True)
 
 
+BACKWARD_LAUNCHES = 11   # permute, 4 GEMMs, logit grads, dx combine, histogram, scan, 2 router
+
+
+def time_backward(moe, args, shape, inp, packed, dist, dev, stream):
+    """A training step on the same workload: moe_layer_forward with training = 1, then
+    moe_layer_backward (CUDA events around each, `steps` timed after `warmup`). The four
+    expert GEMMs of the backward are 2 x the forward's 6 A' H I flops."""
+    cfg = moe.config(shape.N, shape.H, shape.I, shape.E, shape.top_k, shape.ep_size,
+                     shape.capacity_factor, args.mode, shape.dtype,
+                     has_bias=inp["b_router"] is not None, training=True)
+    ws = moe.alloc_workspace(cfg, dev)
+    x, wr, b, wd = inp["x"], inp["w_router"], inp["b_router"], inp["w_down"]
+    out = torch.empty(shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(7)
+    dout = torch.randn(shape.N, shape.H, device=dev, generator=gen).to(shape.torch_dtype)
+    g = dict(dx=torch.empty_like(x), dw_router=torch.empty(shape.E, shape.H, device=dev),
+             db_router=torch.empty(shape.E, device=dev), dw_gate=torch.empty_like(inp["w_gate"]),
+             dw_up=torch.empty_like(inp["w_up"]), dw_down=torch.empty_like(wd))
+    counts_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
+
+    def step(i, evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws,
+                              dict(counts=counts_t) if i == 0 else None)
+        if evs is not None:
+            evs[1].record(stream)
+        moe.moe_layer_backward(cfg, x, wr, packed, wd, dout, g["dx"], g["dw_router"],
+                               g["db_router"], g["dw_gate"], g["dw_up"], g["dw_down"], ws)
+        if evs is not None:
+            evs[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    kept = int(counts_t.sum().item())
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(2_000_000)
+    for i in range(args.steps):
+        step(1, evs[i])
+    torch.cuda.synchronize()
+    if moe.moe_read_device_status(cfg, ws):
+        raise RuntimeError("device status flags set after the backward steps")
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    step_ms = slowest_rank_ms(fwd_ms + bwd_ms, dist, dev)
+    bwd_ms = slowest_rank_ms(bwd_ms, dist, dev)
+    world = dist.get_world_size() if dist is not None else 1
+    flops = 12.0 * kept * shape.H * shape.I
+    peaks, source = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained") if peaks else None
+    ach = flops / (bwd_ms * 1e-3) / 1e12
+    return dict(train_tokens_per_s=round(job_tokens_per_s(shape.N, world, step_ms), 1),
+                forward_training_ms=round(fwd_ms, 4), backward_ms=round(bwd_ms, 4),
+                expert_gemm_tflop=round(flops / 1e12, 4),
+                roofline=dict(bound="tensor", achieved=round(ach, 1), unit="TFLOP/s",
+                              peak=peak, frac=round(ach / peak, 4) if peak else None,
+                              source=f"bf16_tflops_sustained ({source})",
+                              note="whole backward time against the expert GEMMs' flops"),
+                gpu_launches=(6 + BACKWARD_LAUNCHES) * args.steps)
+
+
 def workload_config(shape):
     return dict(workload=shape.name, tokens=shape.N, hidden=shape.H, intermediate=shape.I,
                 experts=shape.E, top_k=shape.top_k, ep_size=shape.ep_size,
@@ -342,6 +407,7 @@ def main():
     ap.add_argument("--mode", default="dispatch", choices=["dispatch", "mask_sum"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -420,6 +486,10 @@ def main():
     ms_step = slowest_rank_ms(ms_total / args.steps, dist, dev)
     value = job_tokens_per_s(shape.N, world, ms_step)
 
+    backward = None
+    if not args.no_backward and shape.dtype == "bf16":
+        backward = time_backward(moe, args, shape, inp, packed, dist, dev, stream)
+
     # end to end through the C ABI: every step copies its input from pinned host memory
     # to the device and reads its output back. Copies run on their own streams, double
     # buffered, so step i+1's upload and step i-1's download overlap step i's compute.
@@ -492,7 +562,7 @@ def main():
                                 parallelism=f"replicas x{world} (one layer per GPU)"),
                     roofline=roof, stages=per_stage, cpu_baseline=cpu, e2e=e2e,
                     gpu_launches=launches_per_step * args.steps, clocks=clk.summary(),
-                    kept_pairs=int(counts.sum()), impl="b300")
+                    kept_pairs=int(counts.sum()), backward=backward, impl="b300")
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
