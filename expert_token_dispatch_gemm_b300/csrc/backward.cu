@@ -41,12 +41,13 @@ router_dl_kernel(int N, int k, int m_tiles, int rows, const float *__restrict__ 
     }
 }
 
-// One warp per token, 16-byte vectors of 8 bf16.
+// One warp per token, 16-byte vectors (8 bf16 or 4 fp32).
+template <typename T>
 __global__ void __launch_bounds__(256)
-dx_combine_kernel(const __nv_bfloat16 *__restrict__ dx_slots, const int32_t *__restrict__ slot_pos,
+dx_combine_kernel(const T *__restrict__ dx_slots, const int32_t *__restrict__ slot_pos,
                   const int32_t *__restrict__ topk_idx, const float *__restrict__ dl,
-                  const __nv_bfloat16 *__restrict__ w_router, int N, int H, int k,
-                  __nv_bfloat16 *__restrict__ dx) {
+                  const T *__restrict__ w_router, int N, int H, int k, T *__restrict__ dx) {
+    constexpr int V = Vec16<T>::N;
     grid_dep_wait();
     grid_dep_trigger();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -55,38 +56,38 @@ dx_combine_kernel(const __nv_bfloat16 *__restrict__ dx_slots, const int32_t *__r
     const int my_slot = lane < k ? slot_pos[(size_t)t * k + lane] : -1;
     const int my_e = lane < k ? topk_idx[(size_t)t * k + lane] : 0;
     const float my_dl = lane < k ? dl[(size_t)t * k + lane] : 0.f;
-    const int nvec = H / 8;
+    const int nvec = H / V;
     for (int v = lane; v < nvec; v += 32) {
-        float acc[8] = {};
+        float acc[V] = {};
         for (int j = 0; j < k; ++j) {
             const int slot = __shfl_sync(0xffffffffu, my_slot, j);
             if (slot < 0) continue;
-            float f[8];
-            Vec16<__nv_bfloat16>::to_float(
+            float f[V];
+            Vec16<T>::to_float(
                 __ldg(reinterpret_cast<const uint4 *>(dx_slots + ((size_t)t * k + j) * H) + v), f);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) acc[c] += f[c];
+            for (int c = 0; c < V; ++c) acc[c] += f[c];
         }
         for (int j = 0; j < k; ++j) {
             const int e = __shfl_sync(0xffffffffu, my_e, j);
             const float c0 = __shfl_sync(0xffffffffu, my_dl, j);
-            float f[8];
-            Vec16<__nv_bfloat16>::to_float(
-                __ldg(reinterpret_cast<const uint4 *>(w_router + (size_t)e * H) + v), f);
+            float f[V];
+            Vec16<T>::to_float(__ldg(reinterpret_cast<const uint4 *>(w_router + (size_t)e * H) + v), f);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) acc[c] = fmaf(c0, f[c], acc[c]);
+            for (int c = 0; c < V; ++c) acc[c] = fmaf(c0, f[c], acc[c]);
         }
-        reinterpret_cast<uint4 *>(dx + (size_t)t * H)[v] = Vec16<__nv_bfloat16>::from_float(acc);
+        reinterpret_cast<uint4 *>(dx + (size_t)t * H)[v] = Vec16<T>::from_float(acc);
     }
 }
 
 // Block (expert e, column chunk of 2048, split z): the z-th contiguous part of e's
-// routed pairs, in order; partial [Z, E, H] fp32, and the part's sum of dl.
+// routed pairs, in order; partial [Z, E, H] fp32, and the part's sum of dl. Each thread
+// owns 8 columns.
+template <typename T>
 __global__ void __launch_bounds__(256)
 router_wgrad_partial_kernel(const int32_t *__restrict__ eoff_all, const int32_t *__restrict__ perm_all,
-                            const float *__restrict__ dl, const __nv_bfloat16 *__restrict__ x,
-                            int H, int E, int k, float *__restrict__ partial,
-                            float *__restrict__ partial_db) {
+                            const float *__restrict__ dl, const T *__restrict__ x, int H, int E,
+                            int k, float *__restrict__ partial, float *__restrict__ partial_db) {
     grid_dep_wait();
     grid_dep_trigger();
     const int e = blockIdx.x, z = blockIdx.z, Z = gridDim.z;
@@ -100,8 +101,9 @@ router_wgrad_partial_kernel(const int32_t *__restrict__ eoff_all, const int32_t 
             const int pr = perm_all[r];
             const float c0 = dl[pr];
             float f[8];
-            Vec16<__nv_bfloat16>::to_float(
-                __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(pr / k) * H + col)), f);
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(pr / k) * H + col);
+            Vec16<T>::to_float(__ldg(src), f);
+            if (Vec16<T>::N == 4) Vec16<T>::to_float(__ldg(src + 1), f + 4);
 #pragma unroll
             for (int c = 0; c < 8; ++c) acc[c] = fmaf(c0, f[c], acc[c]);
             db += c0;
@@ -151,21 +153,28 @@ cudaError_t launch_router_dl(const LayerDims &d, const float *dweight_part, int 
 cudaError_t launch_dx_combine(const LayerDims &d, const void *dx_slots, const int32_t *slot_pos,
                               const int32_t *topk_idx, const float *dl, const void *w_router,
                               void *dx, cudaStream_t s) {
-    return launch_pdl(dx_combine_kernel, dim3(ceil_div(d.N, 8)), dim3(256), 0, s,
-                      (const __nv_bfloat16 *)dx_slots, slot_pos, topk_idx, dl,
-                      (const __nv_bfloat16 *)w_router, d.N, d.H, d.k, (__nv_bfloat16 *)dx);
+    if (d.dtype == MOE_DTYPE_BF16)
+        return launch_pdl(dx_combine_kernel<__nv_bfloat16>, dim3(ceil_div(d.N, 8)), dim3(256), 0, s,
+                          (const __nv_bfloat16 *)dx_slots, slot_pos, topk_idx, dl,
+                          (const __nv_bfloat16 *)w_router, d.N, d.H, d.k, (__nv_bfloat16 *)dx);
+    return launch_pdl(dx_combine_kernel<float>, dim3(ceil_div(d.N, 8)), dim3(256), 0, s,
+                      (const float *)dx_slots, slot_pos, topk_idx, dl, (const float *)w_router, d.N,
+                      d.H, d.k, (float *)dx);
 }
 
 cudaError_t launch_router_wgrad(const LayerDims &d, const int32_t *eoff_all, const int32_t *perm_all,
                                 const float *dl, const void *x, float *partial, float *partial_db,
                                 float *dw_router, float *db_router, cudaStream_t s) {
     const int Z = router_wgrad_splits(d);
-    cudaError_t e = launch_pdl(router_wgrad_partial_kernel, dim3(d.E, ceil_div(d.H, 2048), Z),
-                               dim3(256), 0, s, eoff_all, perm_all, dl, (const __nv_bfloat16 *)x, d.H,
-                               d.E, d.k, partial, partial_db);
+    const dim3 grid(d.E, ceil_div(d.H, 2048), Z);
+    cudaError_t e = d.dtype == MOE_DTYPE_BF16
+        ? launch_pdl(router_wgrad_partial_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, eoff_all,
+                     perm_all, dl, (const __nv_bfloat16 *)x, d.H, d.E, d.k, partial, partial_db)
+        : launch_pdl(router_wgrad_partial_kernel<float>, grid, dim3(256), 0, s, eoff_all, perm_all,
+                     dl, (const float *)x, d.H, d.E, d.k, partial, partial_db);
     if (e != cudaSuccess) return e;
-    const int grid = (int)std::min<int64_t>(ceil_div64((int64_t)d.E * d.H, 256), 148 * 4);
-    return launch_pdl(router_wgrad_reduce_kernel, dim3(grid), dim3(256), 0, s,
+    const int rgrid = (int)std::min<int64_t>(ceil_div64((int64_t)d.E * d.H, 256), 148 * 4);
+    return launch_pdl(router_wgrad_reduce_kernel, dim3(rgrid), dim3(256), 0, s,
                       (const float *)partial, (const float *)partial_db, Z, d.E, d.H, dw_router,
                       db_router);
 }

@@ -161,7 +161,8 @@ cudaError_t launch_tc_route(const LayerDims &d, const void *x, const void *w_rou
 // outputs.
 constexpr int kStatsBlocks = 256;
 
-// Backward (bf16): tensor-core grouped GEMMs, then the router / combine kernels.
+// Backward: grouped GEMMs (tensor cores for bf16, FFMA for fp32), then the router /
+// combine kernels.
 cudaError_t launch_tc_dgrad_down(const LayerDims &d, const void *dout_send, const int32_t *eoff,
                                  const void *w_down, const void *gu, const int32_t *perm,
                                  const float *topk_w, void *dgu, void *wa, float *dweight_part,
@@ -175,6 +176,18 @@ cudaError_t launch_tc_wgrad_gate_up(const LayerDims &d, const void *dgu, const v
 cudaError_t launch_tc_wgrad_down(const LayerDims &d, const void *dout_send, const void *wa,
                                  const int32_t *eoff, void *dw_down, int32_t *status,
                                  cudaStream_t s);
+cudaError_t launch_simt_dgrad_down(const LayerDims &d, const float *dout_send, const int32_t *eoff,
+                                   const float *w_down, const float *gu, const int32_t *perm,
+                                   const float *topk_w, float *dgu, float *wa, float *dweight_part,
+                                   cudaStream_t s);
+cudaError_t launch_simt_dgrad_gate_up(const LayerDims &d, const float *dgu, const int32_t *eoff,
+                                      const float *packed, const int32_t *perm, float *dx_slots,
+                                      cudaStream_t s);
+cudaError_t launch_simt_wgrad_gate_up(const LayerDims &d, const float *dgu, const float *send,
+                                      const int32_t *eoff, float *dw_gate, float *dw_up,
+                                      cudaStream_t s);
+cudaError_t launch_simt_wgrad_down(const LayerDims &d, const float *dout_send, const float *wa,
+                                   const int32_t *eoff, float *dw_down, cudaStream_t s);
 int router_wgrad_splits(const LayerDims &d);
 cudaError_t launch_router_dl(const LayerDims &d, const float *dweight_part, int m_tiles,
                              const int32_t *slot_pos, const float *topk_w, float *dl,
@@ -194,7 +207,8 @@ cudaError_t launch_tp_reduce(const LayerDims &d, int tp_size, const void *padded
 // fp32 FFMA grouped FFN.
 cudaError_t launch_simt_gate_up(const LayerDims &d, const float *send,
                                 const int32_t *expert_offsets, int e_begin, int e_end,
-                                const float *packed, float *h, cudaStream_t s);
+                                const float *packed, float *h, float *gu /* [N*k, 2 Ipad] or nullptr */,
+                                cudaStream_t s);
 cudaError_t launch_simt_down(const LayerDims &d, const float *h, const int32_t *expert_offsets,
                              int e_begin, int e_end, const float *w_down, const int32_t *perm,
                              const float *topk_w, float *out_slots, cudaStream_t s);

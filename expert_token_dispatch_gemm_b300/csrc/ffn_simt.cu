@@ -31,7 +31,7 @@ __device__ __forceinline__ void st_col(float (*s)[W], int k, int r, float4 v) {
 __global__ void __launch_bounds__(256, 2)
 simt_gate_up_kernel(const float *__restrict__ send, const int32_t *__restrict__ eoff, int e_begin,
                     int ne, const float *__restrict__ packed, int H, int Ipad,
-                    float *__restrict__ hbuf) {
+                    float *__restrict__ hbuf, float *__restrict__ gu) {
     grid_dep_wait();
     grid_dep_trigger();
     __shared__ int eo[kMaxExperts + 1], mtp[kMaxExperts + 1];
@@ -107,6 +107,12 @@ simt_gate_up_kernel(const float *__restrict__ send, const int32_t *__restrict__ 
                 }
                 *reinterpret_cast<float4 *>(hbuf + (size_t)(row0 + rr) * Ipad + col0 + tx * 4) =
                     make_float4(o[0], o[1], o[2], o[3]);
+                if (gu != nullptr) {   // training: the pre-activations, packed column order
+                    float *gd = gu + (size_t)(row0 + rr) * 2 * Ipad + (col0 / kGateUpBlock) * 2 * kGateUpBlock + tx * 4;
+                    *reinterpret_cast<float4 *>(gd) = make_float4(ag[r][0], ag[r][1], ag[r][2], ag[r][3]);
+                    *reinterpret_cast<float4 *>(gd + kGateUpBlock) =
+                        make_float4(au[r][0], au[r][1], au[r][2], au[r][3]);
+                }
             }
         }
     }
@@ -192,12 +198,12 @@ int simt_grid(const LayerDims &d, int ne, int n_tiles) {
 
 cudaError_t launch_simt_gate_up(const LayerDims &d, const float *send,
                                 const int32_t *expert_offsets, int e_begin, int e_end,
-                                const float *packed, float *h, cudaStream_t s) {
+                                const float *packed, float *h, float *gu, cudaStream_t s) {
     const int ne = e_end - e_begin;
     const int grid = simt_grid(d, ne, d.Ipad / SBN);
     if (grid <= 0) return cudaSuccess;
     return launch_pdl(simt_gate_up_kernel, dim3(grid), dim3(256), 0, s, send, expert_offsets, e_begin,
-                      ne, packed, d.H, d.Ipad, h);
+                      ne, packed, d.H, d.Ipad, h, gu);
 }
 
 cudaError_t launch_simt_down(const LayerDims &d, const float *h, const int32_t *expert_offsets,

@@ -96,8 +96,6 @@ moe_status_t check_config(const moe_config *cfg, LayerDims *d) {
         return fail(MOE_ERR_INVALID_ARG, "unknown capacity_priority %d", cfg->capacity_priority);
     d->slot_priority = cfg->capacity_priority == MOE_PRIORITY_SLOT;
     if (cfg->training != 0 && cfg->training != 1) return fail(MOE_ERR_INVALID_ARG, "training must be 0 or 1");
-    if (cfg->training && cfg->dtype != MOE_DTYPE_BF16)
-        return fail(MOE_ERR_UNSUPPORTED, "the backward is implemented for bf16 layers");
     d->training = cfg->training;
     if (cfg->capacity_factor > 0.f) {
         // cf * N * k is exact in double (24-bit cf times an integer below 2^29); if the
@@ -172,7 +170,7 @@ Workspace carve(const LayerDims &d, int mode, void *base) {
         w.gu = take(pairs * 2 * d.Ipad * esize(d));
         w.dout_send = take(pairs * d.H * esize(d));
         w.dgu = take(pairs * 2 * d.Ipad * esize(d));
-        w.dweight_part = (float *)take((size_t)(d.Ipad / 128) * pairs * sizeof(float));
+        w.dweight_part = (float *)take((size_t)(d.Ipad / 64) * pairs * sizeof(float));
         w.dl = (float *)take(pairs * sizeof(float));
         w.routed_all = (int32_t *)take(d.E * sizeof(int32_t));
         w.counts_all = (int32_t *)take(d.E * sizeof(int32_t));
@@ -251,7 +249,7 @@ moe_status_t run_gate_up(const LayerDims &d, const void *send, const int32_t *eo
                  "tensor-core gate/up kernel");
     else
         MOE_CUDA(launch_simt_gate_up(d, (const float *)send, eoff, e0, e1, (const float *)packed,
-                                     (float *)w.h, s),
+                                     (float *)w.h, (float *)gu, s),
                  "fp32 gate/up kernel");
     return MOE_OK;
 }
@@ -685,20 +683,40 @@ moe_status_t moe_layer_backward(const moe_config *cfg, const void *x, const void
     // 1. the upstream gradient of every kept pair, in the send layout
     MOE_CUDA(launch_permute(d, dout, w.slot_pos, w.dout_send, s), "permute kernel");
     // 2. dgrad of the down projection with the SwiGLU backward: dgu, w*a, dweight parts
-    MOE_CUDA(launch_tc_dgrad_down(d, w.dout_send, w.eoff, w_down, w.gu, w.perm, w.topk_w, w.dgu,
-                                  w.h, w.dweight_part, w.status, s),
-             "tensor-core dgrad-down kernel");
     // 3. dgrad of gate / up: every kept pair's dx into its slot
-    MOE_CUDA(launch_tc_dgrad_gate_up(d, w.dgu, w.eoff, w_gate_up_packed, w.perm, w.slots, w.status,
-                                     s),
-             "tensor-core dgrad-gate/up kernel");
     // 4. weight gradients of the experts
-    MOE_CUDA(launch_tc_wgrad_gate_up(d, w.dgu, w.send, w.eoff, dw_gate, dw_up, w.status, s),
-             "tensor-core wgrad-gate/up kernel");
-    MOE_CUDA(launch_tc_wgrad_down(d, w.dout_send, w.h, w.eoff, dw_down, w.status, s),
-             "tensor-core wgrad-down kernel");
+    int dw_tiles;   // M tiles of the dweight partials
+    if (d.dtype == MOE_DTYPE_BF16) {
+        dw_tiles = d.Ipad / 128;
+        MOE_CUDA(launch_tc_dgrad_down(d, w.dout_send, w.eoff, w_down, w.gu, w.perm, w.topk_w,
+                                      w.dgu, w.h, w.dweight_part, w.status, s),
+                 "tensor-core dgrad-down kernel");
+        MOE_CUDA(launch_tc_dgrad_gate_up(d, w.dgu, w.eoff, w_gate_up_packed, w.perm, w.slots,
+                                         w.status, s),
+                 "tensor-core dgrad-gate/up kernel");
+        MOE_CUDA(launch_tc_wgrad_gate_up(d, w.dgu, w.send, w.eoff, dw_gate, dw_up, w.status, s),
+                 "tensor-core wgrad-gate/up kernel");
+        MOE_CUDA(launch_tc_wgrad_down(d, w.dout_send, w.h, w.eoff, dw_down, w.status, s),
+                 "tensor-core wgrad-down kernel");
+    } else {
+        dw_tiles = d.Ipad / 64;
+        MOE_CUDA(launch_simt_dgrad_down(d, (const float *)w.dout_send, w.eoff, (const float *)w_down,
+                                        (const float *)w.gu, w.perm, w.topk_w, (float *)w.dgu,
+                                        (float *)w.h, w.dweight_part, s),
+                 "fp32 dgrad-down kernel");
+        MOE_CUDA(launch_simt_dgrad_gate_up(d, (const float *)w.dgu, w.eoff,
+                                           (const float *)w_gate_up_packed, w.perm,
+                                           (float *)w.slots, s),
+                 "fp32 dgrad-gate/up kernel");
+        MOE_CUDA(launch_simt_wgrad_gate_up(d, (const float *)w.dgu, (const float *)w.send, w.eoff,
+                                           (float *)dw_gate, (float *)dw_up, s),
+                 "fp32 wgrad-gate/up kernel");
+        MOE_CUDA(launch_simt_wgrad_down(d, (const float *)w.dout_send, (const float *)w.h, w.eoff,
+                                        (float *)dw_down, s),
+                 "fp32 wgrad-down kernel");
+    }
     // 5. routing-weight and logit gradients, dx
-    MOE_CUDA(launch_router_dl(d, w.dweight_part, d.Ipad / 128, w.slot_pos, w.topk_w, w.dl, s),
+    MOE_CUDA(launch_router_dl(d, w.dweight_part, dw_tiles, w.slot_pos, w.topk_w, w.dl, s),
              "router logit-gradient kernel");
     MOE_CUDA(launch_dx_combine(d, w.slots, w.slot_pos, w.topk_idx, w.dl, w_router, dx, s),
              "dx combine kernel");

@@ -10,5 +10,5 @@ from .moe import (  # noqa: F401
     silu, swiglu_expert, expert_outputs, combine_dispatch, combine_mask_sum,
     layer_forward, token_outputs, selection_scores, group_limited_top_k, route_variant,
     update_selection_bias, silu_grad, layer_backward, balance_stats, tp_slices,
-    tp_row_split_forward,
+    tp_row_split_forward, token_input_grads, expert_weight_grads,
 )

@@ -479,3 +479,54 @@ def layer_backward(x, w_router, b_router, w_gate, w_up, w_down, top_k, ep_size, 
     dbr = dlogits.sum(axis=0)
     return dict(dx=dx, dw_router=dwr, db_router=dbr, dw_gate=dwg, dw_up=dwu, dw_down=dwd,
                 dlogits=dlogits, forward=fwd)
+
+
+def token_input_grads(x_rows, dout_rows, idx_rows, w_rows, keep_rows, w_router, expert_weights):
+    """dx of a few tokens, one at a time (for sampled checks at full size), by the same
+    chain rule as layer_backward with the batch's routing and keep decisions given.
+    Per token: y_j = FFN_{e_j}(x) for kept pairs, dweight_j = <dout, y_j> (0 if dropped),
+    dl_j = w_j (dweight_j - sum_j' w_j' dweight_j'), and
+    dx = sum_j kept [W_g^T dg_j + W_u^T du_j] + sum_j dl_j W_r[e_j], with
+    dg_j = w_j (W_d^T dout) * u * silu'(g), du_j = w_j (W_d^T dout) * silu(g).
+    expert_weights(e) returns (w_gate[e], w_up[e], w_down[e])."""
+    x_rows = _f64(x_rows)
+    dout_rows = _f64(dout_rows)
+    n, k = np.shape(idx_rows)
+    wr = _f64(w_router)
+    out = np.zeros_like(x_rows)
+    for i in range(n):
+        x, dy = x_rows[i], dout_rows[i]
+        dweight = np.zeros(k)
+        dx = np.zeros_like(x)
+        for j in range(k):
+            if not keep_rows[i][j]:
+                continue
+            wg, wu, wd = (_f64(a) for a in expert_weights(int(idx_rows[i][j])))
+            g, u = wg @ x, wu @ x
+            y = wd @ (silu(g) * u)
+            dweight[j] = float(dy @ y)
+            da = float(w_rows[i][j]) * (wd.T @ dy)
+            dx += wg.T @ (da * u * silu_grad(g)) + wu.T @ (da * silu(g))
+        w = _f64(w_rows[i])
+        dl = w * (dweight - float(np.sum(w * dweight)))
+        for j in range(k):
+            dx += dl[j] * wr[int(idx_rows[i][j])]
+        out[i] = dx
+    return out
+
+
+def expert_weight_grads(x_rows, dout_rows, w_rows, w_gate, w_up, w_down):
+    """Weight gradients of one expert from all its kept rows (send order): x_rows,
+    dout_rows [n, H] of the rows' tokens, w_rows [n] their routing weights.
+    dW_down = sum_r (w_r dout_r) a_r^T, dW_gate = sum_r dg_r x_r^T, dW_up = sum_r du_r x_r^T
+    with a = silu(g) * u, da = W_d^T (w dout), dg = da * u * silu'(g), du = da * silu(g).
+    Returns (dw_gate [I, H], dw_up [I, H], dw_down [H, I])."""
+    X = _f64(x_rows)
+    dY = _f64(dout_rows) * _f64(w_rows)[:, None]
+    wg, wu, wd = _f64(w_gate), _f64(w_up), _f64(w_down)
+    G, U = X @ wg.T, X @ wu.T
+    A = silu(G) * U
+    dA = dY @ wd
+    dG = dA * U * silu_grad(G)
+    dU = dA * silu(G)
+    return dG.T @ X, dU.T @ X, dY.T @ A

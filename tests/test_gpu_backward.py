@@ -1,8 +1,9 @@
-"""Backward of the layer on the GPU (moe_layer_backward, bf16), through the C ABI,
-against the fp64 oracle's chain rule (oracle.layer_backward) on the same seeded inputs.
+"""Backward of the layer on the GPU (moe_layer_backward), through the C ABI, against the
+fp64 oracle's chain rule (oracle.layer_backward) on the same seeded inputs.
 
-Bar: every gradient within 2e-2 * max|ref| (the bf16 rule of the forward: the
-operands and the intermediate gradients are bf16, every product accumulates in fp32).
+Bar: every gradient within 2e-2 * max|ref| for bf16 layers (the forward's bf16 rule: the
+operands and the intermediate gradients are bf16, every product accumulates in fp32)
+and 1e-4 * max|ref| for fp32 layers (the forward's fp32 rule).
 Routing is exact on the dyadic input variant, so both sides differentiate the same
 selection. The shapes span several M / N / K tiles with ragged tails (H and I not
 multiples of 64 or 128), capacity drops, slot-major priority, mask-and-sum mode, a
@@ -15,7 +16,7 @@ import torch
 import expert_token_dispatch_gemm_b300 as moe
 import oracle
 import workloads
-from moe_gpu_harness import BF16_TOL, assert_close, f64, make_cfg
+from moe_gpu_harness import BF16_TOL, assert_close, f64, make_cfg, tol_for
 
 pytestmark = pytest.mark.gpu
 
@@ -29,6 +30,10 @@ SHAPES = [
     S("b_sparse", N=20, H=128, I=64, E=32, top_k=2, ep_size=8),     # most experts get no rows
     S("b_one", N=1, H=64, I=64, E=4, top_k=2, ep_size=2),
     S("b_long_seg", N=1200, H=192, I=320, E=4, top_k=1, ep_size=2),  # segments > 256 rows
+    # fp32 layers (FFMA kernels): ragged tiles, drops, the PR1 configuration
+    S("f_ragged", N=333, H=96, I=72, E=8, top_k=2, ep_size=4, dtype="fp32", bias=True),
+    S("f_cap", N=500, H=64, I=136, E=4, top_k=2, ep_size=2, capacity_factor=0.6, dtype="fp32"),
+    workloads.PR1_FP32,
 ]
 
 
@@ -43,7 +48,7 @@ def _run(shape, inp, dout, mode="dispatch", capacity_priority="token"):
     wg, wu, wd = (inp[n].to(dev).contiguous() for n in ("w_gate", "w_up", "w_down"))
     packed = moe.moe_pack_weights(cfg, wg, wu)
     ws = moe.alloc_workspace(cfg)
-    out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((shape.N, shape.H), dtype=shape.torch_dtype, device=dev)
     moe.moe_layer_forward(cfg, x, wr, br, packed, wd, out, ws)
     g = dict(dx=torch.full_like(x, float("nan")),
              dw_router=torch.full((shape.E, shape.H), float("nan"), device=dev),
@@ -60,7 +65,7 @@ def _run(shape, inp, dout, mode="dispatch", capacity_priority="token"):
 
 def _dout(shape, seed):
     gen = torch.Generator().manual_seed(seed)
-    return torch.randn((shape.N, shape.H), generator=gen).to(torch.bfloat16)
+    return torch.randn((shape.N, shape.H), generator=gen).to(shape.torch_dtype)
 
 
 def _oracle(shape, inp, dout, capacity_priority="token"):
@@ -71,9 +76,9 @@ def _oracle(shape, inp, dout, capacity_priority="token"):
                                  capacity_priority=capacity_priority)
 
 
-def _compare(g, ref):
+def _compare(g, ref, tol=BF16_TOL):
     for key in ("dx", "dw_router", "db_router", "dw_gate", "dw_up", "dw_down"):
-        assert_close(g[key], ref[key], BF16_TOL, key)
+        assert_close(g[key], ref[key], tol, key)
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
@@ -81,7 +86,7 @@ def test_layer_backward_matches_oracle(shape):
     inp = workloads.layer_inputs(shape, seed=51, variant="exact")
     dout = _dout(shape, 52)
     _, g = _run(shape, inp, dout)
-    _compare(g, _oracle(shape, inp, dout))
+    _compare(g, _oracle(shape, inp, dout), tol_for(shape))
 
 
 def test_backward_with_slot_priority_and_mask_mode():
@@ -135,3 +140,75 @@ def test_training_forward_output_and_diagnostics_are_unchanged():
     assert torch.equal(outs[0][0], outs[1][0])
     for key in ("topk_idx", "slot_pos"):
         assert torch.equal(outs[0][1][key], outs[1][1][key])
+
+
+# ------------------------------------------------------------------ full size, sampled
+FULL = [workloads.GPTOSS, workloads.E8_TOP2, workloads.SKEWED_CAP, workloads.DECODE]
+
+
+def _sampled_experts(shape, counts):
+    """The most loaded expert plus, where cheap enough in fp64 on the host, a median one
+    (the 8-expert workload's experts hold ~4096 rows of 4096 x 14336: none is sampled)."""
+    if shape.I * shape.H * int(counts.max()) > 3e10:
+        return []
+    order = np.argsort(counts, kind="stable")
+    picks = [int(order[-1]), int(order[len(order) // 2])]
+    return sorted(set(e for e in picks if counts[e] > 0))
+
+
+@pytest.mark.parametrize("shape", FULL, ids=lambda s: s.name)
+def test_full_size_backward_sampled(shape):
+    """The bench's workloads at full size, in the bench's launch configuration (fused
+    training forward, then moe_layer_backward): dx on sampled tokens (tokens with
+    dropped pairs included) and the weight gradients of sampled experts against the
+    oracle's per-token / per-expert chain rule, with the oracle's own routing and drops.
+    The router weight gradient needs every pair's expert output, i.e. the whole fp64
+    layer, so it is checked at the small sizes above only."""
+    from moe_gpu_harness import Layer, full_size_reference_routing
+    torch.manual_seed(0)
+    inp = workloads.layer_inputs(shape, seed=0, variant="exact", device="cuda")
+    layer = Layer(shape, inp)
+    del inp
+    layer.cfg.training = 1
+    layer.ws = moe.alloc_workspace(layer.cfg)
+    dout = _dout(shape, 61).cuda()
+    out = torch.empty((shape.N, shape.H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_layer_forward(layer.cfg, layer.x, layer.w_router, layer.b_router, layer.packed,
+                          layer.w_down, out, layer.ws)
+    g = dict(dx=torch.empty_like(layer.x),
+             dw_router=torch.empty((shape.E, shape.H), device="cuda"),
+             dw_gate=torch.empty_like(layer.w_gate), dw_up=torch.empty_like(layer.w_up),
+             dw_down=torch.empty_like(layer.w_down))
+    moe.moe_layer_backward(layer.cfg, layer.x, layer.w_router, layer.packed, layer.w_down,
+                           dout, g["dx"], g["dw_router"], None, g["dw_gate"], g["dw_up"],
+                           g["dw_down"], layer.ws)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    ref = full_size_reference_routing(layer)
+    sp = ref["slot_pos"].reshape(shape.N, shape.top_k)
+    rng = np.random.default_rng(1)
+    sample = np.sort(rng.choice(shape.N, min(shape.N, 24), replace=False))
+    if ref["capacity"] is not None:
+        dropped = np.nonzero((sp < 0).any(axis=1))[0]
+        assert dropped.size > 0
+        sample = np.unique(np.concatenate([sample, dropped[:4], dropped[-4:]]))
+    s_dev = torch.as_tensor(sample, device="cuda")
+
+    def weights(e):
+        return f64(layer.w_gate[e]), f64(layer.w_up[e]), f64(layer.w_down[e])
+
+    want = oracle.token_input_grads(f64(layer.x[s_dev]), f64(dout[s_dev]), ref["topk_idx"][sample],
+                                    ref["topk_w"][sample], sp[sample] >= 0, f64(layer.w_router),
+                                    weights)
+    assert_close(g["dx"][s_dev], want, BF16_TOL, "sampled dx")
+    counts = np.asarray(ref["counts"])
+    w_flat = np.asarray(ref["topk_w"]).reshape(-1)
+    for e in _sampled_experts(shape, counts):
+        a, z = int(ref["expert_offsets"][e]), int(ref["expert_offsets"][e + 1])
+        pairs = np.asarray(ref["perm"][a:z])
+        t_dev = torch.as_tensor(pairs // shape.top_k, device="cuda")
+        dg, du, dd = oracle.expert_weight_grads(f64(layer.x[t_dev]), f64(dout[t_dev]),
+                                                w_flat[pairs], *weights(e))
+        assert_close(g["dw_gate"][e], dg, BF16_TOL, f"dW_gate[{e}]")
+        assert_close(g["dw_up"][e], du, BF16_TOL, f"dW_up[{e}]")
+        assert_close(g["dw_down"][e], dd, BF16_TOL, f"dW_down[{e}]")

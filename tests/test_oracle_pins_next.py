@@ -301,3 +301,32 @@ def test_tp_split_capacity_is_per_slice():
     whole = brute_force_layer(x, wr, b, wg, wu, wd, k, 2,
                               oracle.expert_capacity(0.5, N, k, E))["out"]
     assert rel_err(out, whole) > 1e-6          # the slices' drops differ from the batch's
+
+
+# ------------------------------------------------------------------ sampled backward
+def test_sampled_backward_functions_equal_the_batch_backward():
+    """The per-token dx and per-expert weight gradients used for full-size sampled checks
+    give the whole-batch backward's rows and blocks (with the batch's keep decisions)."""
+    case = (71, 24, 8, 6, 5, 2, 5, 0.6, None)
+    seed, N, H, I, E, k, P, cf, _ = case
+    x, wr, b, wg, wu, wd, dout = _bwd_inputs(case)
+    g = oracle.layer_backward(x, wr, b, wg, wu, wd, k, P, dout, cf)
+    fwd = g["forward"]
+    keep = fwd["slot_pos"].reshape(N, k) >= 0
+    assert not keep.all()
+    sample = np.array([0, 5, 11, 23])
+    got = oracle.token_input_grads(x[sample], dout[sample], fwd["topk_idx"][sample],
+                                   fwd["topk_w"][sample], keep[sample], wr,
+                                   lambda e: (wg[e], wu[e], wd[e]))
+    assert rel_err(got, g["dx"][sample]) < 1e-12
+    for e in range(E):
+        a, z = fwd["expert_offsets"][e], fwd["expert_offsets"][e + 1]
+        pairs = fwd["perm"][a:z]
+        if len(pairs) == 0:
+            continue
+        t = pairs // k
+        w = fwd["topk_w"].reshape(-1)[pairs]
+        dg, du, dd = oracle.expert_weight_grads(x[t], dout[t], w, wg[e], wu[e], wd[e])
+        assert rel_err(dg, g["dw_gate"][e]) < 1e-12
+        assert rel_err(du, g["dw_up"][e]) < 1e-12
+        assert rel_err(dd, g["dw_down"][e]) < 1e-12
