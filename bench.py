@@ -388,6 +388,63 @@ def time_backward(moe, args, shape, inp, packed, dist, dev, stream):
                 gpu_launches=(6 + BACKWARD_LAUNCHES) * args.steps)
 
 
+def _event_ms(stream, fn, steps):
+    """Mean CUDA-event time of fn over `steps` runs (after one warm-up run)."""
+    fn()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(1_000_000)
+    s0.record(stream)
+    for _ in range(steps):
+        fn()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    return s0.elapsed_time(s1) / steps
+
+
+def time_variants(moe, args, shape, inp, packed, dev, stream):
+    """The widened rows on the same workload: the forward with slot-major capacity
+    priority, the router load statistics (moe_balance_stats over the logits the forward
+    writes) and the TP split's padded ordered sum (tp = 2)."""
+    peaks, source = load_peaks()
+    bw = peaks["hbm_gbs"]
+    s = 2 if shape.dtype == "bf16" else 4
+    x, wr, b, wd = inp["x"], inp["w_router"], inp["b_router"], inp["w_down"]
+    out = torch.empty(shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
+    res = {}
+    cfg = moe.config(shape.N, shape.H, shape.I, shape.E, shape.top_k, shape.ep_size,
+                     shape.capacity_factor, args.mode, shape.dtype,
+                     has_bias=b is not None, capacity_priority="slot")
+    ws = moe.alloc_workspace(cfg, dev)
+    ms = _event_ms(stream, lambda: moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws),
+                   args.steps)
+    res["slot_priority_forward"] = dict(ms=round(ms, 4),
+                                        tokens_per_s=round(shape.N / (ms * 1e-3), 1),
+                                        gpu_launches_per_step=7)
+    logits = torch.empty(shape.N, shape.E, device=dev)
+    routed = torch.empty(shape.E, dtype=torch.int32, device=dev)
+    moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws,
+                          dict(router_logits=logits, routed_counts=routed))
+    load = torch.empty(shape.E, device=dev)
+    prob = torch.empty(shape.E, device=dev)
+    ms = _event_ms(stream, lambda: moe.moe_balance_stats(cfg, logits, routed, load, prob, ws),
+                   args.steps)
+    nbytes = shape.N * shape.E * 4 + shape.E * 12
+    res["balance_stats"] = dict(ms=round(ms, 4), bound="hbm", achieved=round(nbytes / ms / 1e6, 1),
+                                peak=bw, unit="GB/s", frac=round(nbytes / ms / 1e6 / bw, 4),
+                                gpu_launches_per_step=2)
+    padded = torch.zeros(2, shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
+    ms = _event_ms(stream, lambda: moe.moe_tp_reduce(cfg, 2, padded, out), args.steps)
+    nbytes = 3 * shape.N * shape.H * s
+    res["tp_reduce_tp2"] = dict(ms=round(ms, 4), bound="hbm", achieved=round(nbytes / ms / 1e6, 1),
+                                peak=bw, unit="GB/s", frac=round(nbytes / ms / 1e6 / bw, 4),
+                                gpu_launches_per_step=1,
+                                note="inputs below L2 size at small workloads: fractions above "
+                                     "1 are L2 hits")
+    res["peak_source"] = source
+    return res
+
+
 def workload_config(shape):
     return dict(workload=shape.name, tokens=shape.N, hidden=shape.H, intermediate=shape.I,
                 experts=shape.E, top_k=shape.top_k, ep_size=shape.ep_size,
@@ -408,6 +465,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -487,8 +545,11 @@ def main():
     value = job_tokens_per_s(shape.N, world, ms_step)
 
     backward = None
-    if not args.no_backward and shape.dtype == "bf16":
+    if not args.no_backward:
         backward = time_backward(moe, args, shape, inp, packed, dist, dev, stream)
+    variants = None
+    if not args.no_variants:
+        variants = time_variants(moe, args, shape, inp, packed, dev, stream)
 
     # end to end through the C ABI: every step copies its input from pinned host memory
     # to the device and reads its output back. Copies run on their own streams, double
@@ -562,7 +623,8 @@ def main():
                                 parallelism=f"replicas x{world} (one layer per GPU)"),
                     roofline=roof, stages=per_stage, cpu_baseline=cpu, e2e=e2e,
                     gpu_launches=launches_per_step * args.steps, clocks=clk.summary(),
-                    kept_pairs=int(counts.sum()), backward=backward, impl="b300")
+                    kept_pairs=int(counts.sum()), backward=backward, variants=variants,
+                    impl="b300")
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
