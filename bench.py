@@ -376,14 +376,17 @@ def time_backward(moe, args, shape, inp, packed, dist, dev, stream):
     world = dist.get_world_size() if dist is not None else 1
     flops = 12.0 * kept * shape.H * shape.I
     peaks, source = load_peaks()
-    peak = peaks.get("bf16_tflops_sustained") if peaks else None
+    if shape.dtype == "bf16":
+        bound, peak, psrc = "tensor", peaks.get("bf16_tflops_sustained"), f"bf16_tflops_sustained ({source})"
+    else:
+        bound, peak, psrc = "alu", fp32_alu_tflops(peaks), "FFMA: 148 SMs x 128 lanes x 2 x max SM clock"
     ach = flops / (bwd_ms * 1e-3) / 1e12
     return dict(train_tokens_per_s=round(job_tokens_per_s(shape.N, world, step_ms), 1),
                 forward_training_ms=round(fwd_ms, 4), backward_ms=round(bwd_ms, 4),
                 expert_gemm_tflop=round(flops / 1e12, 4),
-                roofline=dict(bound="tensor", achieved=round(ach, 1), unit="TFLOP/s",
+                roofline=dict(bound=bound, achieved=round(ach, 1), unit="TFLOP/s",
                               peak=peak, frac=round(ach / peak, 4) if peak else None,
-                              source=f"bf16_tflops_sustained ({source})",
+                              source=psrc,
                               note="whole backward time against the expert GEMMs' flops"),
                 gpu_launches=(6 + BACKWARD_LAUNCHES) * args.steps)
 
