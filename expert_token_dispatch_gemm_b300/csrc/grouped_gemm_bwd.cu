@@ -22,7 +22,9 @@
 //               weight-gradient GEMMs the warp first zeroes the rows of the last K block
 //               that lie past the expert's segment, in both operands (they hold another
 //               expert's rows, or unwritten memory past the kept rows).
-//   warps 2..5  epilogue (tcgen05.ld, 32 columns at a time).
+//   warps 2..   epilogue: 4 warps in the weight-gradient GEMMs (64 columns at a time),
+//               8 in the dgrad GEMMs (two per TMEM lane quarter, alternate 16-token
+//               chunks, each half with its own named barrier).
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
 // MOE_DEV_TIMEOUT in the status word, stops issuing work, waits (bounded) for its own
 // copies and MMAs, frees TMEM and returns.
@@ -38,7 +40,9 @@ constexpr int BN = 256;                 // max N per tile
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
 constexpr uint32_t MN_BOX = 64 * BK * 2;    // one 64-element x 64-row MN-major box: 8 KB
-constexpr int NUM_THREADS = 192;
+// Threads: producer warp, MMA warp and 4 epilogue warps (weight gradients) or 8 (dgrad:
+// two per TMEM lane quarter, taking alternate 16-token chunks).
+template <int KIND> constexpr int num_threads() { return KIND == 2 ? 192 : 320; }
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int CHUNK = 32;
 
@@ -187,13 +191,48 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float *v) {
     for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive fp32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Named barriers of the 8 dgrad epilogue warps: id 1 + half for one half (128 threads),
+// id 3 for all 256 (also a vote: returns whether `ok` holds in every thread).
+__device__ __forceinline__ void half_sync(int half) {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory");
+}
+__device__ __forceinline__ void epi8_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
+__device__ __forceinline__ bool epi8_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 3, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void load8_bf16(const __nv_bfloat16 *p, float *f) {
     const uint4 v = *reinterpret_cast<const uint4 *>(p);
     Vec16<__nv_bfloat16>::to_float(v, f);
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(num_threads<KIND>(), 1)
 grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
     constexpr bool WG = KIND == BWD_WGRAD;
     using L = Smem<KIND>;
@@ -228,7 +267,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 4);
+            mbar_init(&tempty[a], WG ? 4 : 8);   // one arrival per epilogue warp
         }
         mbar_init(mma_done, 1);
         *abort_s = 0;
@@ -405,7 +444,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 wt = wtile_at(t, eo, p.m_tiles, p.n_tiles);
             } else {
                 dt = dtile_at(t, mtp, eo, p.ne, p.m_tiles);
-                for (int j = etid; j < dt.nmma; j += 128) {
+                for (int j = etid; j < dt.nmma; j += 256) {
                     const bool tv = j < dt.ntok;
                     const int pr = tv ? p.perm[dt.tok0 + j] : -1;
                     pair_s[j] = pr;
@@ -413,7 +452,9 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 }
             }
             const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_s, p.status);
-            if (!epilogue_all(ok)) break;
+            // tcgen05.ld is warp-collective and the epilogue warps share named barriers:
+            // they leave together on abort
+            if (!(WG ? epilogue_all(ok) : epi8_all(ok))) break;
             fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             if (WG) {
@@ -457,40 +498,46 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[acc]);
             } else {
-                for (int c = 0; c < dt.nmma; c += CHUNK) {
-                    float v[32];
-                    tmem_ld32(taddr + c, v);
-                    if (c + CHUNK >= dt.nmma) {
+                // dgrad: half h of the 8 epilogue warps takes the 16-token chunks
+                // c = 16h, 16h + 32, ...; each half stages its chunk [16 tokens][128
+                // features] in its own half of the staging block
+                const int half = (warp - 2) >> 2;
+                const int htid = etid - half * 128;   // 0..127 inside the half
+                const int f = q * 32 + lane;           // accumulator row = feature of the tile
+                float *sf = stage_f + half * (16 * BM);
+                __nv_bfloat16 *sh = stage_h + half * (16 * BM);
+                for (int c = half * 16; c < dt.nmma; c += 32) {
+                    float v[16];
+                    tmem_ld16(taddr + c, v);
+                    if (c + 32 >= dt.nmma) {   // this warp's last read of the accumulator
                         fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&tempty[acc]);
                     }
                     if (KIND == BWD_DGRAD_DOWN) {
-                        // stage [32 tokens][128 features] fp32, then 8 features per item
-                        const int f = q * 32 + lane;
 #pragma unroll
-                        for (int j = 0; j < CHUNK; ++j) stage_f[j * BM + f] = v[j];
-                        epilogue_sync();
-                        // the four items' gate / up vectors are loaded first, so their
-                        // latencies overlap
+                        for (int j = 0; j < 16; ++j) sf[j * BM + f] = v[j];
+                        half_sync(half);
+                        // 16 tokens x 16 groups of 8 features: two items per thread, their
+                        // gate / up vectors loaded first so the latencies overlap
                         const __nv_bfloat16 *__restrict__ gu = p.gu;
-                        uint4 graw[4], uraw[4];
+                        uint4 graw[2], uraw[2];
 #pragma unroll
-                        for (int s = 0; s < 4; ++s) {
-                            const int item = etid + 128 * s;
+                        for (int s2 = 0; s2 < 2; ++s2) {
+                            const int item = htid + 128 * s2;
                             const int j = item >> 4, f8 = (item & 15) * 8;
                             const int i = dt.f * BM + f8;
-                            graw[s] = uraw[s] = make_uint4(0u, 0u, 0u, 0u);
+                            graw[s2] = uraw[s2] = make_uint4(0u, 0u, 0u, 0u);
                             if (c + j < dt.ntok && i < p.I) {
                                 const size_t r = (size_t)dt.tok0 + c + j;
                                 const int gcol = (i / 64) * 128 + (i % 64);
-                                graw[s] = __ldg(reinterpret_cast<const uint4 *>(gu + r * 2 * p.Ipad + gcol));
-                                uraw[s] = __ldg(reinterpret_cast<const uint4 *>(gu + r * 2 * p.Ipad + gcol + 64));
+                                graw[s2] = __ldg(reinterpret_cast<const uint4 *>(gu + r * 2 * p.Ipad + gcol));
+                                uraw[s2] = __ldg(reinterpret_cast<const uint4 *>(gu + r * 2 * p.Ipad + gcol + 64));
                             }
                         }
 #pragma unroll
-                        for (int s = 0; s < 4; ++s) {
-                            const int item = etid + 128 * s;
+                        for (int s2 = 0; s2 < 2; ++s2) {
+                            const int item = htid + 128 * s2;
                             const int j = item >> 4, f8 = (item & 15) * 8;
                             const int i = dt.f * BM + f8;             // intermediate feature
                             const bool tv = c + j < dt.ntok;
@@ -501,13 +548,12 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                                 uint4 dg_v = make_uint4(0u, 0u, 0u, 0u), du_v = dg_v, wa_v = dg_v;
                                 if (i < p.I) {
                                     const float w = wgt_s[c + j];
-                                    float g[8], u[8], da[8], dg[8], du[8], wa[8];
-                                    Vec16<__nv_bfloat16>::to_float(graw[s], g);
-                                    Vec16<__nv_bfloat16>::to_float(uraw[s], u);
-                                    const float4 d0 = *reinterpret_cast<const float4 *>(stage_f + j * BM + f8);
-                                    const float4 d1 = *reinterpret_cast<const float4 *>(stage_f + j * BM + f8 + 4);
-                                    da[0] = d0.x; da[1] = d0.y; da[2] = d0.z; da[3] = d0.w;
-                                    da[4] = d1.x; da[5] = d1.y; da[6] = d1.z; da[7] = d1.w;
+                                    float g[8], u[8], dg[8], du[8], wa[8];
+                                    Vec16<__nv_bfloat16>::to_float(graw[s2], g);
+                                    Vec16<__nv_bfloat16>::to_float(uraw[s2], u);
+                                    const float4 d0 = *reinterpret_cast<const float4 *>(sf + j * BM + f8);
+                                    const float4 d1 = *reinterpret_cast<const float4 *>(sf + j * BM + f8 + 4);
+                                    const float da[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
                                     for (int x = 0; x < 8; ++x) {
                                         const float sg = __frcp_rn(1.0f + __expf(-g[x]));
@@ -533,25 +579,25 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                             if (tv && (item & 15) == 0)
                                 p.dweight_part[(size_t)dt.f * p.rows + dt.tok0 + c + j] = part;
                         }
-                        epilogue_sync();
+                        half_sync(half);
                     } else {   // BWD_DGRAD_GU: dx of the pair, unweighted, into its slot
-                        const int f = q * 32 + lane;
 #pragma unroll
-                        for (int j = 0; j < CHUNK; ++j) stage_h[j * BM + f] = __float2bfloat16_rn(v[j]);
-                        epilogue_sync();
+                        for (int j = 0; j < 16; ++j) sh[j * BM + f] = __float2bfloat16_rn(v[j]);
+                        half_sync(half);
                         const int col0 = dt.f * BM;
 #pragma unroll
-                        for (int s = 0; s < 4; ++s) {
-                            const int item = etid + 128 * s;
+                        for (int s2 = 0; s2 < 2; ++s2) {
+                            const int item = htid + 128 * s2;
                             const int j = item >> 4, f8 = (item & 15) * 8;
                             const int prj = c + j < dt.ntok ? pair_s[c + j] : -1;
                             if (prj >= 0 && col0 + f8 < p.H)
                                 *reinterpret_cast<uint4 *>(p.dx_slots + (size_t)prj * p.H + col0 + f8) =
-                                    *reinterpret_cast<const uint4 *>(stage_h + j * BM + f8);
+                                    *reinterpret_cast<const uint4 *>(sh + j * BM + f8);
                         }
-                        epilogue_sync();
+                        half_sync(half);
                     }
                 }
+                epi8_sync();   // both halves are done with this tile's pair ids and weights
             }
             if (++acc == 2) {
                 acc = 0;
@@ -594,7 +640,7 @@ cudaError_t launch_bwd(const BwdMaps &maps, BwdParams prm, int64_t max_tiles, cu
         sms_dev[dev] = n > 0 ? n : 148;
     }
     const int grid = (int)std::min<int64_t>(max_tiles, sms_dev[dev]);
-    return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), Smem<KIND>::alloc, s, maps, prm);
+    return launch_pdl(kern, dim3(grid), dim3(num_threads<KIND>()), Smem<KIND>::alloc, s, maps, prm);
 }
 
 cudaError_t token_maps(BwdMaps *m, const void *t, uint64_t rows, uint64_t cols, uint64_t ld) {
