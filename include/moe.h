@@ -114,7 +114,7 @@ enum {
  *                   moe_layer_backward needs (the routing, the send layout and the gate /
  *                   up pre-activations; the workspace grows accordingly), and copies the
  *                   routing arrays it keeps to any moe_diagnostics buffers given.
- *                   bf16 layers only (MOE_ERR_UNSUPPORTED for fp32).
+ *                   Both dtypes (bf16: tensor-core backward; fp32: FFMA backward).
  */
 typedef struct moe_config {
     int64_t num_tokens;
