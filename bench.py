@@ -407,23 +407,25 @@ def _event_ms(stream, fn, steps):
 
 def time_variants(moe, args, shape, inp, packed, dev, stream):
     """The widened rows on the same workload: the forward with slot-major capacity
-    priority, the router load statistics (moe_balance_stats over the logits the forward
-    writes) and the TP split's padded ordered sum (tp = 2)."""
+    priority (beside the token-priority forward timed the same way), the router load
+    statistics (moe_balance_stats over the logits the forward writes) and the TP split's
+    padded ordered sum (tp = 2)."""
     peaks, source = load_peaks()
     bw = peaks["hbm_gbs"]
     s = 2 if shape.dtype == "bf16" else 4
     x, wr, b, wd = inp["x"], inp["w_router"], inp["b_router"], inp["w_down"]
     out = torch.empty(shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
     res = {}
-    cfg = moe.config(shape.N, shape.H, shape.I, shape.E, shape.top_k, shape.ep_size,
-                     shape.capacity_factor, args.mode, shape.dtype,
-                     has_bias=b is not None, capacity_priority="slot")
-    ws = moe.alloc_workspace(cfg, dev)
-    ms = _event_ms(stream, lambda: moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws),
-                   args.steps)
-    res["slot_priority_forward"] = dict(ms=round(ms, 4),
-                                        tokens_per_s=round(shape.N / (ms * 1e-3), 1),
-                                        gpu_launches_per_step=7)
+    for prio in ("token", "slot"):   # timed the same way, back to back
+        cfg = moe.config(shape.N, shape.H, shape.I, shape.E, shape.top_k, shape.ep_size,
+                         shape.capacity_factor, args.mode, shape.dtype,
+                         has_bias=b is not None, capacity_priority=prio)
+        ws = moe.alloc_workspace(cfg, dev)
+        ms = _event_ms(stream, lambda: moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws),
+                       args.steps)
+        res[f"{prio}_priority_forward"] = dict(ms=round(ms, 4),
+                                               tokens_per_s=round(shape.N / (ms * 1e-3), 1),
+                                               gpu_launches_per_step=6 if prio == "token" else 7)
     logits = torch.empty(shape.N, shape.E, device=dev)
     routed = torch.empty(shape.E, dtype=torch.int32, device=dev)
     moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws,

@@ -37,9 +37,11 @@ SHAPES = [
 ]
 
 
-def _run(shape, inp, dout, mode="dispatch", capacity_priority="token"):
+def _run(shape, inp, dout, mode="dispatch", capacity_priority="token", group_limit=0,
+         selection_bias=None):
     dev = "cuda"
-    cfg = make_cfg(shape, mode, capacity_priority=capacity_priority)
+    cfg = make_cfg(shape, mode, capacity_priority=capacity_priority, group_limit=group_limit,
+                   selection_bias=selection_bias)
     cfg.training = 1
     x = inp["x"].to(dev).contiguous()
     wr = inp["w_router"].to(dev).contiguous()
@@ -68,11 +70,12 @@ def _dout(shape, seed):
     return torch.randn((shape.N, shape.H), generator=gen).to(shape.torch_dtype)
 
 
-def _oracle(shape, inp, dout, capacity_priority="token"):
+def _oracle(shape, inp, dout, capacity_priority="token", group_limit=None, selection_bias=None):
     b = inp["b_router"]
     return oracle.layer_backward(f64(inp["x"]), f64(inp["w_router"]), None if b is None else f64(b),
                                  f64(inp["w_gate"]), f64(inp["w_up"]), f64(inp["w_down"]),
                                  shape.top_k, shape.ep_size, f64(dout), shape.capacity_factor,
+                                 selection_bias=selection_bias, group_limit=group_limit,
                                  capacity_priority=capacity_priority)
 
 
@@ -95,6 +98,22 @@ def test_backward_with_slot_priority_and_mask_mode():
     dout = _dout(shape, 54)
     _, g = _run(shape, inp, dout, mode="mask_sum", capacity_priority="slot")
     _compare(g, _oracle(shape, inp, dout, capacity_priority="slot"))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_backward_with_selection_bias_and_group_limit(dtype):
+    """DeepSeek-V3-style routing (a selection-only bias, at most 2 partitions per token):
+    the routing weights stay the softmax of the chosen experts' raw logits, so the same
+    chain rule applies; the selection bias gets no gradient."""
+    shape = S("b_variant", N=640, H=128, I=96, E=32, top_k=4, ep_size=8, capacity_factor=1.0,
+              dtype=dtype)
+    inp = workloads.layer_inputs(shape, seed=60, variant="exact")
+    rng = np.random.default_rng(60)
+    beta = np.round(rng.uniform(-0.05, 0.05, shape.E) * 1024) / 1024
+    sel = torch.as_tensor(beta, dtype=torch.float32, device="cuda")
+    dout = _dout(shape, 61)
+    _, g = _run(shape, inp, dout, group_limit=2, selection_bias=sel)
+    _compare(g, _oracle(shape, inp, dout, group_limit=2, selection_bias=beta), tol_for(shape))
 
 
 def test_backward_is_deterministic():
