@@ -8,7 +8,7 @@ binding of that library (see binding.py) plus its build script (build.py).
 from .binding import (  # noqa: F401
     MOE_DEV_BAD_EXPERT_ID, MOE_DEV_TIMEOUT, MOE_DTYPE_BF16, MOE_DTYPE_FP32, MOE_MODE_DISPATCH,
     MOE_MODE_MASK_SUM, MoeConfig, MoeDiagnostics, MoeError, alloc_workspace, config, lib,
-    MOE_PRIORITY_SLOT, MOE_PRIORITY_TOKEN, moe_balance_stats, moe_combine, moe_dispatch,
+    MOE_PRIORITY_SLOT, MOE_PRIORITY_TOKEN, moe_balance_stats, moe_check_wait_timeout, moe_combine, moe_dispatch,
     moe_dispatch_noalloc, moe_expert_ffn, moe_layer_backward, moe_layer_forward, moe_pack_weights,
     moe_packed_gate_up_size, moe_read_device_status, moe_route, moe_tp_reduce, moe_tp_slice,
     moe_update_selection_bias, moe_workspace_size,

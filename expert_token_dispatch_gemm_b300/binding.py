@@ -86,6 +86,7 @@ def _load():
         "moe_tp_slice": (ctypes.c_int, [ctypes.c_int64, I32, I32, ctypes.POINTER(ctypes.c_int64),
                                         ctypes.POINTER(ctypes.c_int64)]),
         "moe_tp_reduce": (ctypes.c_int, [cfgp, I32, P, P, P]),
+        "moe_check_wait_timeout": (ctypes.c_int, [cfgp, P, S, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -309,3 +310,10 @@ def moe_layer_backward(cfg, x, w_router, w_gate_up_packed, w_down, dout, dx, dw_
         _ptr(db_router, "db_router", f32), _ptr(dw_gate, "dw_gate", dt), _ptr(dw_up, "dw_up", dt),
         _ptr(dw_down, "dw_down", dt), _ptr(workspace, "workspace"), workspace.numel(), _stream()),
         "moe_layer_backward")
+
+
+def moe_check_wait_timeout(cfg, workspace):
+    """Enqueues the bounded-wait check (moe.h); read the result with
+    moe_read_device_status."""
+    _check(lib.moe_check_wait_timeout(ctypes.byref(cfg), _ptr(workspace, "workspace"),
+                                      workspace.numel(), _stream()), "moe_check_wait_timeout")

@@ -316,6 +316,10 @@ moe_status_t noalloc_scratch(int32_t **out) {
 }  // namespace
 }  // namespace moe
 
+namespace moe {
+cudaError_t launch_wait_timeout_check(int32_t *status, cudaStream_t s);
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
@@ -732,6 +736,19 @@ moe_status_t moe_layer_backward(const moe_config *cfg, const void *x, const void
     MOE_CUDA(launch_router_wgrad(d, w.eoff_all, w.perm_all, w.dl, x, w.rw_partial, w.rw_partial_db,
                                  dw_router, db_router, s),
              "router wgrad kernels");
+    return MOE_OK;
+}
+
+moe_status_t moe_check_wait_timeout(const moe_config *cfg, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+    LayerDims d;
+    moe_status_t st = check_config(cfg, &d);
+    if (st != MOE_OK) return st;
+    Workspace w;
+    st = check_workspace(d, cfg->mode, workspace, workspace_bytes, &w);
+    if (st != MOE_OK) return st;
+    g_last_error.clear();
+    MOE_CUDA(launch_wait_timeout_check(w.status, (cudaStream_t)stream), "wait check kernel");
     return MOE_OK;
 }
 

@@ -395,6 +395,17 @@ moe_status_t moe_tp_slice(int64_t num_tokens, int32_t tp_size, int32_t tp_rank, 
 moe_status_t moe_tp_reduce(const moe_config *cfg, int32_t tp_size, const void *padded, void *out,
                            void *stream);
 
+/*
+ * Check of the device-side failure path (not part of the layer): enqueues one warp that
+ * waits, with the bounded mbarrier wait every tensor-core kernel of the library uses, on
+ * a barrier that nothing arrives at. After the wait limit (about 2 s) it records
+ * MOE_DEV_TIMEOUT in the workspace's status word and returns; no fault or trap is
+ * involved and the context stays usable. moe_read_device_status then reports
+ * MOE_ERR_TIMEOUT (and clears the word when asked to).
+ */
+moe_status_t moe_check_wait_timeout(const moe_config *cfg, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
