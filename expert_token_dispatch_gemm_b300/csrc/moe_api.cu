@@ -27,7 +27,10 @@ moe_status_t fail(moe_status_t s, const char *fmt, ...) {
     return s;
 }
 
+// The error is reported to the caller here; the runtime's last-error state is cleared
+// (for a non-sticky error) so that it is not reported again by a later launch check.
 moe_status_t cuda_fail(cudaError_t e, const char *what) {
+    (void)cudaGetLastError();
     return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 

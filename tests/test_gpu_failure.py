@@ -7,8 +7,8 @@
   matches the oracle.
 * A CUDA error reaches the caller as MOE_ERR_CUDA: moe_read_device_status synchronises
   its stream, which is illegal while the stream is being captured into a graph; the
-  call returns MOE_ERR_CUDA with a reason, nothing runs on the GPU, and the context
-  stays usable.
+  call returns MOE_ERR_CUDA with a reason, nothing runs on the GPU, and the next calls
+  succeed (the library clears the reported error, so no later launch check sees it).
 """
 import ctypes
 
@@ -54,18 +54,22 @@ def test_cuda_error_is_reported_as_moe_err_cuda():
     err, stream = cudart.cudaStreamCreate()
     assert err == cudart.cudaError_t.cudaSuccess
     try:
+        # relaxed mode: the capture restricts nothing outside the captured stream
         err, = cudart.cudaStreamBeginCapture(
-            stream, cudart.cudaStreamCaptureMode.cudaStreamCaptureModeThreadLocal)
+            stream, cudart.cudaStreamCaptureMode.cudaStreamCaptureModeRelaxed)
         assert err == cudart.cudaError_t.cudaSuccess
         flags = ctypes.c_int32(0)
         st = moe.lib.moe_read_device_status(ctypes.byref(cfg), ctypes.c_void_p(ws.data_ptr()),
                                             ws.numel(), ctypes.byref(flags), 0,
                                             ctypes.c_void_p(int(stream)))
         reason = moe.lib.moe_last_error().decode()
-        cudart.cudaStreamEndCapture(stream)        # invalidated capture: no graph
+        err, _graph = cudart.cudaStreamEndCapture(stream)   # invalidated: no graph
+        assert err != cudart.cudaError_t.cudaSuccess
+        err, capturing = cudart.cudaStreamIsCapturing(stream)
+        assert err == cudart.cudaError_t.cudaSuccess
+        assert capturing == cudart.cudaStreamCaptureStatus.cudaStreamCaptureStatusNone
     finally:
         cudart.cudaStreamDestroy(stream)
-        cudart.cudaGetLastError()                  # leave no stale error for later launches
     assert st == moe.binding.MOE_ERR_CUDA, reason
     assert reason
     _layer_matches_oracle()
