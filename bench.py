@@ -323,6 +323,17 @@ def run_reference(args, shape):
     print(json.dumps(line), flush=True)
 
 
+def load_summary(shape, routed, kept):
+    """The routing example's load quantities on the bench batch: per expert and per
+    partition (expert // (E / ep_size)) pairs before capacity, and the dropped pairs."""
+    parts = routed.reshape(shape.ep_size, -1).sum(axis=1)
+    return dict(expert_max=int(routed.max()), expert_min=int(routed.min()),
+                expert_mean=round(float(routed.mean()), 2),
+                partition_max=int(parts.max()), partition_min=int(parts.min()),
+                partition_mean=round(float(parts.mean()), 2),
+                routed_pairs=int(routed.sum()), dropped_pairs=int(routed.sum() - kept.sum()))
+
+
 BACKWARD_LAUNCHES = 11   # permute, 4 GEMMs, logit grads, dx combine, histogram, scan, 2 router
 
 
@@ -505,9 +516,12 @@ def main():
 
     # one run with diagnostics for the kept counts (algorithmic work of each stage)
     counts_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
-    moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws, dict(counts=counts_t))
+    routed_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
+    moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws,
+                          dict(counts=counts_t, routed_counts=routed_t))
     torch.cuda.synchronize()
     counts = counts_t.cpu().numpy()
+    load = load_summary(shape, routed_t.cpu().numpy(), counts)
     work = stage_work(shape, counts)
 
     nst = moe.binding.MOE_NUM_STAGES
@@ -628,7 +642,7 @@ def main():
                                 parallelism=f"replicas x{world} (one layer per GPU)"),
                     roofline=roof, stages=per_stage, cpu_baseline=cpu, e2e=e2e,
                     gpu_launches=launches_per_step * args.steps, clocks=clk.summary(),
-                    kept_pairs=int(counts.sum()), backward=backward, variants=variants,
+                    kept_pairs=int(counts.sum()), load=load, backward=backward, variants=variants,
                     impl="b300")
         print(json.dumps(line), flush=True)
     if dist is not None:
