@@ -184,27 +184,41 @@ scan_assign_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ 
     __syncwarp();
     const SegWalk<SLOT> walk(seg, N, k);
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int ic = 0; ic < walk.count; ic += 32) {
-        const bool live = ic + lane < walk.count;
-        const int64_t p = live ? walk.pair(ic + lane) : 0;
-        int e = live ? idx[p] : -1;
-        const bool valid = live && e >= 0 && e < E;
-        if (live && !valid) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
-        if (!valid) e = -1 - lane;   // unique key: never matches another lane
-        const unsigned same = __match_any_sync(0xffffffffu, e);
-        int rank = 0;
-        if (valid) rank = base[e] + __popc(same & lt_mask);
-        __syncwarp();
-        // the lowest lane of each group advances that expert's running base
-        if (valid && (same & lt_mask) == 0) base[e] += __popc(same);
-        __syncwarp();
-        if (live) {
-            int slot = -1;
-            if (valid && rank < capacity) {
-                slot = off_s[e] + rank;
-                perm[slot] = (int32_t)p;
+    // the expert ids of 8 rounds of 32 pairs are loaded first, so the loads' latencies
+    // overlap instead of adding up round after round
+    constexpr int PF = 8;
+    for (int ic0 = 0; ic0 < walk.count; ic0 += 32 * PF) {
+        int ev[PF];
+#pragma unroll
+        for (int u = 0; u < PF; ++u) {
+            const int ic = ic0 + 32 * u;
+            ev[u] = ic + lane < walk.count ? idx[walk.pair(ic + lane)] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < PF; ++u) {
+            const int ic = ic0 + 32 * u;
+            if (ic >= walk.count) break;   // warp-uniform
+            const bool live = ic + lane < walk.count;
+            const int64_t p = live ? walk.pair(ic + lane) : 0;
+            int e = ev[u];
+            const bool valid = live && e >= 0 && e < E;
+            if (live && !valid) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+            if (!valid) e = -1 - lane;   // unique key: never matches another lane
+            const unsigned same = __match_any_sync(0xffffffffu, e);
+            int rank = 0;
+            if (valid) rank = base[e] + __popc(same & lt_mask);
+            __syncwarp();
+            // the lowest lane of each group advances that expert's running base
+            if (valid && (same & lt_mask) == 0) base[e] += __popc(same);
+            __syncwarp();
+            if (live) {
+                int slot = -1;
+                if (valid && rank < capacity) {
+                    slot = off_s[e] + rank;
+                    perm[slot] = (int32_t)p;
+                }
+                slot_pos[p] = slot;
             }
-            slot_pos[p] = slot;
         }
     }
 }
