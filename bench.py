@@ -420,23 +420,38 @@ def time_variants(moe, args, shape, inp, packed, dev, stream):
     """The widened rows on the same workload: the forward with slot-major capacity
     priority (beside the token-priority forward timed the same way), the router load
     statistics (moe_balance_stats over the logits the forward writes) and the TP split's
-    padded ordered sum (tp = 2)."""
+    padded ordered sum (tp = 2). Timed before the backward."""
     peaks, source = load_peaks()
     bw = peaks["hbm_gbs"]
     s = 2 if shape.dtype == "bf16" else 4
     x, wr, b, wd = inp["x"], inp["w_router"], inp["b_router"], inp["w_down"]
     out = torch.empty(shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
     res = {}
-    for prio in ("token", "slot"):   # timed the same way, back to back
-        cfg = moe.config(shape.N, shape.H, shape.I, shape.E, shape.top_k, shape.ep_size,
-                         shape.capacity_factor, args.mode, shape.dtype,
-                         has_bias=b is not None, capacity_priority=prio)
-        ws = moe.alloc_workspace(cfg, dev)
-        ms = _event_ms(stream, lambda: moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws),
-                       args.steps)
+    # token and slot priority alternate step by step, each step between its own events,
+    # so both see the same clock and power state
+    cfgs, wss = {}, {}
+    for prio in ("token", "slot"):
+        cfgs[prio] = moe.config(shape.N, shape.H, shape.I, shape.E, shape.top_k, shape.ep_size,
+                                shape.capacity_factor, args.mode, shape.dtype,
+                                has_bias=b is not None, capacity_priority=prio)
+        wss[prio] = moe.alloc_workspace(cfgs[prio], dev)
+        moe.moe_layer_forward(cfgs[prio], x, wr, b, packed, wd, out, wss[prio])
+    evs = {p: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] for p in cfgs}
+    torch.cuda.synchronize()
+    torch.cuda._sleep(1_000_000)
+    for i in range(args.steps):
+        for prio in ("token", "slot"):
+            evs[prio][i][0].record(stream)
+            moe.moe_layer_forward(cfgs[prio], x, wr, b, packed, wd, out, wss[prio])
+            evs[prio][i][1].record(stream)
+    torch.cuda.synchronize()
+    for prio in ("token", "slot"):
+        ms = float(np.mean([a.elapsed_time(z) for a, z in evs[prio]]))
         res[f"{prio}_priority_forward"] = dict(ms=round(ms, 4),
                                                tokens_per_s=round(shape.N / (ms * 1e-3), 1),
                                                gpu_launches_per_step=6 if prio == "token" else 7)
+    cfg, ws = cfgs["slot"], wss["slot"]
     logits = torch.empty(shape.N, shape.E, device=dev)
     routed = torch.empty(shape.E, dtype=torch.int32, device=dev)
     moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws,
@@ -563,12 +578,12 @@ def main():
     ms_step = slowest_rank_ms(ms_total / args.steps, dist, dev)
     value = job_tokens_per_s(shape.N, world, ms_step)
 
+    variants = None
+    if not args.no_variants:   # before the backward's long high-power stretch
+        variants = time_variants(moe, args, shape, inp, packed, dev, stream)
     backward = None
     if not args.no_backward:
         backward = time_backward(moe, args, shape, inp, packed, dist, dev, stream)
-    variants = None
-    if not args.no_variants:
-        variants = time_variants(moe, args, shape, inp, packed, dev, stream)
 
     # end to end through the C ABI: every step copies its input from pinned host memory
     # to the device and reads its output back. Copies run on their own streams, double
