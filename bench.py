@@ -407,7 +407,9 @@ def _event_ms(stream, fn, steps):
     fn()
     torch.cuda.synchronize()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda._sleep(1_000_000)
+    # a longer device-side delay before `start`: the host enqueues all steps of these
+    # few-microsecond kernels ahead of the GPU
+    torch.cuda._sleep(20_000_000)
     s0.record(stream)
     for _ in range(steps):
         fn()
