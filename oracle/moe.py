@@ -23,7 +23,12 @@ Readings taken where the pages are silent (each listed in the design notes):
 
 Parity status: routing and load counts are pinned by the worked example's printed loads;
 dispatch, expert math and combine are pinned by an independent dense brute force, a
-library SwiGLU-MLP special case and a library softmax special case (see tests/).
+library SwiGLU-MLP special case and a library softmax special case. The widened steps:
+layer_backward / silu_grad by finite differences and torch autograd of a dense layer,
+token_input_grads / expert_weight_grads against layer_backward, slot-major priority by a
+loop and a cumulative-sum formulation, balance_stats by closed forms and torch.softmax,
+tp_slices / tp_row_split_forward by their cover rule and the brute force (see tests/).
+No function is left unpinned.
 """
 from __future__ import annotations
 
