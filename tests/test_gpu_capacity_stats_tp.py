@@ -174,3 +174,33 @@ def test_tp_row_split_matches_oracle(shape, mode, tp):
     for s in range(tp):
         lo, hi = moe.moe_tp_slice(shape.N, tp, s)
         assert torch.equal(out[lo:hi], padded[s, lo:hi])
+
+
+@pytest.mark.parametrize("shape", [workloads.SKEWED_CAP, workloads.GPTOSS], ids=lambda s: s.name)
+def test_slot_priority_at_full_size(shape):
+    """Slot-major priority on the full skewed + capacity workload (where the keep set
+    depends on it) and the gpt-oss workload, in the bench's launch configuration:
+    routing and the whole dispatch layout bit-exact against the oracle's full-batch
+    layout, outputs on sampled tokens (tokens with dropped pairs included)."""
+    from moe_gpu_harness import full_size_reference_routing, sampled_token_check
+    torch.manual_seed(0)
+    inp = workloads.layer_inputs(shape, seed=0, variant="exact", device="cuda")
+    layer = Layer(shape, inp, capacity_priority="slot")
+    del inp
+    out, diag = layer.forward()
+    ref = full_size_reference_routing(layer)
+    lay = oracle.dispatch_layout(ref["topk_idx"], shape.E, shape.ep_size, ref["capacity"],
+                                 priority="slot")
+    ref = dict(ref, **lay)
+    assert_routing_and_layout_exact(diag, ref, shape)
+    rng = np.random.default_rng(2)
+    sample = np.sort(rng.choice(shape.N, 32, replace=False))
+    if ref["capacity"] is not None:
+        sp = ref["slot_pos"].reshape(shape.N, shape.top_k)
+        dropped = np.nonzero((sp < 0).any(axis=1))[0]
+        assert dropped.size > 0
+        sample = np.unique(np.concatenate([sample, dropped[:8], dropped[-8:]]))
+        tok = oracle.dispatch_layout(ref["topk_idx"], shape.E, shape.ep_size, ref["capacity"])
+        assert not np.array_equal(tok["slot_pos"] >= 0, lay["slot_pos"] >= 0)
+    sampled_token_check(layer, diag, out, ref, sample, tol_for(shape))
+    assert layer.device_status() == 0
