@@ -1,0 +1,81 @@
+"""The benchmark's host arithmetic, on CPU: algorithmic work per stage (closed forms of
+the SURVEY-style byte and flop counts on a hand-checked shape), the roofline's choice of
+bound and fraction, the traffic record's guard on the GEMM sources, whole-job
+throughput, and the load summary."""
+import json
+import math
+
+import numpy as np
+import pytest
+
+import bench
+import workloads
+
+
+def test_stage_work_closed_forms():
+    shape = workloads.LayerShape("w", N=128, H=64, I=32, E=4, top_k=2, ep_size=2)
+    counts = np.array([100, 0, 80, 76])                 # 256 kept pairs, 3 experts touched
+    w = bench.stage_work(shape, counts)
+    s, N, H, I, E, k, A = 2, 128, 64, 32, 4, 2, 256
+    assert w["permute"]["bytes"] == N * H * s + A * H * s + N * k * 4
+    assert w["gate_up"]["bytes"] == 3 * 2 * I * H * s + A * H * s + A * I * s
+    assert w["gate_up"]["flops"] == 4 * A * H * I
+    assert w["down"]["flops"] == 2 * A * H * I
+    assert w["down"]["bytes"] == 3 * H * I * s + A * I * s + A * H * s + 8 * A
+    assert w["combine"]["bytes"] == A * H * s + N * H * s + N * k * 4
+    assert w["route"]["flops"] == 2 * N * H * E
+    assert w["route"]["bytes"] == N * H * s + E * H * s + N * k * 8 + math.ceil(N / 64) * E * 4
+
+
+PEAKS = {"hbm_gbs": 6000.0, "bf16_tflops": 1800.0, "sm_max_mhz": 2000.0}
+
+
+def test_roofline_picks_the_binding_resource():
+    # memory-bound: 6 GB in 1 ms at 6 TB/s is exactly the peak
+    r = bench.roofline_entry(dict(bytes=6e9, flops=1e12), 1.0, PEAKS, "m", "bf16")
+    assert r["bound"] == "hbm" and r["frac"] == pytest.approx(1.0)
+    assert r["tensor_frac"] == pytest.approx(1e12 / 1e-3 / 1e12 / 1800, abs=1e-4)   # rounded
+    # compute-bound: 1.8 PFLOP/s worth of flops
+    r = bench.roofline_entry(dict(bytes=1e6, flops=0.9e12), 1.0, PEAKS, "m", "bf16")
+    assert r["bound"] == "tensor" and r["frac"] == pytest.approx(0.5)
+    # fp32: FFMA peak 148 x 128 x 2 x 2 GHz
+    alu = 148 * 128 * 2 * 2000e6 / 1e12
+    assert bench.fp32_alu_tflops(PEAKS) == pytest.approx(alu)
+    r = bench.roofline_entry(dict(bytes=1e6, flops=alu * 1e9 / 2), 1.0, PEAKS, "m", "fp32")
+    assert r["bound"] == "alu" and r["frac"] == pytest.approx(0.5)
+
+
+def test_job_throughput_is_weak_scaling():
+    assert bench.job_tokens_per_s(8192, 4, 2.0) == pytest.approx(4 * 8192 / 2e-3)
+    assert bench.slowest_rank_ms(3.5, None, None) == 3.5
+
+
+def test_traffic_record_holds_only_for_its_sources(tmp_path, monkeypatch):
+    rec = dict(sources_sha256=bench.gemm_sources_sha256(),
+               per_launch_bytes=dict(gate_up=dict(dram_read=10, dram_write=5),
+                                     down=dict(dram_read=7, dram_write=1)))
+    (tmp_path / "profiles").mkdir()
+    path = tmp_path / "profiles" / "grouped_gemm_pair_traffic_wl.json"
+    path.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "gemm_sources_sha256", lambda: rec["sources_sha256"])
+    assert bench.measured_traffic("wl", "gate_up") == 15
+    assert bench.measured_traffic("wl", "down") == 8
+    assert bench.measured_traffic("wl", "route") is None
+    assert bench.measured_traffic("other", "gate_up") is None
+    monkeypatch.setattr(bench, "gemm_sources_sha256", lambda: "changed")
+    assert bench.measured_traffic("wl", "gate_up") is None
+
+
+def test_committed_traffic_record_matches_the_current_sources():
+    assert bench.measured_traffic(workloads.GPTOSS.name, "gate_up") is not None
+
+
+def test_load_summary():
+    shape = workloads.LayerShape("l", N=10, H=8, I=8, E=4, top_k=2, ep_size=2)
+    routed = np.array([7, 3, 6, 4])
+    kept = np.array([5, 3, 5, 4])
+    s = bench.load_summary(shape, routed, kept)
+    assert (s["expert_max"], s["expert_min"], s["expert_mean"]) == (7, 3, 5.0)
+    assert (s["partition_max"], s["partition_min"]) == (10, 10)
+    assert s["routed_pairs"] == 20 and s["dropped_pairs"] == 3
