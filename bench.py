@@ -220,10 +220,13 @@ def blas_threads():
         return 1
 
 
-def time_oracle(shape, x, w_router, b_router, expert_fn, n_sample_experts, seed=0):
+def time_oracle(shape, x, w_router, b_router, expert_fn, n_sample_experts, seed=0,
+                ffn_budget_s=None):
     """Times the fp64 oracle on the whole batch for routing, dispatch and combine, and on
-    the full segments of `n_sample_experts` experts for the SwiGLU experts; the expert
-    time is extrapolated to every kept pair. Returns (seconds for the batch, detail)."""
+    the full segments of up to `n_sample_experts` experts (in a seeded random order; with
+    `ffn_budget_s`, until that much expert time is spent) for the SwiGLU experts; the
+    expert time is extrapolated to every kept pair (exact when every expert ran).
+    Returns (seconds for the batch, detail)."""
     import oracle
     N, k, E = shape.N, shape.top_k, shape.E
     t0 = time.perf_counter()
@@ -238,7 +241,11 @@ def time_oracle(shape, x, w_router, b_router, expert_fn, n_sample_experts, seed=
     pick = rng.choice(busy, size=min(n_sample_experts, busy.size), replace=False)
     rows = 0
     t_ffn = 0.0
+    done = 0
     for e in pick:
+        if ffn_budget_s is not None and done > 0 and t_ffn >= ffn_budget_s:
+            break
+        done += 1
         wg, wu, wd = expert_fn(int(e))
         a, b = int(lay["expert_offsets"][e]), int(lay["expert_offsets"][e + 1])
         ts = time.perf_counter()
@@ -254,7 +261,7 @@ def time_oracle(shape, x, w_router, b_router, expert_fn, n_sample_experts, seed=
     total = (t1 - t0) + (t2 - t1) + ffn_total + (t4 - t3)
     detail = dict(route_s=t1 - t0, dispatch_s=t2 - t1, ffn_sample_s=t_ffn,
                   ffn_extrapolated_s=ffn_total, combine_s=t4 - t3, sample_rows=rows,
-                  kept_pairs=kept, sampled_experts=len(pick))
+                  kept_pairs=kept, sampled_experts=done, busy_experts=int(busy.size))
     return total, detail
 
 
@@ -263,21 +270,25 @@ def host_inputs_for_oracle(shape, inp):
     return f(inp["x"]), f(inp["w_router"]), f(inp["b_router"])
 
 
-def cpu_baseline_from_device(shape, inp, n_sample_experts=4):
+def cpu_baseline_from_device(shape, inp, ffn_budget_s=10.0):
+    """The oracle on the bench workload: route, dispatch and combine on every token, and
+    the SwiGLU experts one by one until about `ffn_budget_s` seconds of expert work are
+    spent (every expert when they fit: then nothing is extrapolated)."""
     x, wr, b = host_inputs_for_oracle(shape, inp)
 
     def expert_fn(e):
         return tuple(inp[k][e].detach().to("cpu", torch.float64).numpy()
                      for k in ("w_gate", "w_up", "w_down"))
 
-    total, detail = time_oracle(shape, x, wr, b, expert_fn, n_sample_experts)
+    total, detail = time_oracle(shape, x, wr, b, expert_fn, shape.E, ffn_budget_s=ffn_budget_s)
+    whole = detail["sampled_experts"] == detail["busy_experts"]
+    ffn = ("SwiGLU experts on every kept pair (the whole layer, nothing extrapolated)" if whole
+           else f"SwiGLU experts timed on the full segments of {detail['sampled_experts']} of "
+                f"{shape.E} experts ({detail['sample_rows']} of {detail['kept_pairs']} kept "
+                f"pairs, about {ffn_budget_s:.0f} s), extrapolated linearly in kept pairs")
     return dict(value=round(shape.N / total, 2), unit="tokens/s", cores=blas_threads(),
                 kind="oracle",
-                sample=(f"fp64 oracle: route, dispatch and combine on all {shape.N} tokens; "
-                        f"SwiGLU experts timed on the full segments of "
-                        f"{detail['sampled_experts']} of {shape.E} experts "
-                        f"({detail['sample_rows']} of {detail['kept_pairs']} kept pairs), "
-                        f"extrapolated linearly in kept pairs"),
+                sample=f"fp64 oracle: route, dispatch and combine on all {shape.N} tokens; {ffn}",
                 seconds=round(total, 3), detail={k: (round(v, 4) if isinstance(v, float) else v)
                                                  for k, v in detail.items()})
 
