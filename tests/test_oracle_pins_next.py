@@ -330,3 +330,39 @@ def test_sampled_backward_functions_equal_the_batch_backward():
         assert rel_err(dg, g["dw_gate"][e]) < 1e-12
         assert rel_err(du, g["dw_up"][e]) < 1e-12
         assert rel_err(dd, g["dw_down"][e]) < 1e-12
+
+
+@pytest.mark.parametrize("priority", ["token", "slot"])
+def test_backward_under_routing_variants_matches_finite_differences(priority):
+    """The backward paths the GPU tests compare against: a selection-only bias, a group
+    limit and both capacity priorities. The selection (piecewise constant) is unchanged
+    by the small perturbations, so central differences of the forward pin every
+    gradient."""
+    N, H, I, E, k, P, cf = 12, 5, 4, 6, 2, 3, 0.7
+    x, wr, b, wg, wu, wd = tiny_inputs(81, N, H, I, E)
+    wr = wr * 4.0
+    beta = np.random.default_rng(82).uniform(-0.3, 0.3, E)
+    dout = np.random.default_rng(83).standard_normal((N, H))
+    g = oracle.layer_backward(x, wr, b, wg, wu, wd, k, P, dout, cf, selection_bias=beta,
+                              group_limit=2, capacity_priority=priority)
+
+    def loss(**kw):
+        a = dict(x=x, wr=wr, b=b, wg=wg, wu=wu, wd=wd)
+        a.update(kw)
+        return float(np.sum(oracle.layer_forward(a["x"], a["wr"], a["b"], a["wg"], a["wu"],
+                                                 a["wd"], k, P, cf, "dispatch", beta, 2,
+                                                 priority)["out"] * dout))
+
+    eps = 1e-6
+    for name, arr, key in [("x", x, "dx"), ("wr", wr, "dw_router"), ("b", b, "db_router"),
+                           ("wg", wg, "dw_gate"), ("wd", wd, "dw_down")]:
+        num = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            hi, lo = arr.copy(), arr.copy()
+            hi[i] += eps
+            lo[i] -= eps
+            num[i] = (loss(**{name: hi}) - loss(**{name: lo})) / (2 * eps)
+        assert np.max(np.abs(num - g[key])) < 1e-6 * max(np.max(np.abs(num)), 1e-3), name
+    # and the routing really is a variant: the bias or the limit changed the selection
+    plain = oracle.layer_forward(x, wr, b, wg, wu, wd, k, P, cf)
+    assert not np.array_equal(plain["topk_idx"], g["forward"]["topk_idx"])
