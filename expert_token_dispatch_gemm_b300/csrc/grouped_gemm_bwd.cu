@@ -72,26 +72,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
         : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// TMA tile load whose data and completion are replicated to the same shared-memory
-// offsets in the CTAs of `mask` (this GPU's own memory; a cluster of two CTAs).
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                               int x, int y, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-        : "memory");
-}
-// Arrives, once this thread's MMAs so far complete, on the mbarrier at the same offset in
-// both CTAs of the cluster.
-__device__ __forceinline__ void commit_both(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"((uint16_t)3)
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_store_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
@@ -299,7 +279,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     } else if (warp == 2 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], WG ? 2 : 1);   // weight gradients: both CTAs' MMAs
+            mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -320,22 +300,13 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     }
     fence_before();
     __syncthreads();
-    if (WG) cluster_sync_all();   // both CTAs' barriers exist before any remote signal
     fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // Weight gradients run as clusters of two CTAs: pair tile t covers M tiles 2 mp and
-    // 2 mp + 1 of one (expert, N tile); each CTA loads its own A tile and half of the
-    // shared B tile, multicast to both. The dgrad GEMMs run one CTA per tile.
-    const uint32_t cta = WG ? cluster_ctarank() : 0u;
-    const int mp = (p.m_tiles + 1) / 2;
-    const int tile0 = WG ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int tstride = WG ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-    const int total = WG ? p.ne * mp * p.n_tiles : mtp[p.ne] * p.m_tiles;
-    auto wtile = [&](int t) {
-        WTile w = wtile_at(t, eo, mp, p.n_tiles);
-        w.mt = 2 * w.mt + (int)cta;
-        return w;
-    };
+    // One CTA per tile, persistent over the tiles t = blockIdx.x + j * gridDim.x.
+    const int tile0 = (int)blockIdx.x;
+    const int tstride = (int)gridDim.x;
+    const int total = WG ? p.ne * p.m_tiles * p.n_tiles : mtp[p.ne] * p.m_tiles;
+    auto wtile = [&](int t) { return wtile_at(t, eo, p.m_tiles, p.n_tiles); };
 
     if (warp == 0) {
         if (lane == 0) {   // ------------------------------------------ TMA producer
@@ -364,9 +335,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     tx = A_BYTES + (uint32_t)(32 << bsel) * BK * 2;
                 }
                 for (int kb = 0; kb < nkb; ++kb) {
-                    const bool freed = WG ? mbar_wait<true>(&empty[stage], phase ^ 1u, abort_s, p.status)
-                                          : mbar_wait(&empty[stage], phase ^ 1u, abort_s, p.status);
-                    if (!freed) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_s, p.status)) {
                         ok = false;
                         break;
                     }
@@ -376,13 +345,11 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     const uint32_t b_dst = smem_u32(smem + L::b_off + stage * B_BYTES);
                     tma_load_2d(a_dst, &maps.a, fb, a_x, a_y0 + kb * BK);
                     tma_load_2d(a_dst + MN_BOX, &maps.a, fb, a_x + 64, a_y0 + kb * BK);
-                    if (WG) {   // this CTA's half of B, into both CTAs
+                    if (WG) {   // the B tile: four 64-column MN-major boxes
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int q = 2 * (int)cta + h;
-                            tma_load_2d_mc(b_dst + q * MN_BOX, &maps.b[0], fb, b_x + 64 * q,
-                                           b_y0 + kb * BK, (uint16_t)3);
-                        }
+                        for (int q = 0; q < 4; ++q)
+                            tma_load_2d(b_dst + q * MN_BOX, &maps.b[0], fb, b_x + 64 * q,
+                                        b_y0 + kb * BK);
                     } else {
                         tma_load_2d(b_dst, &maps.b[bsel], fb, kb * BK, b_y0);
                     }
@@ -397,10 +364,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             for (int s = 0; s < STAGES; ++s)
                 if ((armed >> s) & 1u) {
                     volatile int no_abort = 0;
-                    if (WG)
-                        mbar_wait<true>(&full[s], (armed_parity >> s) & 1u, &no_abort, p.status);
-                    else
-                        mbar_wait(&full[s], (armed_parity >> s) & 1u, &no_abort, p.status);
+                    mbar_wait(&full[s], (armed_parity >> s) & 1u, &no_abort, p.status);
                 }
         }
     } else if (warp == 1) {   // ------------------------------------- MMA issuer
@@ -428,9 +392,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int kb = 0; kb < nkb; ++kb) {
-                const bool landed = WG ? mbar_wait<true>(&full[stage], phase, abort_s, p.status)
-                                       : mbar_wait(&full[stage], phase, abort_s, p.status);
-                if (!__all_sync(0xffffffffu, landed)) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_s, p.status))) {
                     ok = false;
                     break;
                 }
@@ -465,10 +427,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                                                : smem_desc_sw128(b_addr + kk * 32);
                         mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
                     }
-                    if (WG)
-                        commit_both(&empty[stage]);   // the stage is free in both CTAs' view
-                    else
-                        commit(&empty[stage]);
+                    commit(&empty[stage]);
                 }
                 __syncwarp();
                 if (++stage == STAGES) {
@@ -676,7 +635,6 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     if (WG && warp >= 2 && lane == 0) tma_store_wait_all();   // stores done, staging free
     fence_before();
     __syncthreads();
-    if (WG) cluster_sync_all();   // no CTA leaves while its peer may still signal it
     if (warp == 1) {
         fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -693,62 +651,29 @@ cudaError_t launch_bwd(const BwdMaps &maps, BwdParams prm, int64_t max_tiles, cu
     prm.lbo = MN_BOX;
     prm.sbo = 1024;
     auto kern = grouped_gemm_bwd_kernel<KIND>;
-    constexpr bool WG = KIND == BWD_WGRAD;
-    // per device: CTAs (dgrad) or clusters of two (weight gradients) resident at once
+    // per device: the SM count (one persistent CTA per SM), set up once
     static std::mutex mu;
-    static int slots_dev[64] = {};
+    static int sms_dev[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    int slots;
+    int sms;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (slots_dev[dev] == 0) {
+        if (sms_dev[dev] == 0) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)Smem<KIND>::alloc);
             if (e != cudaSuccess) return e;
             int n = 0;
-            if (WG) {
-                cudaLaunchConfig_t cfg = {};
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = 2;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.gridDim = dim3(2, 1, 1);
-                cfg.blockDim = dim3(num_threads<KIND>(), 1, 1);
-                cfg.dynamicSmemBytes = Smem<KIND>::alloc;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
-                e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-            } else {
-                e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-            }
+            e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return e;
-            if (n < 1) return cudaErrorInvalidConfiguration;
-            slots_dev[dev] = n;
+            sms_dev[dev] = n > 0 ? n : 148;
         }
-        slots = slots_dev[dev];
+        sms = sms_dev[dev];
     }
-    const int units = (int)std::min<int64_t>(max_tiles, slots);
-    if (!WG)
-        return launch_pdl(kern, dim3(units), dim3(num_threads<KIND>()), Smem<KIND>::alloc, s, maps, prm);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(2 * units, 1, 1);
-    cfg.blockDim = dim3(num_threads<KIND>(), 1, 1);
-    cfg.dynamicSmemBytes = Smem<KIND>::alloc;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, maps, prm);
+    const int grid = (int)std::min<int64_t>(max_tiles, sms);
+    return launch_pdl(kern, dim3(grid), dim3(num_threads<KIND>()), Smem<KIND>::alloc, s, maps, prm);
 }
 
 cudaError_t token_maps(BwdMaps *m, const void *t, uint64_t rows, uint64_t cols, uint64_t ld) {
@@ -837,7 +762,7 @@ cudaError_t launch_tc_wgrad_gate_up(const LayerDims &d, const void *dgu, const v
     prm.rows = (int)rows;
     prm.wgrad_gu = 1;
     prm.status = status;
-    return launch_bwd<BWD_WGRAD>(maps, prm, (int64_t)d.E * ((prm.m_tiles + 1) / 2) * prm.n_tiles, s);
+    return launch_bwd<BWD_WGRAD>(maps, prm, (int64_t)d.E * prm.m_tiles * prm.n_tiles, s);
 }
 
 cudaError_t launch_tc_wgrad_down(const LayerDims &d, const void *dout_send, const void *wa,
@@ -862,7 +787,7 @@ cudaError_t launch_tc_wgrad_down(const LayerDims &d, const void *dout_send, cons
     prm.rows = (int)rows;
     prm.wgrad_gu = 0;
     prm.status = status;
-    return launch_bwd<BWD_WGRAD>(maps, prm, (int64_t)d.E * ((prm.m_tiles + 1) / 2) * prm.n_tiles, s);
+    return launch_bwd<BWD_WGRAD>(maps, prm, (int64_t)d.E * prm.m_tiles * prm.n_tiles, s);
 }
 
 }  // namespace moe

@@ -249,20 +249,25 @@ moe_status_t moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const 
 /*
  * moe_dispatch without a workspace argument. The pages have no counterpart: this entry
  * point exists for callers that cannot allocate device memory on their own -- code that
- * runs where cudaMalloc is unavailable or forbidden (inside a host callback, or under an
- * allocator that owns all device memory and hands out only the layer's inputs and
- * outputs) and therefore cannot provide moe_dispatch's workspace.
+ * runs under an allocator that owns all device memory and hands out only the layer's
+ * inputs and outputs, and therefore cannot provide moe_dispatch's workspace. (It makes
+ * CUDA calls, so like every entry point here it must not be called from a host function
+ * enqueued on a stream.)
  *
  * Same arguments, results and errors as moe_dispatch, minus workspace and its size. The
  * per-segment histograms live instead in a fixed array of device memory inside the
  * library (1 MiB, plus 256 bytes for a status word), which every GPU that
- * loads the library keeps until the process exits. Limit: ceil(num_tokens / 64) *
- * num_experts must not exceed 262144 (for example 65536 tokens with 256 experts);
- * larger calls return MOE_ERR_UNSUPPORTED and enqueue nothing.
+ * loads the library keeps until the process exits. Limit: segments * num_experts must
+ * not exceed 262144, where segments = ceil(num_tokens / 64) in token-order capacity
+ * priority and top_k * ceil(num_tokens / (64 * top_k)) in slot-major priority (for
+ * example 65536 tokens with 256 experts in token order); larger calls return
+ * MOE_ERR_UNSUPPORTED and enqueue nothing.
  *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  *  - The first call on a device looks up the array's device address on that device
  *    (cudaGetSymbolAddress, with that device current); make that first call before
- *    any stream capture.
+ *    any stream capture. The address is kept for the life of the process, so the
+ *    device must not be reset (cudaDeviceReset) nor its primary context destroyed
+ *    while the library is in use.
  *  - All calls share the one array: calls whose work overlaps on the GPU (on different
  *    streams, or from different threads) race and corrupt each other's results. Order
  *    them on one stream or synchronise between them.

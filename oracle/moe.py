@@ -12,7 +12,7 @@ Sources, cited by page title and section:
            GPUs" (the four steps and the routing example) and "Load balancing and
            capacity".
 
-Readings taken where the pages are silent (each listed in the design notes):
+Readings taken where the pages are silent:
   * the router score is the raw linear logit; the k largest are chosen, ties going to
     the lower expert id; the routing weights are a softmax over the k chosen logits;
   * each expert is a SwiGLU FFN  y = Wd (silu(Wg x) * (Wu x)), no biases;

@@ -66,3 +66,11 @@ def test_noalloc_dispatch_rejects_sizes_beyond_its_scratch():
                                       fake, fake, fake, None)
     assert st == moe.binding.MOE_ERR_UNSUPPORTED
     assert "exceeds" in moe.lib.moe_last_error().decode()
+    # slot-major priority counts its segments per slot: 7 * ceil(65436 / 448) = 1029
+    # segments x 256 experts = 263424 > 262144, rejected, although the token-order count
+    # of the same call, ceil(65436 / 64) * 256 = 261888, would fit
+    cfg = moe.config(65436, 64, 64, 256, 7, 8, capacity_priority="slot")
+    st = moe.lib.moe_dispatch_noalloc(ctypes.byref(cfg), fake, fake, fake, fake, fake, fake,
+                                      fake, fake, fake, None)
+    assert st == moe.binding.MOE_ERR_UNSUPPORTED
+    assert "1029 histogram segments" in moe.lib.moe_last_error().decode()
