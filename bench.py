@@ -9,16 +9,24 @@ gpt-oss-120b-shaped layer (8192 tokens x hidden 2880, 128 experts, top-4, SwiGLU
 intermediate 2880, 8 logical EP partitions). Its 6.4 GB of expert weights are ~50x the
 L2, so no L2 flush is needed between steps.
 
+The line also carries, for the same workload, the per-stage rooflines, the training
+step, the routing variants and an end-to-end figure with host copies, and (one GPU
+only) a `workloads` object: the other forward rule on the same inputs and the PR1,
+8-expert, skewed + capacity and decode workloads, each with its stage rooflines,
+clocks and training step.
+
 Under torchrun (N > 1) every rank runs the same layer on its own batch (different
 seed): the expert-parallel partitions live inside one GPU, so ranks share no data and
 the scaling is weak, with no collective on the data path.
 
---impl reference times the fp64 CPU oracle instead (rank 0 only), on a bounded sample
-of the same workload, extrapolated to the whole batch.
+--impl reference times the fp64 CPU oracle instead (rank 0 only, one thread): every
+step is the whole layer on a token slice of the same batch, and the line reports the
+measured time of that work.
 """
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import math
@@ -30,6 +38,12 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
+
+# The CPU legs time the oracle on one core: numpy's BLAS reads its thread count when it
+# loads, so the limit is set before numpy is imported (SingleThread also sets and checks
+# it at run time).
+os.environ["OPENBLAS_NUM_THREADS"] = "1"
+os.environ["MKL_NUM_THREADS"] = "1"
 
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
@@ -211,58 +225,138 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle timing
-def blas_threads():
+def host_cpu():
+    """The host's CPU model and logical core count."""
+    model = "unknown"
     try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        return max(n) if n else 1
-    except Exception:
-        return 1
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return dict(model=model, logical_cores=os.cpu_count())
 
 
-def time_oracle(shape, x, w_router, b_router, expert_fn, n_sample_experts, seed=0,
-                ffn_budget_s=None):
-    """Times the fp64 oracle on the whole batch for routing, dispatch and combine, and on
-    the full segments of up to `n_sample_experts` experts (in a seeded random order; with
-    `ffn_budget_s`, until that much expert time is spent) for the SwiGLU experts; the
-    expert time is extrapolated to every kept pair (exact when every expert ran).
-    Returns (seconds for the batch, detail)."""
+def _openblas_libs():
+    """The OpenBLAS libraries loaded into this process (numpy's), by path."""
+    import ctypes
+    paths = []
+    try:
+        with open("/proc/self/maps") as f:
+            for ln in f:
+                path = ln.split()[-1] if len(ln.split()) >= 6 else ""
+                if "openblas" in os.path.basename(path).lower() and ".so" in path and path not in paths:
+                    paths.append(path)
+    except OSError:
+        return []
+    libs = []
+    for path in paths:
+        try:
+            libs.append(ctypes.CDLL(path))
+        except OSError:
+            continue
+    return libs
+
+
+def _blas_fn(lib, what):
+    """OpenBLAS's openblas_{get,set}_num_threads under the names its builds export."""
+    for name in (f"openblas_{what}_num_threads", f"scipy_openblas_{what}_num_threads64_",
+                 f"openblas_{what}_num_threads64_", f"scipy_openblas_{what}_num_threads"):
+        fn = getattr(lib, name, None)
+        if fn is not None:
+            return fn
+    return None
+
+
+class SingleThread:
+    """Limits numpy's BLAS to one thread for the timed oracle work and reports the thread
+    count in force, read back from the library: through threadpoolctl when it is
+    installed, else through OpenBLAS's own get/set calls. Raises when neither can
+    confirm one thread: the CPU figures claim one core."""
+
+    def __enter__(self):
+        self._undo = None
+        try:
+            from threadpoolctl import threadpool_info, threadpool_limits
+        except ImportError:
+            threadpool_info = None
+        if threadpool_info is not None:
+            ctx = threadpool_limits(limits=1)
+            ctx.__enter__()
+            self._undo = lambda *a: ctx.__exit__(*a)
+            pools = threadpool_info()
+            self.threads = max([int(i.get("num_threads", 1)) for i in pools] or [1])
+            self.pools = sorted({f"{i.get('user_api')}:{i.get('internal_api')}" for i in pools})
+        else:
+            libs = [(lib, _blas_fn(lib, "get"), _blas_fn(lib, "set")) for lib in _openblas_libs()]
+            libs = [x for x in libs if x[1] is not None and x[2] is not None]
+            if not libs:
+                raise RuntimeError("no OpenBLAS thread control found to pin the oracle to one thread")
+            before = [int(get()) for _, get, _ in libs]
+            for _, _, set_ in libs:
+                set_(1)
+            self._undo = lambda *a: [set_(n) for (_, _, set_), n in zip(libs, before)]
+            self.threads = max(int(get()) for _, get, _ in libs)
+            self.pools = [f"blas:openblas (set through its API; OPENBLAS_NUM_THREADS="
+                          f"{os.environ.get('OPENBLAS_NUM_THREADS')})"]
+        if self.threads != 1:
+            raise RuntimeError(f"the oracle's BLAS still uses {self.threads} threads: {self.pools}")
+        return self
+
+    def __exit__(self, *a):
+        if self._undo is not None:
+            self._undo(*a)
+        return False
+
+
+# Token sample of the CPU runs: as many tokens as fit about 2e11 expert flops (1024 at the
+# gpt-oss shape), so one pass of the fp64 oracle takes a few seconds on one core.
+CPU_SAMPLE_FLOPS = 2.0e11
+
+
+def cpu_sample_tokens(shape):
+    per_token = 6.0 * shape.top_k * shape.H * shape.I
+    return int(max(1, min(shape.N, CPU_SAMPLE_FLOPS // per_token)))
+
+
+def time_oracle_slice(shape, x, w_router, b_router, expert_fn, t0, S, mode="dispatch"):
+    """The fp64 oracle's whole layer (route, capacity, dispatch layout, permute, every
+    expert that received rows, combine) on the S tokens t0 .. t0+S-1, as a layer call
+    of its own. Only the oracle's work is timed: expert_fn(e) hands over an expert's
+    fp64 weights outside the timed region (they are resident, as on the GPU side).
+    Returns (timed seconds, detail)."""
     import oracle
-    N, k, E = shape.N, shape.top_k, shape.E
-    t0 = time.perf_counter()
-    logits, idx, w = oracle.route(x, w_router, b_router, k)
-    t1 = time.perf_counter()
-    C = oracle.expert_capacity(shape.capacity_factor, N, k, E)
-    lay = oracle.dispatch_layout(idx, E, shape.ep_size, C)
-    send = oracle.permute(x, lay["perm"], k)
-    t2 = time.perf_counter()
-    rng = np.random.default_rng(seed)
-    busy = np.nonzero(lay["counts"])[0]
-    pick = rng.choice(busy, size=min(n_sample_experts, busy.size), replace=False)
-    rows = 0
+    k, E, P = shape.top_k, shape.E, shape.ep_size
+    xs = x[t0:t0 + S]
+    c0 = time.perf_counter()
+    logits, idx, w = oracle.route(xs, w_router, b_router, k)
+    C = oracle.expert_capacity(shape.capacity_factor, S, k, E)
+    lay = oracle.dispatch_layout(idx, E, P, C)
+    send = oracle.permute(xs, lay["perm"], k)
+    y = np.zeros((send.shape[0], shape.H))
+    t_route = time.perf_counter() - c0
     t_ffn = 0.0
-    done = 0
-    for e in pick:
-        if ffn_budget_s is not None and done > 0 and t_ffn >= ffn_budget_s:
-            break
-        done += 1
-        wg, wu, wd = expert_fn(int(e))
+    busy = 0
+    for e in range(E):
         a, b = int(lay["expert_offsets"][e]), int(lay["expert_offsets"][e + 1])
-        ts = time.perf_counter()
-        oracle.swiglu_expert(send[a:b], wg, wu, wd)
-        t_ffn += time.perf_counter() - ts
-        rows += b - a
-    y_send = np.zeros((send.shape[0], shape.H))
-    t3 = time.perf_counter()
-    oracle.combine_dispatch(y_send, lay["slot_pos"], w, N, k)
-    t4 = time.perf_counter()
-    kept = int(lay["expert_offsets"][-1])
-    ffn_total = t_ffn * kept / max(rows, 1)
-    total = (t1 - t0) + (t2 - t1) + ffn_total + (t4 - t3)
-    detail = dict(route_s=t1 - t0, dispatch_s=t2 - t1, ffn_sample_s=t_ffn,
-                  ffn_extrapolated_s=ffn_total, combine_s=t4 - t3, sample_rows=rows,
-                  kept_pairs=kept, sampled_experts=done, busy_experts=int(busy.size))
-    return total, detail
+        if b == a:
+            continue
+        busy += 1
+        wg, wu, wd = expert_fn(e)
+        c1 = time.perf_counter()
+        y[a:b] = oracle.swiglu_expert(send[a:b], wg, wu, wd)
+        t_ffn += time.perf_counter() - c1
+    c2 = time.perf_counter()
+    if mode == "dispatch":
+        oracle.combine_dispatch(y, lay["slot_pos"], w, S, k)
+    else:
+        oracle.combine_mask_sum(y, lay["slot_pos"], idx, w, E, P)
+    t_combine = time.perf_counter() - c2
+    total = t_route + t_ffn + t_combine
+    return total, dict(route_dispatch_s=t_route, experts_s=t_ffn, combine_s=t_combine,
+                       tokens=S, kept_pairs=int(lay["expert_offsets"][-1]), busy_experts=busy)
 
 
 def host_inputs_for_oracle(shape, inp):
@@ -270,67 +364,90 @@ def host_inputs_for_oracle(shape, inp):
     return f(inp["x"]), f(inp["w_router"]), f(inp["b_router"])
 
 
-def cpu_baseline_from_device(shape, inp, ffn_budget_s=10.0):
-    """The oracle on the bench workload: route, dispatch and combine on every token, and
-    the SwiGLU experts one by one until about `ffn_budget_s` seconds of expert work are
-    spent (every expert when they fit: then nothing is extrapolated)."""
+def cpu_baseline_from_device(shape, inp, mode="dispatch"):
+    """The oracle on one core on a bounded token sample of the bench workload: the whole
+    layer (every step, every expert the sample reaches) on the first S tokens, each
+    expert's weights copied from the device and widened to fp64 outside the timing."""
     x, wr, b = host_inputs_for_oracle(shape, inp)
+    S = cpu_sample_tokens(shape)
 
     def expert_fn(e):
         return tuple(inp[k][e].detach().to("cpu", torch.float64).numpy()
                      for k in ("w_gate", "w_up", "w_down"))
 
-    total, detail = time_oracle(shape, x, wr, b, expert_fn, shape.E, ffn_budget_s=ffn_budget_s)
-    whole = detail["sampled_experts"] == detail["busy_experts"]
-    ffn = ("SwiGLU experts on every kept pair (the whole layer, nothing extrapolated)" if whole
-           else f"SwiGLU experts timed on the full segments of {detail['sampled_experts']} of "
-                f"{shape.E} experts ({detail['sample_rows']} of {detail['kept_pairs']} kept "
-                f"pairs, about {ffn_budget_s:.0f} s), extrapolated linearly in kept pairs")
-    return dict(value=round(shape.N / total, 2), unit="tokens/s", cores=blas_threads(),
-                kind="oracle",
-                sample=f"fp64 oracle: route, dispatch and combine on all {shape.N} tokens; {ffn}",
-                seconds=round(total, 3), detail={k: (round(v, 4) if isinstance(v, float) else v)
-                                                 for k, v in detail.items()})
+    with SingleThread() as st:
+        total, detail = time_oracle_slice(shape, x, wr, b, expert_fn, 0, S, mode)
+    return dict(value=round(S / total, 2), unit="tokens/s", cores=st.threads, kind="oracle",
+                sample=f"fp64 oracle, one thread: the whole layer on tokens 0..{S - 1} of the "
+                       f"{shape.N}-token batch as one call ({detail['kept_pairs']} kept pairs, "
+                       f"{detail['busy_experts']} experts)",
+                seconds=round(total, 3), host=host_cpu(), thread_pools=st.pools,
+                detail={k: (round(v, 4) if isinstance(v, float) else v) for k, v in detail.items()})
+
+
+def resident_expert_weights(shape, seed=0):
+    """Every expert's fp64 weights drawn on the CPU (the GPU arm's seeded weights), held
+    in host memory when they fit in half of it; else None and they are drawn per use."""
+    need = 3 * shape.E * shape.I * shape.H * 8
+    try:
+        avail = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError):
+        avail = 0
+    if need > avail // 2:
+        return None
+    return {key: [workloads.expert_weight(shape, key, e, seed, "cpu").double().numpy()
+                  for e in range(shape.E)] for key in ("w_gate", "w_up", "w_down")}
 
 
 def run_reference(args, shape):
-    """--impl reference: the fp64 CPU oracle as it stands, one bounded sample per step."""
+    """--impl reference: the fp64 CPU oracle as it stands, on one core. Every step (warm-up
+    and timed) is the whole layer on a slice of S tokens of the bench batch, a different
+    slice per step; ms_per_step is the measured time of that work and value the tokens it
+    processed per second."""
     inp = workloads.layer_inputs(shape, seed=0, variant="perf", device="cpu",
                                  with_experts=False)
     x, wr, b = host_inputs_for_oracle(shape, inp)
-    cache = {}
+    S = cpu_sample_tokens(shape)
+    res = resident_expert_weights(shape)
 
     def expert_fn(e):
-        if e not in cache:
-            cache.clear()
-            cache[e] = tuple(workloads.expert_weight(shape, k, e, 0, "cpu").double().numpy()
-                             for k in ("w_gate", "w_up", "w_down"))
-        return cache[e]
+        if res is not None:
+            return res["w_gate"][e], res["w_up"][e], res["w_down"][e]
+        return tuple(workloads.expert_weight(shape, k, e, 0, "cpu").double().numpy()
+                     for k in ("w_gate", "w_up", "w_down"))
 
-    for i in range(args.warmup):
-        time_oracle(shape, x, wr, b, expert_fn, 1, seed=i)
-    totals = []
-    details = None
-    for i in range(args.steps):
-        t, details = time_oracle(shape, x, wr, b, expert_fn, 1, seed=100 + i)
-        totals.append(t)
+    slices = max(1, shape.N // S)
+    totals, details = [], []
+    with SingleThread() as st:
+        for i in range(args.warmup):
+            time_oracle_slice(shape, x, wr, b, expert_fn, (i % slices) * S, S, args.mode)
+        for i in range(args.steps):
+            t, det = time_oracle_slice(shape, x, wr, b, expert_fn,
+                                       ((args.warmup + i) % slices) * S, S, args.mode)
+            totals.append(t)
+            details.append(det)
     sec = float(np.mean(totals))
-    value = shape.N / sec
-    cores = blas_threads()
-    sample = (f"per step: fp64 oracle route, dispatch and combine on all {shape.N} tokens, "
-              f"SwiGLU of 1 of {shape.E} experts on its full segment, extrapolated "
-              f"linearly in kept pairs")
-    line = dict(metric=METRIC, value=round(value, 3), unit="tokens/s", n_gpus=args.gpus,
+    value = S / sec
+    sample = (f"per step: fp64 oracle, one thread, the whole layer on a {S}-token slice of "
+              f"the {shape.N}-token batch as one call (slice i*{S} of step i)")
+    world = args.gpus
+    line = dict(metric=METRIC, value=round(value, 3), unit="tokens/s", n_gpus=world,
                 steps=args.steps, warmup=args.warmup, ms_per_step=round(sec * 1e3, 3),
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
-                data="synthetic (seeded; same distributions as the GPU arm)",
-                config=workload_config(shape), impl="reference",
-                cpu_baseline=dict(value=round(value, 3), unit="tokens/s", cores=cores,
-                                  kind="oracle", sample=sample),
+                data=DATA, config=run_config(shape, args.mode, world), impl="reference",
+                cpu_baseline=dict(value=round(value, 3), unit="tokens/s", cores=st.threads,
+                                  kind="oracle", sample=sample, host=host_cpu(),
+                                  thread_pools=st.pools,
+                                  weights="resident fp64" if res is not None
+                                  else "drawn per use, outside the timing"),
                 e2e=dict(value=round(value, 3), unit="tokens/s", h2d_bytes_per_step=0,
                          d2h_bytes_per_step=0),
-                detail={k: (round(v, 4) if isinstance(v, float) else v)
-                        for k, v in details.items()})
+                detail=dict(tokens_per_step=S,
+                            kept_pairs_per_step=int(np.mean([d["kept_pairs"] for d in details])),
+                            experts_s=round(float(np.mean([d["experts_s"] for d in details])), 4),
+                            route_dispatch_s=round(float(np.mean([d["route_dispatch_s"]
+                                                                  for d in details])), 4),
+                            combine_s=round(float(np.mean([d["combine_s"] for d in details])), 4)))
     print(json.dumps(line), flush=True)
 
 
@@ -348,12 +465,12 @@ def load_summary(shape, routed, kept):
 BACKWARD_LAUNCHES = 11   # permute, 4 GEMMs, logit grads, dx combine, histogram, scan, 2 router
 
 
-def time_backward(moe, args, shape, inp, packed, dist, dev, stream):
+def time_backward(moe, args, shape, inp, packed, dist, dev, stream, mode=None):
     """A training step on the same workload: moe_layer_forward with training = 1, then
     moe_layer_backward (CUDA events around each, `steps` timed after `warmup`). The four
     expert GEMMs of the backward are 2 x the forward's 6 A' H I flops."""
     cfg = moe.config(shape.N, shape.H, shape.I, shape.E, shape.top_k, shape.ep_size,
-                     shape.capacity_factor, args.mode, shape.dtype,
+                     shape.capacity_factor, mode or args.mode, shape.dtype,
                      has_bias=inp["b_router"] is not None, training=True)
     ws = moe.alloc_workspace(cfg, dev)
     x, wr, b, wd = inp["x"], inp["w_router"], inp["b_router"], inp["w_down"]
@@ -489,15 +606,195 @@ def time_variants(moe, args, shape, inp, packed, dev, stream):
     return res
 
 
+DATA = "synthetic (seeded; x~N(0,1), router~U(+-1/sqrt(H)), experts~N(0,0.02))"
+
+
 def workload_config(shape):
     return dict(workload=shape.name, tokens=shape.N, hidden=shape.H, intermediate=shape.I,
                 experts=shape.E, top_k=shape.top_k, ep_size=shape.ep_size,
                 capacity_factor=shape.capacity_factor, router_zipf_s=shape.zipf_s,
-                mode="dispatch", values="perf (continuous)",
-                l2="inputs larger than L2 (expert weights >> 126 MB); no flush")
+                values="perf (continuous)",
+                l2=("inputs larger than L2 (expert weights >> 126 MB); no flush"
+                    if 3 * shape.E * shape.H * shape.I * (2 if shape.dtype == "bf16" else 4) > 126e6
+                    else "inputs within L2 size: steps may hit L2; no flush"))
+
+
+def run_config(shape, mode, world):
+    """The `config` object of both arms' lines (the same dict for the same run)."""
+    return dict(workload_config(shape), mode=mode,
+                parallelism=f"replicas x{world} (one layer per GPU)")
 
 
 # ------------------------------------------------------------------ GPU arm
+class Layer:
+    """One workload's inputs, packed weights, workspace and output on the device."""
+
+    def __init__(self, moe, shape, mode, dev, seed, inp=None, packed=None):
+        self.shape, self.mode = shape, mode
+        self.inp = inp if inp is not None else workloads.layer_inputs(shape, seed=seed,
+                                                                      variant="perf", device=dev)
+        self.cfg = moe.config(shape.N, shape.H, shape.I, shape.E, shape.top_k, shape.ep_size,
+                              shape.capacity_factor, mode, shape.dtype,
+                              has_bias=self.inp["b_router"] is not None)
+        self.packed = packed if packed is not None else moe.moe_pack_weights(
+            self.cfg, self.inp["w_gate"], self.inp["w_up"])
+        self.ws = moe.alloc_workspace(self.cfg, dev)
+        self.out = torch.empty(shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
+
+    def forward(self, moe, diag=None, events=None, x=None, out=None):
+        i = self.inp
+        moe.moe_layer_forward(self.cfg, i["x"] if x is None else x, i["w_router"], i["b_router"],
+                              self.packed, i["w_down"], self.out if out is None else out,
+                              self.ws, diag, events)
+
+
+FORWARD_LAUNCHES = 6   # route, scan/assign, permute, gate_up, down, combine
+
+
+def time_forward(moe, L, steps, warmup, dist, dev, stream, clocks=True):
+    """`warmup` untimed steps, then `steps` timed forward steps between a barrier and a
+    synchronize on both sides (CUDA events on the launching stream; the library records
+    an event at every stage boundary). Returns the slowest rank's step time, the mean
+    stage times, the kept and routed counts and the clock record."""
+    shape = L.shape
+    counts_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
+    routed_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
+    L.forward(moe, dict(counts=counts_t, routed_counts=routed_t))
+    torch.cuda.synchronize()
+    counts, routed = counts_t.cpu().numpy(), routed_t.cpu().numpy()
+    nst = moe.binding.MOE_NUM_STAGES
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)     # creates the handles before the library re-records them
+    for _ in range(warmup):
+        L.forward(moe, None, evs[0])
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    sampler = ClockSampler(dev.index or 0) if clocks else contextlib.nullcontext()
+    with sampler as clk:
+        # a short device-side delay lets the host enqueue ahead of the timed steps, so
+        # the first step does not wait for its launches (the delay is before `start`)
+        torch.cuda._sleep(2_000_000)
+        start.record(stream)
+        for i in range(steps):
+            L.forward(moe, None, evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    stage_ms = {name: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)]))
+                for j, name in enumerate(moe.binding.STAGE_NAMES)}
+    flags = moe.moe_read_device_status(L.cfg, L.ws)
+    if flags:
+        raise RuntimeError(f"device status flags {flags} after the timed steps of {shape.name}")
+    ms_step = slowest_rank_ms(start.elapsed_time(end) / steps, dist, dev)
+    return dict(ms_step=ms_step, stage_ms=stage_ms, counts=counts, routed=routed,
+                clocks=clk.summary() if clocks else None)
+
+
+def stage_rooflines(shape, stage_ms, counts, names):
+    peaks, source = load_peaks()
+    work = stage_work(shape, counts)
+    return {n: dict(ms=round(stage_ms[n], 4),
+                    **{k: v for k, v in roofline_entry(work[n], max(stage_ms[n], 1e-6), peaks,
+                                                       source, shape.dtype).items()
+                       if k in ("bound", "achieved", "unit", "frac", "hbm_frac", "tensor_frac")})
+            for n in names}
+
+
+def dominant_roofline(shape, stage_ms, counts, with_traffic=True):
+    peaks, source = load_peaks()
+    work = stage_work(shape, counts)
+    dom = max(("gate_up", "down", "route", "permute", "combine"), key=lambda n: stage_ms[n])
+    roof = roofline_entry(work[dom], stage_ms[dom], peaks, source, shape.dtype)
+    return dict(kernel=dom, **roof,
+                traffic=measured_traffic(shape.name, dom) if with_traffic else None)
+
+
+def time_e2e(moe, L, steps, dist, dev, stream):
+    """End to end through the C ABI: every step copies its input from pinned host memory
+    to the device and reads its output back. Copies run on their own streams, double
+    buffered, so step i+1's upload and step i-1's download overlap step i's compute."""
+    x, out = L.inp["x"], L.out
+    x_host = [x.cpu().pin_memory() for _ in range(2)]
+    out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    out_dev = [torch.empty_like(out) for _ in range(2)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run_pipeline(n):
+        uploaded = [torch.cuda.Event() for _ in range(n)]
+        computed = [torch.cuda.Event() for _ in range(n)]
+        downloaded = [torch.cuda.Event() for _ in range(n)]
+        for i in range(n):
+            bb = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(computed[i - 2])     # x_dev[bb] no longer read
+                x_dev[bb].copy_(x_host[bb], non_blocking=True)
+                uploaded[i].record(up)
+            stream.wait_event(uploaded[i])
+            if i >= 2:
+                stream.wait_event(downloaded[i - 2])   # out_dev[bb] already read back
+            L.forward(moe, x=x_dev[bb], out=out_dev[bb])
+            computed[i].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[i])
+                out_host[bb].copy_(out_dev[bb], non_blocking=True)
+                downloaded[i].record(down)
+        stream.wait_event(downloaded[n - 1])
+
+    run_pipeline(3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    run_pipeline(steps)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    world = dist.get_world_size() if dist is not None else 1
+    e2e_ms = slowest_rank_ms(s0.elapsed_time(s1) / steps, dist, dev)
+    return dict(value=round(job_tokens_per_s(L.shape.N, world, e2e_ms), 1), unit="tokens/s",
+                ms_per_step=round(e2e_ms, 4), h2d_bytes_per_step=x.numel() * x.element_size(),
+                d2h_bytes_per_step=out.numel() * out.element_size(),
+                overlap="uploads and downloads on their own streams, double buffered")
+
+
+# The other workloads of the layer, timed after the headline one in the default run
+# (forward, its stage rooflines and clocks, and the training step): the PR1 fp32 layer,
+# the 8-expert and skewed + capacity layers (where the grouped GEMM is tensor bound) and
+# the decode batch (weight-read bound; its step time is the layer's latency).
+EXTRA_WORKLOADS = (workloads.PR1_FP32, workloads.E8_TOP2, workloads.SKEWED_CAP, workloads.DECODE)
+
+
+def workload_entry(moe, args, L, dist, dev, stream, backward=True):
+    shape = L.shape
+    world = dist.get_world_size() if dist is not None else 1
+    r = time_forward(moe, L, args.steps, args.warmup, dist, dev, stream)
+    stages = ("route", "scan", "permute", "gate_up", "down", "combine")
+    entry = dict(mode=L.mode, tokens_per_s=round(job_tokens_per_s(shape.N, world, r["ms_step"]), 1),
+                 ms_per_step=round(r["ms_step"], 4), dtype=shape.dtype,
+                 config=workload_config(shape),
+                 roofline=dominant_roofline(shape, r["stage_ms"], r["counts"], with_traffic=False),
+                 stages=stage_rooflines(shape, r["stage_ms"], r["counts"], stages),
+                 kept_pairs=int(r["counts"].sum()), load=load_summary(shape, r["routed"], r["counts"]),
+                 clocks=r["clocks"], gpu_launches=FORWARD_LAUNCHES * args.steps)
+    if shape.N <= 256:
+        entry["latency_ms"] = round(r["ms_step"], 4)
+    if backward:
+        entry["backward"] = time_backward(moe, args, shape, L.inp, L.packed, dist, dev, stream,
+                                          mode=L.mode)
+    return entry
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -510,6 +807,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads and the mask-and-sum line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -532,146 +831,57 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     dev = torch.device("cuda", local)
-    inp = workloads.layer_inputs(shape, seed=rank, variant="perf", device=dev)
-    cfg = moe.config(shape.N, shape.H, shape.I, shape.E, shape.top_k, shape.ep_size,
-                     shape.capacity_factor, args.mode, shape.dtype,
-                     has_bias=inp["b_router"] is not None)
-    packed = moe.moe_pack_weights(cfg, inp["w_gate"], inp["w_up"])
-    ws = moe.alloc_workspace(cfg, dev)
-    out = torch.empty(shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
-    x, wr, b, wd = inp["x"], inp["w_router"], inp["b_router"], inp["w_down"]
     stream = torch.cuda.current_stream()
-
-    # one run with diagnostics for the kept counts (algorithmic work of each stage)
-    counts_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
-    routed_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
-    moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws,
-                          dict(counts=counts_t, routed_counts=routed_t))
-    torch.cuda.synchronize()
-    counts = counts_t.cpu().numpy()
-    load = load_summary(shape, routed_t.cpu().numpy(), counts)
-    work = stage_work(shape, counts)
-
-    nst = moe.binding.MOE_NUM_STAGES
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
-           for _ in range(args.steps)]
-    for row in evs:
-        for e in row:
-            e.record(stream)     # creates the handles before the library re-records them
-    for _ in range(args.warmup):
-        moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws, None, evs[0])
-    torch.cuda.synchronize()
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    with ClockSampler(local) as clk:
-        # a short device-side delay lets the host enqueue ahead of the timed steps, so
-        # the first step does not wait for its launches (the delay is before `start`)
-        torch.cuda._sleep(2_000_000)
-        start.record(stream)
-        for i in range(args.steps):
-            moe.moe_layer_forward(cfg, x, wr, b, packed, wd, out, ws, None, evs[i])
-        end.record(stream)
-        torch.cuda.synchronize()
-    barrier()
-    ms_total = start.elapsed_time(end)
-    stage_ms = {}
-    for j, name in enumerate(moe.binding.STAGE_NAMES):
-        stage_ms[name] = float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1])
-                                         for i in range(args.steps)]))
-    flags = moe.moe_read_device_status(cfg, ws)
-    if flags:
-        raise RuntimeError(f"device status flags {flags} after the timed steps")
-
-    ms_step = slowest_rank_ms(ms_total / args.steps, dist, dev)
+    L = Layer(moe, shape, args.mode, dev, seed=rank)
+    r = time_forward(moe, L, args.steps, args.warmup, dist, dev, stream)
+    ms_step = r["ms_step"]
     value = job_tokens_per_s(shape.N, world, ms_step)
+    counts = r["counts"]
 
     variants = None
     if not args.no_variants:   # before the backward's long high-power stretch
-        variants = time_variants(moe, args, shape, inp, packed, dev, stream)
+        variants = time_variants(moe, args, shape, L.inp, L.packed, dev, stream)
     backward = None
     if not args.no_backward:
-        backward = time_backward(moe, args, shape, inp, packed, dist, dev, stream)
+        backward = time_backward(moe, args, shape, L.inp, L.packed, dist, dev, stream)
+    e2e = None if args.no_e2e else time_e2e(moe, L, args.steps, dist, dev, stream)
 
-    # end to end through the C ABI: every step copies its input from pinned host memory
-    # to the device and reads its output back. Copies run on their own streams, double
-    # buffered, so step i+1's upload and step i-1's download overlap step i's compute.
-    e2e = None
-    if not args.no_e2e:
-        K = args.steps
-        x_host = [x.cpu().pin_memory() for _ in range(2)]
-        out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-        x_dev = [torch.empty_like(x) for _ in range(2)]
-        out_dev = [torch.empty_like(out) for _ in range(2)]
-        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-
-        def run_pipeline(n):
-            uploaded = [torch.cuda.Event() for _ in range(n)]
-            computed = [torch.cuda.Event() for _ in range(n)]
-            downloaded = [torch.cuda.Event() for _ in range(n)]
-            for i in range(n):
-                bb = i % 2
-                with torch.cuda.stream(up):
-                    if i >= 2:
-                        up.wait_event(computed[i - 2])     # x_dev[bb] no longer read
-                    x_dev[bb].copy_(x_host[bb], non_blocking=True)
-                    uploaded[i].record(up)
-                stream.wait_event(uploaded[i])
-                if i >= 2:
-                    stream.wait_event(downloaded[i - 2])   # out_dev[bb] already read back
-                moe.moe_layer_forward(cfg, x_dev[bb], wr, b, packed, wd, out_dev[bb], ws)
-                computed[i].record(stream)
-                with torch.cuda.stream(down):
-                    down.wait_event(computed[i])
-                    out_host[bb].copy_(out_dev[bb], non_blocking=True)
-                    downloaded[i].record(down)
-            stream.wait_event(downloaded[n - 1])
-
-        run_pipeline(3)
-        barrier()
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        run_pipeline(K)
-        s1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = slowest_rank_ms(s0.elapsed_time(s1) / K, dist, dev)
-        nbytes = x.numel() * x.element_size()
-        e2e = dict(value=round(job_tokens_per_s(shape.N, world, e2e_ms), 1), unit="tokens/s",
-                   ms_per_step=round(e2e_ms, 4), h2d_bytes_per_step=nbytes,
-                   d2h_bytes_per_step=out.numel() * out.element_size(),
-                   overlap="uploads and downloads on their own streams, double buffered")
-
-    peaks, source = load_peaks()
-    dom = max(("gate_up", "down", "route", "permute", "combine"), key=lambda n: stage_ms[n])
-    roof = roofline_entry(work[dom], stage_ms[dom], peaks, source, shape.dtype)
-    roof = dict(kernel=dom, **roof, traffic=measured_traffic(shape.name, dom))
-    per_stage = {n: dict(ms=round(stage_ms[n], 4),
-                         **{k: v for k, v in roofline_entry(work[n], max(stage_ms[n], 1e-6),
-                                                            peaks, source, shape.dtype).items()
-                            if k in ("bound", "achieved", "unit", "frac")})
-                 for n in moe.binding.STAGE_NAMES}
+    roof = dominant_roofline(shape, r["stage_ms"], counts)
+    per_stage = stage_rooflines(shape, r["stage_ms"], counts, moe.binding.STAGE_NAMES)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_from_device(shape, inp)
+        cpu = cpu_baseline_from_device(shape, L.inp, args.mode)
 
-    launches_per_step = 6   # route, scan/assign, permute, gate_up, down, combine
+    # the other forward rule on the same inputs, then the other workloads (one replica
+    # per GPU; skipped under torchrun, where only the headline line is compared)
+    others = None
+    if world == 1 and not args.no_workloads:
+        others = {}
+        other_mode = "mask_sum" if args.mode == "dispatch" else "dispatch"
+        M = Layer(moe, shape, other_mode, dev, seed=rank, inp=L.inp, packed=L.packed)
+        others[f"{shape.name}:{other_mode}"] = workload_entry(moe, args, M, dist, dev, stream,
+                                                             backward=False)
+        del M, L
+        torch.cuda.empty_cache()
+        for extra in EXTRA_WORKLOADS:
+            if extra.name == shape.name:
+                continue
+            X = Layer(moe, extra, "dispatch", dev, seed=rank)
+            others[extra.name] = workload_entry(moe, args, X, dist, dev, stream,
+                                                backward=not args.no_backward)
+            del X
+            torch.cuda.empty_cache()
+
     if rank == 0:
         line = dict(metric=METRIC, value=round(value, 1), unit="tokens/s", n_gpus=world,
                     steps=args.steps, warmup=args.warmup, ms_per_step=round(ms_step, 4),
                     higher_is_better=True, scaling="weak", vs_baseline=None, dtype=shape.dtype,
-                    data="synthetic (seeded; x~N(0,1), router~U(+-1/sqrt(H)), experts~N(0,0.02))",
-                    config=dict(workload_config(shape), mode=args.mode,
-                                parallelism=f"replicas x{world} (one layer per GPU)"),
+                    data=DATA, config=run_config(shape, args.mode, world),
                     roofline=roof, stages=per_stage, cpu_baseline=cpu, e2e=e2e,
-                    gpu_launches=launches_per_step * args.steps, clocks=clk.summary(),
-                    kept_pairs=int(counts.sum()), load=load, backward=backward, variants=variants,
-                    impl="b300")
+                    gpu_launches=FORWARD_LAUNCHES * args.steps, clocks=r["clocks"],
+                    kept_pairs=int(counts.sum()), load=load_summary(shape, r["routed"], counts),
+                    backward=backward, variants=variants, workloads=others, impl="b300")
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -1,7 +1,8 @@
 """The benchmark's host arithmetic, on CPU: algorithmic work per stage (closed forms of
-the SURVEY-style byte and flop counts on a hand-checked shape), the roofline's choice of
+each stage's byte and flop counts on a hand-checked shape), the roofline's choice of
 bound and fraction, the traffic record's guard on the GEMM sources, whole-job
-throughput, and the load summary."""
+throughput, the load summary, and the CPU legs (one-thread pinning, token sample,
+the same config in both arms)."""
 import json
 import math
 
@@ -79,3 +80,57 @@ def test_load_summary():
     assert (s["expert_max"], s["expert_min"], s["expert_mean"]) == (7, 3, 5.0)
     assert (s["partition_max"], s["partition_min"]) == (10, 10)
     assert s["routed_pairs"] == 20 and s["dropped_pairs"] == 3
+
+
+def test_cpu_legs_run_on_one_thread():
+    from threadpoolctl import threadpool_info
+    with bench.SingleThread() as st:
+        assert st.threads == 1
+        assert all(int(i.get("num_threads", 1)) == 1 for i in threadpool_info())
+    info = bench.host_cpu()
+    assert info["logical_cores"] == __import__("os").cpu_count()
+
+
+def test_cpu_legs_pin_openblas_without_threadpoolctl(monkeypatch):
+    # hosts without threadpoolctl: the limit is set and read back through OpenBLAS's API
+    import sys
+    monkeypatch.setitem(sys.modules, "threadpoolctl", None)
+    libs = bench._openblas_libs()
+    if not any(bench._blas_fn(lib, "get") for lib in libs):
+        pytest.skip("numpy here is not linked against OpenBLAS")
+    with bench.SingleThread() as st:
+        assert st.threads == 1 and "openblas" in st.pools[0]
+
+
+def test_cpu_sample_tokens_is_a_flop_budget():
+    # about 2e11 expert flops: 6 k H I per token
+    g = workloads.GPTOSS
+    assert bench.cpu_sample_tokens(g) == int(2e11 // (6 * 4 * 2880 * 2880)) == 1004
+    assert bench.cpu_sample_tokens(workloads.DECODE) == 128          # the whole batch
+    assert 1 <= bench.cpu_sample_tokens(workloads.E8_TOP2) < workloads.E8_TOP2.N
+
+
+def test_oracle_slice_is_a_layer_call_of_its_own():
+    import oracle
+    shape = workloads.LayerShape("slice", N=96, H=16, I=8, E=4, top_k=2, ep_size=2,
+                                 capacity_factor=1.0)
+    inp = workloads.layer_inputs(shape, seed=3, variant="perf")
+    f = lambda t: None if t is None else t.double().numpy()
+    x, wr = f(inp["x"]), f(inp["w_router"])
+    W = {k: f(inp[k]) for k in ("w_gate", "w_up", "w_down")}
+    t, det = bench.time_oracle_slice(shape, x, wr, None,
+                                     lambda e: (W["w_gate"][e], W["w_up"][e], W["w_down"][e]),
+                                     32, 40)
+    assert t > 0 and det["tokens"] == 40
+    # the slice's capacity is its own: ceil(1.0 * 40 * 2 / 4) = 20 per expert
+    ref = oracle.layer_forward(x[32:72], wr, None, W["w_gate"], W["w_up"], W["w_down"],
+                               2, 2, capacity_factor=1.0)
+    assert det["kept_pairs"] == int(ref["expert_offsets"][-1])
+    assert det["busy_experts"] == int((ref["counts"] > 0).sum())
+
+
+def test_both_arms_share_one_config():
+    c1 = bench.run_config(workloads.GPTOSS, "dispatch", 1)
+    c2 = bench.run_config(workloads.GPTOSS, "dispatch", 1)
+    assert c1 == c2 and c1["workload"] == workloads.GPTOSS.name
+    assert c1["mode"] == "dispatch" and "parallelism" in c1
