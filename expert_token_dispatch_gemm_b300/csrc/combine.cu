@@ -94,40 +94,65 @@ mask_sum_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
     uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)t * H);
     const unsigned live = __ballot_sync(0xffffffffu, owner >= 0);
     if (k <= 8) {
-        // every kept slot of a vector is loaded before the ordered partition sums
+        // Once per token: the kept slots in (partition, slot) order, packed four bits per
+        // entry, and a bit at every position that ends a partition's run. Each vector
+        // then runs one fixed sequence of adds: the slots in that order into the
+        // partition's partial, which is added to the sum where its run ends -- the same
+        // additions, in the same order, as summing each partition and then the partials.
         int own[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) own[j] = __shfl_sync(0xffffffffu, owner, j);
-        for (int v = lane; v < nvec; v += 32) {
-            uint4 r[8];
+        uint32_t order = 0, ends = 0;
+        int nk = 0;
+        unsigned todo = live & ((1u << k) - 1u);
+        while (todo) {
+            int pmin = 0x7fffffff;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                r[j] = (j < k && own[j] >= 0) ? __ldg(src + (size_t)j * nvec + v) : make_uint4(0, 0, 0, 0);
-            float acc[V::N];
+                if ((todo >> j) & 1u) pmin = own[j] < pmin ? own[j] : pmin;
 #pragma unroll
-            for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
-            unsigned todo = live & ((1u << k) - 1u);
-            while (todo) {
-                int pmin = 0x7fffffff;
+            for (int j = 0; j < 8; ++j)
+                if (((todo >> j) & 1u) && own[j] == pmin) {
+                    order |= (uint32_t)j << (4 * nk);
+                    ++nk;
+                    todo &= ~(1u << j);
+                }
+            ends |= 1u << (nk - 1);
+        }
+        constexpr int VU = 2;   // vectors per lane per step: 2 nk loads in flight
+        for (int v0 = lane; v0 < nvec; v0 += 32 * VU) {
+            uint4 r[8][VU];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if ((todo >> j) & 1u) pmin = own[j] < pmin ? own[j] : pmin;
-                float part[V::N];
+            for (int s = 0; s < 8; ++s)
 #pragma unroll
-                for (int i = 0; i < V::N; ++i) part[i] = 0.f;
+                for (int w = 0; w < VU; ++w) {
+                    const int v = v0 + 32 * w;
+                    const int j = (int)((order >> (4 * s)) & 15u);
+                    r[s][w] = (s < nk && v < nvec) ? __ldg(src + (size_t)j * nvec + v)
+                                                    : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (((todo >> j) & 1u) && own[j] == pmin) {
+            for (int w = 0; w < VU; ++w) {
+                float acc[V::N], part[V::N];
+#pragma unroll
+                for (int i = 0; i < V::N; ++i) acc[i] = part[i] = 0.f;
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    if (s < nk) {
                         float f[V::N];
-                        V::to_float(r[j], f);
+                        V::to_float(r[s][w], f);
 #pragma unroll
                         for (int i = 0; i < V::N; ++i) part[i] += f[i];
-                        todo &= ~(1u << j);
-                    }
+                        if ((ends >> s) & 1u) {
 #pragma unroll
-                for (int i = 0; i < V::N; ++i) acc[i] += part[i];
+                            for (int i = 0; i < V::N; ++i) {
+                                acc[i] += part[i];
+                                part[i] = 0.f;
+                            }
+                        }
+                    }
+                if (v0 + 32 * w < nvec) dst[v0 + 32 * w] = V::from_float(acc);
             }
-            dst[v] = V::from_float(acc);
         }
         return;
     }

@@ -5,14 +5,23 @@
 // the lower expert id), applies the softmax over the k chosen logits and adds the
 // token's experts to the per-segment histogram that the dispatch scan consumes.
 //
-// One CTA per 128-token tile. The top-k runs over column slices: with SLICES groups of
-// four epilogue warps, group g selects each token's top-k among its slice of the experts
-// and group 0 merges the other groups' lists in expert order, which keeps the ordering
-// (value descending, ties to the lower id).
+// One CTA per 128-token tile, or (KSPLIT = 2, when there are fewer tiles than SMs) a
+// cluster of two CTAs per tile that split the hidden dimension: CTA r accumulates the
+// partial logits of K blocks [r * ceil(kb/2), ...) for all 128 tokens, keeps the 64
+// tokens of histogram segment 2 * tile + r and sends its partials of the other 64 rows to
+// the peer's shared memory (st.shared::cluster, then a release arrive on the peer's
+// mbarrier). Each CTA adds own + received partials (fp32 addition commutes, so both see
+// the same sums) and finishes the top-k of its 64 tokens. Twice the SMs stream x.
+// The top-k runs over column slices: with SLICES groups of four epilogue warps, group g
+// selects each token's top-k among its slice of the experts and group 0 merges the other
+// groups' lists in expert order, which keeps the ordering (value descending, ties to the
+// lower id).
 //
 // Per CTA (64 + 128 * SLICES threads, one tile):
 //   warp 0      TMA producer: 128x64 x tile + round16(E) x 64 router tile per stage,
-//               128-byte swizzle, 3-stage ring guarded by full/empty mbarriers;
+//               128-byte swizzle, a ring of 2..8 stages (as many as the shared memory
+//               left to the CTA holds: the copies in flight per SM set the streaming
+//               rate) guarded by full/empty mbarriers;
 //   warp 1      allocates TMEM (round16(E) columns, at least 32) and one thread issues
 //               tcgen05.mma (M=128, N=round16(E), K=16, bf16 in, fp32 acc);
 //   warps 2..   epilogue: tcgen05.ld of the logits of their TMEM lane quarter and
@@ -23,6 +32,7 @@
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
 // MOE_DEV_TIMEOUT in the status word, skips the remaining work, waits (bounded) for its
 // own copies, frees TMEM and returns.
+#include <algorithm>
 #include <mutex>
 
 #include "sm100.cuh"
@@ -33,7 +43,7 @@ namespace {
 using namespace tc;
 
 constexpr int BM = kTcBlockM;   // 128 tokens per tile
-constexpr int STAGES = 3;
+constexpr int MAX_STAGES = 8;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 static_assert(BM == 2 * kSegTokens, "a route tile covers two histogram segments");
 
@@ -45,6 +55,8 @@ enum { ROUTE_PLAIN = 0, ROUTE_SELBIAS = 1, ROUTE_GROUP = 2 };
 struct RouteParams {
     int rows;                // tokens
     int bn;                  // MMA N (E rounded up to 16)
+    int stages;              // ring depth, 2..MAX_STAGES
+    int kb_half;             // KSPLIT = 2: K blocks of CTA 0 (CTA 1 takes the rest)
     uint32_t idesc;
     int num_kb;              // K blocks of BK
     uint32_t tmem_cols;
@@ -59,20 +71,29 @@ struct RouteParams {
     int32_t *status;         // or nullptr
 };
 
-// Shared-memory layout for a given MMA N.
+// Shared-memory layout for a given MMA N and ring depth.
+// KSPLIT = 2 adds the receive buffer of the peer's partial logits, [bn / 4][64 rows][4]
+// fp32 (a warp's 32 rows of 4 columns are 512 contiguous bytes), and its mbarrier.
 struct RouteSmem {
-    uint32_t b_off, bar_off, misc_off, bias_off, sbias_off, hist_off, alloc;
+    uint32_t b_off, recv_off, bar_off, misc_off, bias_off, sbias_off, hist_off, alloc;
 };
-__host__ __device__ inline RouteSmem route_smem(int bn, int E) {
+__host__ __device__ inline RouteSmem route_smem(int bn, int E, int stages, int ksplit) {
     RouteSmem m;
-    m.b_off = STAGES * A_BYTES;
-    m.bar_off = m.b_off + STAGES * (uint32_t)bn * BK * 2;
-    m.misc_off = m.bar_off + 16 * 8;
+    m.b_off = (uint32_t)stages * A_BYTES;
+    m.recv_off = m.b_off + (uint32_t)stages * (uint32_t)bn * BK * 2;
+    m.bar_off = m.recv_off + (ksplit == 2 ? 64u * (uint32_t)bn * 4u : 0u);
+    m.misc_off = m.bar_off + (2 * MAX_STAGES + 2) * 8;
     m.bias_off = m.misc_off + 16;
     m.sbias_off = m.bias_off + (uint32_t)(E + 3) / 4 * 16;
     m.hist_off = m.sbias_off + (uint32_t)(E + 3) / 4 * 16;
     m.alloc = m.hist_off + 2 * (uint32_t)E * 4 + 1024;   // + slack to align the base
     return m;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
 }
 
 template <int KMAX>
@@ -116,19 +137,23 @@ __device__ __forceinline__ void topk_push_raw(float (&val)[KMAX], float (&raw)[K
     }
 }
 
-template <int KMAX, int SLICES, int MODE>
-__global__ void __launch_bounds__(64 + 128 * SLICES, 1)
+// SLICES = 2 runs two CTAs per SM: at most 102 registers per thread
+template <int KMAX, int SLICES, int MODE, int KSPLIT>
+__global__ void __launch_bounds__(64 + 128 * SLICES, SLICES == 2 ? 2 : 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w, const RouteParams p) {
     constexpr int NT = 128 * SLICES;   // epilogue threads
+    static_assert(KSPLIT == 1 || (KSPLIT == 2 && MODE != ROUTE_GROUP), "split routing modes");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const RouteSmem L = route_smem(p.bn, p.E);
+    const RouteSmem L = route_smem(p.bn, p.E, p.stages, KSPLIT);
+    const int STAGES = p.stages;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     uint64_t *full = bars;                  // [STAGES]
     uint64_t *empty = bars + STAGES;        // [STAGES]
     uint64_t *tfull = bars + 2 * STAGES;    // [1]
+    uint64_t *recv_full = tfull + 1;        // [1] KSPLIT = 2: the peer's partials landed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.misc_off);
     volatile int *abort_s = reinterpret_cast<volatile int *>(smem + L.misc_off + 4);
     float *bias_s = reinterpret_cast<float *>(smem + L.bias_off);
@@ -136,7 +161,11 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     int *hist_s = reinterpret_cast<int *>(smem + L.hist_off);   // [2][E]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int tile = blockIdx.x;
+    const int tile = KSPLIT == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const uint32_t crank = KSPLIT == 2 ? cluster_ctarank() : 0u;
+    // this CTA's K blocks
+    const int kb0 = KSPLIT == 2 && crank == 1 ? p.kb_half : 0;
+    const int kb1 = KSPLIT == 2 && crank == 0 ? p.kb_half : p.num_kb;
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tmap_x);
@@ -154,6 +183,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
             mbar_init(&empty[s], 1);
         }
         mbar_init(tfull, 1);
+        if (KSPLIT == 2) mbar_init(recv_full, 64 * SLICES);   // every sending thread
         *abort_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -168,6 +198,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
     fence_before();
     __syncthreads();
+    if (KSPLIT == 2) cluster_sync_all();   // the peer's barriers exist before any arrival
     fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -176,7 +207,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
             int stage = 0;
             uint32_t phase = 0, armed = 0, armed_parity = 0;
             const uint32_t tx = A_BYTES + (uint32_t)p.bn * BK * 2;
-            for (int kb = 0; kb < p.num_kb; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_s, p.status)) break;
                 mbar_arrive_expect_tx(&full[stage], tx);
                 const uint32_t fb = smem_u32(&full[stage]);
@@ -201,7 +232,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         if (lane == 0) {   // ------------------------------------------ MMA issuer
             int stage = 0;
             uint32_t phase = 0;
-            for (int kb = 0; kb < p.num_kb; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(&full[stage], phase, abort_s, p.status)) break;
                 fence_after();
                 const uint32_t a_addr = smem_u32(smem + stage * A_BYTES);
@@ -209,7 +240,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
                     mma_bf16(tmem_base, smem_desc_sw128(a_addr + kk * 32),
-                             smem_desc_sw128(b_addr + kk * 32), p.idesc, (kb | kk) != 0);
+                             smem_desc_sw128(b_addr + kk * 32), p.idesc, ((kb - kb0) | kk) != 0);
                 commit(&empty[stage]);
                 if (++stage == STAGES) {
                     stage = 0;
@@ -226,10 +257,35 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
         const int r = q * 32 + lane;           // accumulator row = token of the tile
         const int tok = tile * BM + r;
         const int etid = threadIdx.x - 64;     // 0 .. NT-1
+        // KSPLIT = 2: rows 64 crank .. 64 crank + 63 are this CTA's; its other rows' partials
+        // go to the peer
+        const bool own = KSPLIT == 1 || (q >> 1) == (int)crank;
+        const int cps = (p.bn + 32 * SLICES - 1) / (32 * SLICES) * 32;   // columns per slice
+        const int cs0 = slice * cps, cs1 = min(p.bn, (slice + 1) * cps);
         // tcgen05.ld is warp-collective and the epilogue warps share named barriers:
         // all of them decide together
         const bool ok = epilogue_all<NT>(mbar_wait(tfull, 0, abort_s, p.status) && *abort_s == 0);
         fence_after();
+        if (KSPLIT == 2 && !own) {
+            // send this slice's partials of the peer's rows, then arrive on its barrier
+            // (also after an abort, so that the peer does not wait for them)
+            const uint32_t peer = crank ^ 1u;
+            const int prow = (q & 1) * 32 + lane;   // row inside the peer's 64
+            if (ok) {
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
+                const uint32_t recv = mapa_shared(smem_u32(smem + L.recv_off), peer);
+                for (int c = cs0; c < cs1; c += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        if (c + j < p.bn)
+                            st_cluster_v4(recv + ((uint32_t)((c + j) >> 2) * 64u + (uint32_t)prow) * 16u,
+                                          v[j], v[j + 1], v[j + 2], v[j + 3]);
+                }
+            }
+            mbar_arrive_cluster(mapa_shared(smem_u32(recv_full), peer));
+        }
         float val[KMAX], raw[KMAX];   // raw: the entry's logit (MODE > ROUTE_PLAIN)
         int idx[KMAX];
 #pragma unroll
@@ -264,9 +320,28 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 for (int j = 0; j < 32 && c + j < p.E; ++j) dst[j] = v[j] + bias_s[c + j];
             }
         };
+        // the peer's partial logits of one of this CTA's rows, columns c .. c + 3
+        const int lrow = (q & 1) * 32 + lane;
+        auto add_recv = [&](float (&v)[32], int c) {
+            if constexpr (KSPLIT == 2) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    if (c + j < p.bn) {
+                        const float4 pv = *reinterpret_cast<const float4 *>(
+                            smem + L.recv_off + ((size_t)((c + j) >> 2) * 64 + lrow) * 16);
+                        v[j] += pv.x;
+                        v[j + 1] += pv.y;
+                        v[j + 2] += pv.z;
+                        v[j + 3] += pv.w;
+                    }
+            }
+        };
         if (ok) {
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
-            if (MODE == ROUTE_GROUP) {
+            if (KSPLIT == 2 && own) mbar_wait<true>(recv_full, 0, abort_s, p.status);
+            if (!own) {
+                // KSPLIT = 2: sent above; only the merge barriers remain
+            } else if (MODE == ROUTE_GROUP) {
                 // pass 1: every partition's best selection score, the best partitions
                 // in a list (pushed in increasing partition id: ties keep the lower)
                 float pv[kMaxGroupLimit];
@@ -313,11 +388,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     store_logits(v, c);
                 }
             } else {
-                const int cps = (p.bn + 32 * SLICES - 1) / (32 * SLICES) * 32;   // columns per slice
-                const int c1 = min(p.bn, (slice + 1) * cps);
-                for (int c = slice * cps; c < c1; c += 32) {
+                for (int c = cs0; c < cs1; c += 32) {
                     float v[32];
                     tmem_ld32(taddr + c, v);
+                    add_recv(v, c);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int e = c + j;
@@ -332,7 +406,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 float *lv = reinterpret_cast<float *>(smem);   // [SLICES-1][BM][KMAX]
                 float *lr = lv + (SLICES - 1) * BM * KMAX;
                 int *li = reinterpret_cast<int *>(lr + (SLICES - 1) * BM * KMAX);
-                if (slice > 0)
+                if (slice > 0 && own)
 #pragma unroll
                     for (int j = 0; j < KMAX; ++j) {
                         lv[((slice - 1) * BM + r) * KMAX + j] = val[j];
@@ -340,7 +414,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                         li[((slice - 1) * BM + r) * KMAX + j] = idx[j];
                     }
                 epilogue_sync<NT>();
-                if (slice == 0)
+                if (slice == 0 && own)
                     for (int g = 0; g < SLICES - 1; ++g)
 #pragma unroll
                         for (int j = 0; j < KMAX; ++j) {
@@ -353,7 +427,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                 topk_push_raw<KMAX>(val, raw, idx, lv[o], lr[o], e);
                         }
             }
-            if (slice == 0 && tok < p.rows) {
+            if (slice == 0 && own && tok < p.rows) {
                 // softmax over the chosen experts' logits
                 const float *lg = MODE == ROUTE_PLAIN ? val : raw;
                 float m = lg[0];
@@ -377,8 +451,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
             }
             if (p.seg_hist != nullptr) {
                 epilogue_sync<NT>();
+                // KSPLIT = 2: the CTA's own segment only (the peer writes the other)
                 for (int j = etid; j < 2 * p.E; j += NT) {
                     const int seg = 2 * tile + j / p.E;
+                    if (KSPLIT == 2 && j / p.E != (int)crank) continue;
                     if (seg < p.nseg) p.seg_hist[(size_t)seg * p.E + j % p.E] = hist_s[j];
                 }
             }
@@ -387,6 +463,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
 
     fence_before();
     __syncthreads();
+    if (KSPLIT == 2) cluster_sync_all();   // no CTA leaves while its peer may still write to it
     if (warp == 1) {
         fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -395,11 +472,30 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
 }
 
-template <int KMAX, int SLICES, int MODE>
+// Ring depth: as many stages as the shared memory of one CTA (SLICES = 4: one CTA per SM)
+// or of half an SM (SLICES <= 2: two per SM) holds, at least enough to stage the slices'
+// top-k lists for the merge; 0 when fewer than two stages fit.
+int ring_stages(int bn, int E, int slices, int kmax, int ksplit) {
+    const uint32_t limit = (slices == 4 ? 227u : 113u) * 1024u;
+    const uint32_t fixed = route_smem(bn, E, 0, ksplit).alloc;
+    if (fixed >= limit) return 0;
+    const uint32_t stage_bytes = A_BYTES + (uint32_t)bn * BK * 2;
+    const int lists = (slices - 1) * BM * kmax * 12;
+    int st = (int)std::min<uint32_t>(MAX_STAGES, (limit - fixed) / stage_bytes);
+    while (st * (int)stage_bytes < lists) ++st;
+    if (st < 2 || st > MAX_STAGES || route_smem(bn, E, st, ksplit).alloc > limit) return 0;
+    return st;
+}
+
+template <int KMAX, int SLICES, int MODE, int KSPLIT>
 cudaError_t launch_route_tc(const CUtensorMap &mx, const CUtensorMap &mw, const RouteParams &prm,
                             int tiles, cudaStream_t s) {
-    auto kern = route_tc_kernel<KMAX, SLICES, MODE>;
-    const RouteSmem L = route_smem(prm.bn, prm.E);
+    auto kern = route_tc_kernel<KMAX, SLICES, MODE, KSPLIT>;
+    RouteParams p = prm;
+    p.kb_half = (p.num_kb + 1) / 2;
+    p.stages = ring_stages(p.bn, p.E, SLICES, KMAX, KSPLIT);
+    if (p.stages == 0) return cudaErrorInvalidConfiguration;
+    const RouteSmem L = route_smem(p.bn, p.E, p.stages, KSPLIT);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -416,28 +512,58 @@ cudaError_t launch_route_tc(const CUtensorMap &mx, const CUtensorMap &mw, const 
             attr_max[dev] = L.alloc;
         }
     }
-    return launch_pdl(kern, dim3(tiles), dim3(64 + 128 * SLICES), L.alloc, s, mx, mw, prm);
+    if (KSPLIT == 1)
+        return launch_pdl(kern, dim3(tiles), dim3(64 + 128 * SLICES), L.alloc, s, mx, mw, p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(2 * tiles, 1, 1);
+    cfg.blockDim = dim3(64 + 128 * SLICES, 1, 1);
+    cfg.dynamicSmemBytes = L.alloc;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, mx, mw, p);
 }
 
-// Four column slices while one CTA per SM covers every tile, two otherwise (two CTAs of
-// 320 threads fit on an SM); lists longer than 8 are not sliced.
+// Tiles fewer than the SMs: split the hidden dimension over a cluster of two CTAs per tile
+// (at least two K blocks); four column slices while one CTA per SM covers every CTA, two
+// otherwise (two CTAs of 320 threads fit on an SM). Lists longer than 8, and the
+// group-limited routing, run one unsplit, unsliced CTA per tile.
 template <int KMAX>
 cudaError_t launch_route_k(const CUtensorMap &mx, const CUtensorMap &mw, const RouteParams &prm,
                            int tiles, int num_sms, cudaStream_t s) {
     if (tiles <= 0) return cudaSuccess;
-    if (prm.group_limit > 0) return launch_route_tc<KMAX, 1, ROUTE_GROUP>(mx, mw, prm, tiles, s);
+    if (prm.group_limit > 0) return launch_route_tc<KMAX, 1, ROUTE_GROUP, 1>(mx, mw, prm, tiles, s);
     if constexpr (KMAX > 8) {
         (void)num_sms;
         if (prm.sel_bias != nullptr)
-            return launch_route_tc<KMAX, 1, ROUTE_SELBIAS>(mx, mw, prm, tiles, s);
-        return launch_route_tc<KMAX, 1, ROUTE_PLAIN>(mx, mw, prm, tiles, s);
+            return launch_route_tc<KMAX, 1, ROUTE_SELBIAS, 1>(mx, mw, prm, tiles, s);
+        return launch_route_tc<KMAX, 1, ROUTE_PLAIN, 1>(mx, mw, prm, tiles, s);
     } else {
-        const bool wide = tiles <= num_sms;
-        if (prm.sel_bias != nullptr)
-            return wide ? launch_route_tc<KMAX, 4, ROUTE_SELBIAS>(mx, mw, prm, tiles, s)
-                        : launch_route_tc<KMAX, 2, ROUTE_SELBIAS>(mx, mw, prm, tiles, s);
-        return wide ? launch_route_tc<KMAX, 4, ROUTE_PLAIN>(mx, mw, prm, tiles, s)
-                    : launch_route_tc<KMAX, 2, ROUTE_PLAIN>(mx, mw, prm, tiles, s);
+        const bool wide_split = 2 * tiles <= num_sms;
+        const bool split = tiles < num_sms && prm.num_kb >= 2 &&
+                           ring_stages(prm.bn, prm.E, wide_split ? 4 : 2, KMAX, 2) > 0;
+        const int ctas = split ? 2 * tiles : tiles;
+        const bool wide = ctas <= num_sms;
+        const bool sb = prm.sel_bias != nullptr;
+        if (split) {
+            if (sb)
+                return wide ? launch_route_tc<KMAX, 4, ROUTE_SELBIAS, 2>(mx, mw, prm, tiles, s)
+                            : launch_route_tc<KMAX, 2, ROUTE_SELBIAS, 2>(mx, mw, prm, tiles, s);
+            return wide ? launch_route_tc<KMAX, 4, ROUTE_PLAIN, 2>(mx, mw, prm, tiles, s)
+                        : launch_route_tc<KMAX, 2, ROUTE_PLAIN, 2>(mx, mw, prm, tiles, s);
+        }
+        if (sb)
+            return wide ? launch_route_tc<KMAX, 4, ROUTE_SELBIAS, 1>(mx, mw, prm, tiles, s)
+                        : launch_route_tc<KMAX, 2, ROUTE_SELBIAS, 1>(mx, mw, prm, tiles, s);
+        return wide ? launch_route_tc<KMAX, 4, ROUTE_PLAIN, 1>(mx, mw, prm, tiles, s)
+                    : launch_route_tc<KMAX, 2, ROUTE_PLAIN, 1>(mx, mw, prm, tiles, s);
     }
 }
 
