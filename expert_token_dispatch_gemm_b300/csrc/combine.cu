@@ -73,6 +73,87 @@ combine_kernel(const T *__restrict__ slots, const int32_t *__restrict__ slot_pos
 // Mask-and-sum: partition p's partial output of token t is the fp32 sum, in slot order,
 // of the slots whose expert partition p owns (the other partitions' experts are masked
 // out); the partials are then added in partition order. Partials stay in registers.
+//
+// k <= KS (4 or 8): once per token, the kept slots in (partition, slot) order, packed four
+// bits per entry, and a bit at every position that ends a partition's run. Each vector
+// then runs one fixed sequence of adds: the slots in that order into the partition's
+// partial, which is added to the sum where its run ends -- the same additions, in the
+// same order, as summing each partition and then the partials. KS * VU loads are in
+// flight per lane; four blocks of 256 threads fit on an SM.
+template <typename T, int KS>
+__global__ void __launch_bounds__(256, 4)
+mask_sum_small_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
+                      const int32_t *__restrict__ slot_pos, int N, int k, int H, int E, int P,
+                      T *__restrict__ out) {
+    grid_dep_wait();
+    grid_dep_trigger();
+    using V = Vec16<T>;
+    constexpr int VU = KS == 4 ? 2 : 1;   // vectors per lane per step
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= N) return;
+    const int per_part = E / P;
+    int owner = -1;
+    if (lane < k && slot_pos[(size_t)t * k + lane] >= 0) owner = idx[(size_t)t * k + lane] / per_part;
+    const int nvec = H / V::N;
+    const uint4 *src = reinterpret_cast<const uint4 *>(slots + (size_t)t * k * H);
+    uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)t * H);
+    // partitions that own at least one kept slot of this token, in increasing order; an
+    // empty partition's partial is 0 and adding it leaves the sum unchanged
+    unsigned todo = __ballot_sync(0xffffffffu, owner >= 0) & ((1u << k) - 1u);
+    uint32_t order = 0, ends = 0;
+    int nk = 0;
+    while (todo) {
+        int pmin = 0x7fffffff;
+        for (unsigned m = todo; m; m &= m - 1) {
+            const int o = __shfl_sync(0xffffffffu, owner, __ffs(m) - 1);
+            pmin = o < pmin ? o : pmin;
+        }
+        const unsigned mine = __ballot_sync(0xffffffffu, owner == pmin) & todo;
+        for (unsigned m = mine; m; m &= m - 1) {
+            order |= (uint32_t)(__ffs(m) - 1) << (4 * nk);
+            ++nk;
+        }
+        ends |= 1u << (nk - 1);
+        todo &= ~mine;
+    }
+    for (int v0 = lane; v0 < nvec; v0 += 32 * VU) {
+        uint4 r[KS][VU];
+#pragma unroll
+        for (int s = 0; s < KS; ++s)
+#pragma unroll
+            for (int w = 0; w < VU; ++w) {
+                const int v = v0 + 32 * w;
+                const int j = (int)((order >> (4 * s)) & 15u);
+                r[s][w] = (s < nk && v < nvec) ? __ldg(src + (size_t)j * nvec + v)
+                                                : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+        for (int w = 0; w < VU; ++w) {
+            float acc[V::N], part[V::N];
+#pragma unroll
+            for (int i = 0; i < V::N; ++i) acc[i] = part[i] = 0.f;
+#pragma unroll
+            for (int s = 0; s < KS; ++s)
+                if (s < nk) {
+                    float f[V::N];
+                    V::to_float(r[s][w], f);
+#pragma unroll
+                    for (int i = 0; i < V::N; ++i) part[i] += f[i];
+                    if ((ends >> s) & 1u) {
+#pragma unroll
+                        for (int i = 0; i < V::N; ++i) {
+                            acc[i] += part[i];
+                            part[i] = 0.f;
+                        }
+                    }
+                }
+            if (v0 + 32 * w < nvec) dst[v0 + 32 * w] = V::from_float(acc);
+        }
+    }
+}
+
+// k > 8: the same sums, with each partition's slots found per vector.
 template <typename T>
 __global__ void __launch_bounds__(256)
 mask_sum_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
@@ -87,75 +168,9 @@ mask_sum_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
     const int per_part = E / P;
     int owner = -1;
     if (lane < k && slot_pos[(size_t)t * k + lane] >= 0) owner = idx[(size_t)t * k + lane] / per_part;
-    // partitions that own at least one kept slot of this token, in increasing order; an
-    // empty partition's partial is 0 and adding it leaves the sum unchanged
     const int nvec = H / V::N;
     const uint4 *src = reinterpret_cast<const uint4 *>(slots + (size_t)t * k * H);
     uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)t * H);
-    const unsigned live = __ballot_sync(0xffffffffu, owner >= 0);
-    if (k <= 8) {
-        // Once per token: the kept slots in (partition, slot) order, packed four bits per
-        // entry, and a bit at every position that ends a partition's run. Each vector
-        // then runs one fixed sequence of adds: the slots in that order into the
-        // partition's partial, which is added to the sum where its run ends -- the same
-        // additions, in the same order, as summing each partition and then the partials.
-        int own[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) own[j] = __shfl_sync(0xffffffffu, owner, j);
-        uint32_t order = 0, ends = 0;
-        int nk = 0;
-        unsigned todo = live & ((1u << k) - 1u);
-        while (todo) {
-            int pmin = 0x7fffffff;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if ((todo >> j) & 1u) pmin = own[j] < pmin ? own[j] : pmin;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (((todo >> j) & 1u) && own[j] == pmin) {
-                    order |= (uint32_t)j << (4 * nk);
-                    ++nk;
-                    todo &= ~(1u << j);
-                }
-            ends |= 1u << (nk - 1);
-        }
-        constexpr int VU = 2;   // vectors per lane per step: 2 nk loads in flight
-        for (int v0 = lane; v0 < nvec; v0 += 32 * VU) {
-            uint4 r[8][VU];
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-#pragma unroll
-                for (int w = 0; w < VU; ++w) {
-                    const int v = v0 + 32 * w;
-                    const int j = (int)((order >> (4 * s)) & 15u);
-                    r[s][w] = (s < nk && v < nvec) ? __ldg(src + (size_t)j * nvec + v)
-                                                    : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-            for (int w = 0; w < VU; ++w) {
-                float acc[V::N], part[V::N];
-#pragma unroll
-                for (int i = 0; i < V::N; ++i) acc[i] = part[i] = 0.f;
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    if (s < nk) {
-                        float f[V::N];
-                        V::to_float(r[s][w], f);
-#pragma unroll
-                        for (int i = 0; i < V::N; ++i) part[i] += f[i];
-                        if ((ends >> s) & 1u) {
-#pragma unroll
-                            for (int i = 0; i < V::N; ++i) {
-                                acc[i] += part[i];
-                                part[i] = 0.f;
-                            }
-                        }
-                    }
-                if (v0 + 32 * w < nvec) dst[v0 + 32 * w] = V::from_float(acc);
-            }
-        }
-        return;
-    }
     for (int v = lane; v < nvec; v += 32) {
         float acc[V::N];
 #pragma unroll
@@ -225,15 +240,26 @@ cudaError_t launch_combine(const LayerDims &d, const void *out_slots, const int3
                       slot_pos, d.N, d.k, d.H, (float *)out);
 }
 
+template <typename T>
+cudaError_t launch_mask_sum_t(const LayerDims &d, const T *out_slots, const int32_t *topk_idx,
+                              const int32_t *slot_pos, T *out, cudaStream_t s) {
+    const int grid = ceil_div(d.N, 8);
+    if (d.k <= 4)
+        return launch_pdl(mask_sum_small_kernel<T, 4>, dim3(grid), dim3(256), 0, s, out_slots,
+                          topk_idx, slot_pos, d.N, d.k, d.H, d.E, d.P, out);
+    if (d.k <= 8)
+        return launch_pdl(mask_sum_small_kernel<T, 8>, dim3(grid), dim3(256), 0, s, out_slots,
+                          topk_idx, slot_pos, d.N, d.k, d.H, d.E, d.P, out);
+    return launch_pdl(mask_sum_kernel<T>, dim3(grid), dim3(256), 0, s, out_slots, topk_idx,
+                      slot_pos, d.N, d.k, d.H, d.E, d.P, out);
+}
+
 cudaError_t launch_mask_sum(const LayerDims &d, const void *out_slots, const int32_t *topk_idx,
                             const int32_t *slot_pos, void *out, cudaStream_t s) {
-    const int grid = ceil_div(d.N, 8);
     if (d.dtype == MOE_DTYPE_BF16)
-        return launch_pdl(mask_sum_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s,
-                          (const __nv_bfloat16 *)out_slots, topk_idx, slot_pos, d.N, d.k, d.H, d.E,
-                          d.P, (__nv_bfloat16 *)out);
-    return launch_pdl(mask_sum_kernel<float>, dim3(grid), dim3(256), 0, s, (const float *)out_slots,
-                      topk_idx, slot_pos, d.N, d.k, d.H, d.E, d.P, (float *)out);
+        return launch_mask_sum_t(d, (const __nv_bfloat16 *)out_slots, topk_idx, slot_pos,
+                                 (__nv_bfloat16 *)out, s);
+    return launch_mask_sum_t(d, (const float *)out_slots, topk_idx, slot_pos, (float *)out, s);
 }
 
 cudaError_t launch_pack_gate_up(const LayerDims &d, const void *w_gate, const void *w_up,

@@ -317,7 +317,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                         make_float4(v[j] + bias_s[c + j], v[j + 1] + bias_s[c + j + 1],
                                     v[j + 2] + bias_s[c + j + 2], v[j + 3] + bias_s[c + j + 3]);
             } else {
-                for (int j = 0; j < 32 && c + j < p.E; ++j) dst[j] = v[j] + bias_s[c + j];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (c + j < p.E) dst[j] = v[j] + bias_s[c + j];
             }
         };
         // the peer's partial logits of one of this CTA's rows, columns c .. c + 3
@@ -429,7 +431,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
             }
             if (slice == 0 && own && tok < p.rows) {
                 // softmax over the chosen experts' logits
-                const float *lg = MODE == ROUTE_PLAIN ? val : raw;
+                float lg[KMAX];
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) lg[j] = MODE == ROUTE_PLAIN ? val[j] : raw[j];
                 float m = lg[0];
 #pragma unroll
                 for (int j = 1; j < KMAX; ++j)
