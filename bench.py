@@ -652,10 +652,15 @@ FORWARD_LAUNCHES = 6   # route, scan/assign, permute, gate_up, down, combine
 
 
 def time_forward(moe, L, steps, warmup, dist, dev, stream, clocks=True):
-    """`warmup` untimed steps, then `steps` timed forward steps between a barrier and a
-    synchronize on both sides (CUDA events on the launching stream; the library records
-    an event at every stage boundary). Returns the slowest rank's step time, the mean
-    stage times, the kept and routed counts and the clock record."""
+    """`warmup` untimed steps, then two timed passes of `steps` forward steps, each between
+    a barrier and a synchronize on both sides (CUDA events on the launching stream):
+      1. the layer calls alone -- the step time (an event between two kernels would
+         stop the next one from launching while the previous drains, so none is
+         recorded inside this pass);
+      2. the same calls with the library recording an event at every stage boundary --
+         each kernel's duration.
+    Returns the slowest rank's step time, the mean stage times, the kept and routed
+    counts and the clock record of pass 1."""
     shape = L.shape
     counts_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
     routed_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
@@ -668,7 +673,7 @@ def time_forward(moe, L, steps, warmup, dist, dev, stream, clocks=True):
         for e in row:
             e.record(stream)     # creates the handles before the library re-records them
     for _ in range(warmup):
-        L.forward(moe, None, evs[0])
+        L.forward(moe)
     torch.cuda.synchronize()
 
     def barrier():
@@ -685,18 +690,26 @@ def time_forward(moe, L, steps, warmup, dist, dev, stream, clocks=True):
         torch.cuda._sleep(2_000_000)
         start.record(stream)
         for i in range(steps):
-            L.forward(moe, None, evs[i])
+            L.forward(moe)
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
+    ms_step = slowest_rank_ms(start.elapsed_time(end) / steps, dist, dev)
+    # pass 2: stage boundaries
+    barrier()
+    torch.cuda._sleep(2_000_000)
+    for i in range(steps):
+        L.forward(moe, None, evs[i])
+    torch.cuda.synchronize()
+    barrier()
     stage_ms = {name: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)]))
                 for j, name in enumerate(moe.binding.STAGE_NAMES)}
+    staged_ms = float(np.mean([evs[i][0].elapsed_time(evs[i][nst]) for i in range(steps)]))
     flags = moe.moe_read_device_status(L.cfg, L.ws)
     if flags:
         raise RuntimeError(f"device status flags {flags} after the timed steps of {shape.name}")
-    ms_step = slowest_rank_ms(start.elapsed_time(end) / steps, dist, dev)
-    return dict(ms_step=ms_step, stage_ms=stage_ms, counts=counts, routed=routed,
-                clocks=clk.summary() if clocks else None)
+    return dict(ms_step=ms_step, stage_ms=stage_ms, staged_ms=staged_ms, counts=counts,
+                routed=routed, clocks=clk.summary() if clocks else None)
 
 
 def stage_rooflines(shape, stage_ms, counts, names):
@@ -785,6 +798,7 @@ def workload_entry(moe, args, L, dist, dev, stream, backward=True):
                  config=workload_config(shape),
                  roofline=dominant_roofline(shape, r["stage_ms"], r["counts"], with_traffic=False),
                  stages=stage_rooflines(shape, r["stage_ms"], r["counts"], stages),
+                 stage_pass_ms_per_step=round(r["staged_ms"], 4),
                  kept_pairs=int(r["counts"].sum()), load=load_summary(shape, r["routed"], r["counts"]),
                  clocks=r["clocks"], gpu_launches=FORWARD_LAUNCHES * args.steps)
     if shape.N <= 256:
@@ -878,7 +892,9 @@ def main():
                     steps=args.steps, warmup=args.warmup, ms_per_step=round(ms_step, 4),
                     higher_is_better=True, scaling="weak", vs_baseline=None, dtype=shape.dtype,
                     data=DATA, config=run_config(shape, args.mode, world),
-                    roofline=roof, stages=per_stage, cpu_baseline=cpu, e2e=e2e,
+                    roofline=roof, stages=per_stage,
+                    stage_pass_ms_per_step=round(r["staged_ms"], 4),
+                    cpu_baseline=cpu, e2e=e2e,
                     gpu_launches=FORWARD_LAUNCHES * args.steps, clocks=r["clocks"],
                     kept_pairs=int(counts.sum()), load=load_summary(shape, r["routed"], counts),
                     backward=backward, variants=variants, workloads=others, impl="b300")

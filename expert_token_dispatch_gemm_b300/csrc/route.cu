@@ -52,14 +52,51 @@ route_kernel(const T *__restrict__ x, const T *__restrict__ wr, const float *__r
 #pragma unroll
         for (int q = 0; q < RE; ++q) acc[r][q] = 0.f;
 
+    // Staging: every thread first issues all of its 16-byte loads of the chunk (x rows and
+    // router rows; H is a multiple of 8, so a vector lies wholly inside or outside H),
+    // then widens them into shared memory, so the loads' latencies overlap.
+    using V = Vec16<T>;
+    constexpr int XV = V::N;                               // elements per vector
+    constexpr int CV = KC / XV;                            // vectors per staged row
+    constexpr int XIT = TB * CV / kRouteThreads;           // x vectors per thread
+    constexpr int WIT = (EP * CV + kRouteThreads - 1) / kRouteThreads;
+    static_assert(TB * CV % kRouteThreads == 0, "x staging layout");
     for (int h0 = 0; h0 < H; h0 += KC) {
-        for (int i = tid; i < TB * KC; i += kRouteThreads) {
-            const int r = i / KC, c = i % KC, t = t0 + r, h = h0 + c;
-            xs[r * (KC + 1) + c] = (t < N && h < H) ? to_f32(x[(size_t)t * H + h]) : 0.f;
+        uint4 xr[XIT], wv[WIT];
+#pragma unroll
+        for (int u = 0; u < XIT; ++u) {
+            const int i = tid + u * kRouteThreads;
+            const int r = i / CV, c = (i % CV) * XV, t = t0 + r, h = h0 + c;
+            xr[u] = (t < N && h < H) ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * H + h))
+                                     : make_uint4(0u, 0u, 0u, 0u);
         }
-        for (int i = tid; i < EP * KC; i += kRouteThreads) {
-            const int r = i / KC, c = i % KC, h = h0 + c;
-            ws[r * (KC + 1) + c] = (r < E && h < H) ? to_f32(wr[(size_t)r * H + h]) : 0.f;
+#pragma unroll
+        for (int u = 0; u < WIT; ++u) {
+            const int i = tid + u * kRouteThreads;
+            const int r = i / CV, c = (i % CV) * XV, h = h0 + c;
+            wv[u] = (i < EP * CV && r < E && h < H)
+                        ? __ldg(reinterpret_cast<const uint4 *>(wr + (size_t)r * H + h))
+                        : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < XIT; ++u) {
+            const int i = tid + u * kRouteThreads;
+            const int r = i / CV, c = (i % CV) * XV;
+            float f[XV];
+            V::to_float(xr[u], f);
+#pragma unroll
+            for (int q = 0; q < XV; ++q) xs[r * (KC + 1) + c + q] = f[q];
+        }
+#pragma unroll
+        for (int u = 0; u < WIT; ++u) {
+            const int i = tid + u * kRouteThreads;
+            if (i < EP * CV) {
+                const int r = i / CV, c = (i % CV) * XV;
+                float f[XV];
+                V::to_float(wv[u], f);
+#pragma unroll
+                for (int q = 0; q < XV; ++q) ws[r * (KC + 1) + c + q] = f[q];
+            }
         }
         __syncthreads();
 #pragma unroll 4

@@ -137,6 +137,62 @@ __device__ __forceinline__ void topk_push_raw(float (&val)[KMAX], float (&raw)[K
     }
 }
 
+// Plain routing ranks candidates by (logit desc, expert id asc) through order-preserving
+// 32-bit keys: a NaN ranks as -inf, -0 as +0, and every real key is above 0, the key of
+// an empty candidate. A top-k is then k rounds of: the largest key (a max tree), the
+// lowest id among the candidates holding it (a min tree), that candidate cleared -- a
+// depth of log2(N) per round instead of one long chain of list insertions.
+__device__ __forceinline__ uint32_t rank_key(float v) {
+    if (isnan(v)) v = -INFINITY;
+    if (v == 0.0f) v = 0.0f;
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+template <int N>
+__device__ __forceinline__ uint32_t tree_max_u32(const uint32_t (&a)[N]) {
+    static_assert((N & (N - 1)) == 0, "power of two");
+    uint32_t t[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) t[j] = a[j];
+#pragma unroll
+    for (int w = N / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) t[j] = max(t[j], t[j + w]);
+    return t[0];
+}
+template <int N>
+__device__ __forceinline__ int tree_min_i32(const int (&a)[N]) {
+    int t[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) t[j] = a[j];
+#pragma unroll
+    for (int w = N / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) t[j] = min(t[j], t[j + w]);
+    return t[0];
+}
+// The KMAX best of N (key, id) candidates, in ranking order, into (ok, oi); the
+// candidates' keys are consumed. An entry with key 0 is empty (id -1).
+template <int N, int KMAX>
+__device__ __forceinline__ void top_by_key(uint32_t (&o)[N], const int (&id)[N], uint32_t (&ok)[KMAX],
+                                           int (&oi)[KMAX]) {
+#pragma unroll
+    for (int t = 0; t < KMAX; ++t) {
+        const uint32_t m = tree_max_u32<N>(o);
+        int c[N];
+#pragma unroll
+        for (int j = 0; j < N; ++j) c[j] = (o[j] == m) ? id[j] : 0x7fffffff;
+        const int bi = tree_min_i32<N>(c);
+#pragma unroll
+        for (int j = 0; j < N; ++j) o[j] = (id[j] == bi) ? 0u : o[j];
+        ok[t] = m;
+        oi[t] = m != 0u ? bi : -1;
+    }
+}
+
 // SLICES = 2 runs two CTAs per SM: at most 102 registers per thread
 template <int KMAX, int SLICES, int MODE, int KSPLIT>
 __global__ void __launch_bounds__(64 + 128 * SLICES, SLICES == 2 ? 2 : 1)
@@ -294,6 +350,16 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
             raw[j] = -INFINITY;
             idx[j] = -1;
         }
+        // plain routing with k <= 4 selects by rank keys; larger lists (whose key trees
+        // spill registers) and the routing variants by list insertion
+        constexpr bool KEYED = MODE == ROUTE_PLAIN && KMAX <= 4;
+        uint32_t kk[KMAX];
+        int ki[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            kk[j] = 0u;
+            ki[j] = -1;
+        }
         // a candidate: logit l = acc + bias, selection score l (+ selection bias); a NaN
         // ranks last
         auto push = [&](float acc, int e) {
@@ -389,6 +455,39 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     }
                     store_logits(v, c);
                 }
+            } else if (KEYED) {
+                // the slice's candidates 32 columns at a time: the chunk's best KMAX, then
+                // (after the first chunk) merged with the running list
+                for (int c = cs0; c < cs1; c += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+                    add_recv(v, c);
+                    store_logits(v, c);
+                    uint32_t o[32];
+                    int id[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        id[j] = c + j;
+                        o[j] = c + j < p.E ? rank_key(v[j] + bias_s[c + j]) : 0u;
+                    }
+                    if (c == cs0) {
+                        top_by_key<32, KMAX>(o, id, kk, ki);
+                    } else {
+                        uint32_t co[KMAX];
+                        int ci[KMAX];
+                        top_by_key<32, KMAX>(o, id, co, ci);
+                        uint32_t mo[2 * KMAX];
+                        int mi[2 * KMAX];
+#pragma unroll
+                        for (int j = 0; j < KMAX; ++j) {
+                            mo[j] = kk[j];
+                            mi[j] = ki[j];
+                            mo[KMAX + j] = co[j];
+                            mi[KMAX + j] = ci[j];
+                        }
+                        top_by_key<2 * KMAX, KMAX>(mo, mi, kk, ki);
+                    }
+                }
             } else {
                 for (int c = cs0; c < cs1; c += 32) {
                     float v[32];
@@ -402,7 +501,37 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     store_logits(v, c);
                 }
             }
-            if (SLICES > 1) {
+            if (KEYED && SLICES > 1) {
+                // keyed lists of slices 1.. into the stage ring (every MMA has read it);
+                // group 0 takes the best KMAX of all SLICES lists
+                uint32_t *lk = reinterpret_cast<uint32_t *>(smem);   // [SLICES-1][BM][KMAX]
+                int *lki = reinterpret_cast<int *>(lk + (SLICES - 1) * BM * KMAX);
+                if (slice > 0 && own)
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j) {
+                        lk[((slice - 1) * BM + r) * KMAX + j] = kk[j];
+                        lki[((slice - 1) * BM + r) * KMAX + j] = ki[j];
+                    }
+                epilogue_sync<NT>();
+                if (slice == 0 && own) {
+                    constexpr int NC = SLICES * KMAX;   // 2..32, a power of two
+                    uint32_t mo[NC];
+                    int mi[NC];
+#pragma unroll
+                    for (int j = 0; j < KMAX; ++j) {
+                        mo[j] = kk[j];
+                        mi[j] = ki[j];
+                    }
+#pragma unroll
+                    for (int g = 0; g < SLICES - 1; ++g)
+#pragma unroll
+                        for (int j = 0; j < KMAX; ++j) {
+                            mo[(g + 1) * KMAX + j] = lk[(g * BM + r) * KMAX + j];
+                            mi[(g + 1) * KMAX + j] = lki[(g * BM + r) * KMAX + j];
+                        }
+                    top_by_key<NC, KMAX>(mo, mi, kk, ki);
+                }
+            } else if (SLICES > 1) {
                 // lists of slices 1.. into the stage ring (every MMA has read it), then
                 // group 0 pushes them in slice order, i.e. in increasing expert id
                 float *lv = reinterpret_cast<float *>(smem);   // [SLICES-1][BM][KMAX]
@@ -428,6 +557,13 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmap_x,
                             else
                                 topk_push_raw<KMAX>(val, raw, idx, lv[o], lr[o], e);
                         }
+            }
+            if (KEYED) {
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    val[j] = key_value(kk[j]);
+                    idx[j] = ki[j];
+                }
             }
             if (slice == 0 && own && tok < p.rows) {
                 // softmax over the chosen experts' logits

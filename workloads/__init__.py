@@ -91,7 +91,19 @@ ROUTE_PROFILE = LayerShape("route_profile_n8192_h2880_e128_k4", N=8192, H=2880, 
 ROUTE_PROFILE_DECODE = LayerShape("route_profile_n128_h2880_e128_k4", N=128, H=2880, I=128,
                                   E=128, top_k=4, ep_size=8)
 
-BY_NAME = {s.name: s for s in ALL_SHAPES + (GPTOSS_PROFILE, ROUTE_PROFILE, ROUTE_PROFILE_DECODE)}
+# The 8-expert layer's per-expert GEMMs (4096 rows per expert, hidden 4096, intermediate
+# 14336) on 2 experts: every token routes to both, ~1.5 GB on the device.
+E8K2_PROFILE = LayerShape("e8k2_profile_n4096_h4096_e2_k2", N=4096, H=4096, I=14336, E=2,
+                          top_k=2, ep_size=2)
+
+# The skewed + capacity layer's per-expert GEMMs at its capacity (5120 rows per expert,
+# hidden 2048, intermediate 1408) on 8 experts: every token routes to all 8, under 1 GB.
+SKEWED_PROFILE = LayerShape("skewed_profile_n5120_h2048_e8_k8", N=5120, H=2048, I=1408, E=8,
+                            top_k=8, ep_size=8)
+
+PROFILE_SHAPES = (GPTOSS_PROFILE, ROUTE_PROFILE, ROUTE_PROFILE_DECODE, E8K2_PROFILE,
+                  SKEWED_PROFILE)
+BY_NAME = {s.name: s for s in ALL_SHAPES + PROFILE_SHAPES}
 
 
 def _gen(seed: int, tensor_id: int, device, sub: int = 0) -> torch.Generator:
