@@ -22,9 +22,10 @@
 //               weight-gradient GEMMs the warp first zeroes the rows of the last K block
 //               that lie past the expert's segment, in both operands (they hold another
 //               expert's rows, or unwritten memory past the kept rows).
-//   warps 2..   epilogue: 4 warps in the weight-gradient GEMMs (64 columns at a time),
-//               8 in the dgrad GEMMs (two per TMEM lane quarter, alternate 16-token
-//               chunks, each half with its own named barrier).
+//   warps 2..9  epilogue, two warps per TMEM lane quarter: in the weight-gradient GEMMs
+//               each takes 128 of the tile's 256 columns (one TMEM load, two 64-column
+//               TMA stores); in the dgrad GEMMs alternate 16-token chunks, each half
+//               with its own named barrier.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
 // MOE_DEV_TIMEOUT in the status word, stops issuing work, waits (bounded) for its own
 // copies and MMAs, frees TMEM and returns.
@@ -42,9 +43,8 @@ constexpr int BN = 256;                 // max N per tile
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
 constexpr uint32_t MN_BOX = 64 * BK * 2;    // one 64-element x 64-row MN-major box: 8 KB
-// Threads: producer warp, MMA warp and 4 epilogue warps (weight gradients) or 8 (dgrad:
-// two per TMEM lane quarter, taking alternate 16-token chunks).
-template <int KIND> constexpr int num_threads() { return KIND == 2 ? 192 : 320; }
+// Threads: producer warp, MMA warp and 8 epilogue warps (two per TMEM lane quarter).
+template <int KIND> constexpr int num_threads() { return 320; }
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int CHUNK = 32;
 
@@ -74,9 +74,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
 }
 __device__ __forceinline__ void tma_store_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void tma_store_wait_read1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void tma_store_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -116,8 +113,8 @@ struct BwdParams {
 };
 
 // 4-stage ring. The dgrad GEMMs add a 16 KB staging block, the token tile's pair ids and
-// weights and two tile tables; the weight-gradient GEMMs 32 KB of TMA-store staging (4
-// warps x 2 buffers x 4 KB) and the expert offsets only.
+// weights and two tile tables; the weight-gradient GEMMs 32 KB of TMA-store staging (8
+// warps x one 4 KB buffer) and the expert offsets only.
 template <int KIND>
 struct Smem {
     static constexpr bool WG = KIND == BWD_WGRAD;
@@ -125,7 +122,7 @@ struct Smem {
     static constexpr uint32_t a_off = 0;
     static constexpr uint32_t b_off = STAGES * A_BYTES;
     static constexpr uint32_t epi_off = b_off + STAGES * B_BYTES;
-    static constexpr uint32_t epi_bytes = WG ? 4 * 2 * 4096 : CHUNK * BM * 4;
+    static constexpr uint32_t epi_bytes = WG ? 8 * 4096 : CHUNK * BM * 4;
     static constexpr uint32_t pairs_off = epi_off + epi_bytes;       // [BN] int + [BN] float
     static constexpr uint32_t bar_off = pairs_off + (WG ? 0 : 2 * BN * 4);
     static constexpr uint32_t misc_off = bar_off + 24 * 8;
@@ -164,33 +161,6 @@ __device__ __forceinline__ WTile wtile_at(int t, const int *eo, int m_tiles, int
     r.nrows = eo[r.e + 1] - r.row0;
     r.nkb = (r.nrows + BK - 1) / BK;
     return r;
-}
-
-// 64 consecutive fp32 accumulator columns of this thread's TMEM lane (one load, one wait).
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float *v) {
-    uint32_t r[64];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
-        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
-          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
-          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
-          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
-          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
-          "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 128 consecutive fp32 accumulator columns of this thread's TMEM lane (one load, one wait).
@@ -242,11 +212,6 @@ __device__ __forceinline__ bool epi8_all(bool ok) {
     return r != 0;
 }
 
-__device__ __forceinline__ void load8_bf16(const __nv_bfloat16 *p, float *f) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(p);
-    Vec16<__nv_bfloat16>::to_float(v, f);
-}
-
 template <int KIND>
 __global__ void __launch_bounds__(num_threads<KIND>(), 1)
 grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
@@ -283,7 +248,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], WG ? 4 : 8);   // one arrival per epilogue warp
+            mbar_init(&tempty[a], 8);   // one arrival per epilogue warp
         }
         mbar_init(mma_done, 1);
         *abort_s = 0;
@@ -474,14 +439,17 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_s, p.status);
             // tcgen05.ld is warp-collective and the epilogue warps share named barriers:
             // they leave together on abort
-            if (!(WG ? epilogue_all(ok) : epi8_all(ok))) break;
+            if (!epi8_all(ok)) break;
             fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             if (WG) {
-                // The warp's 32 accumulator rows are 32 consecutive rows of one output:
-                // 64 columns at a time go through a 128-byte-swizzled staging block
-                // [32 rows][128 bytes] into a TMA store (rows past I / H and columns past
-                // the output's width are clipped by the 3-D map).
+                // The warp's 32 accumulator rows are 32 consecutive rows of one output;
+                // half h of the 8 epilogue warps takes accumulator columns 128 h ..
+                // 128 h + 127 in one TMEM load and stores them as two 64-column chunks,
+                // each through the warp's 128-byte-swizzled staging block [32 rows][128
+                // bytes] into a TMA store (rows past I / H and columns past the output's
+                // width are clipped by the 3-D map).
+                const int half = (warp - 2) >> 2;
                 const int m0 = wt.mt * BM + q * 32;
                 int sel = 0, r0 = m0, ncols = p.I;
                 if (p.wgrad_gu) {
@@ -490,26 +458,29 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     ncols = p.H;
                 }
                 const bool live = r0 < (p.wgrad_gu ? p.I : p.H);
-                uint8_t *stage = smem + L::epi_off + q * 8192;   // 2 chunk buffers
-                // 128 accumulator columns per TMEM load, stored as two 64-column chunks
-                for (int c2 = 0; c2 < BN; c2 += 128) {
-                    if (wt.nt * BN + c2 >= ncols) break;   // uniform over the CTA
-                    float v[128];
+                uint8_t *buf = smem + L::epi_off + (warp - 2) * 4096;
+                const int c2 = 128 * half;
+                const bool cols_live = wt.nt * BN + c2 < ncols;   // uniform over the warp
+                float v[128];
+                if (cols_live) {
                     if (wt.nkb > 0) {
                         tmem_ld128(taddr + c2, v);
                     } else {
 #pragma unroll
                         for (int j = 0; j < 128; ++j) v[j] = 0.f;   // an expert with no rows
                     }
-                    if (!live) continue;
+                }
+                // the warp's accumulator columns are read: hand them back
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+                if (live && cols_live) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int c = c2 + 64 * h;
-                        const int col0 = wt.nt * BN + c;
+                        const int col0 = wt.nt * BN + c2 + 64 * h;
                         if (col0 >= ncols) break;
-                        uint8_t *buf = stage + h * 4096;
-                        // the store that last read this buffer (two stores ago) is done
-                        if (lane == 0) tma_store_wait_read1();
+                        // the store that last read the staging block is done
+                        if (lane == 0) tma_store_wait_read();
                         __syncwarp();
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
@@ -520,9 +491,6 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                         if (lane == 0) tma_store_3d(&maps.out[sel], smem_u32(buf), col0, r0, wt.e);
                     }
                 }
-                fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc]);
             } else {
                 // dgrad: half h of the 8 epilogue warps takes the 16-token chunks
                 // c = 16h, 16h + 32, ...; each half stages its chunk [16 tokens][128
