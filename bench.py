@@ -502,10 +502,11 @@ def time_backward(moe, args, shape, inp, packed, dist, dev, stream, mode=None):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    torch.cuda._sleep(2_000_000)
-    for i in range(args.steps):
-        step(1, evs[i])
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        torch.cuda._sleep(2_000_000)
+        for i in range(args.steps):
+            step(1, evs[i])
+        torch.cuda.synchronize()
     if moe.moe_read_device_status(cfg, ws):
         raise RuntimeError("device status flags set after the backward steps")
     fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
@@ -527,7 +528,7 @@ def time_backward(moe, args, shape, inp, packed, dist, dev, stream, mode=None):
                               peak=peak, frac=round(ach / peak, 4) if peak else None,
                               source=psrc,
                               note="whole backward time against the expert GEMMs' flops"),
-                gpu_launches=(6 + BACKWARD_LAUNCHES) * args.steps)
+                gpu_launches=(6 + BACKWARD_LAUNCHES) * args.steps, clocks=clk.summary())
 
 
 def _event_ms(stream, fn, steps):
@@ -569,13 +570,15 @@ def time_variants(moe, args, shape, inp, packed, dev, stream):
     evs = {p: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)] for p in cfgs}
     torch.cuda.synchronize()
-    torch.cuda._sleep(1_000_000)
-    for i in range(args.steps):
-        for prio in ("token", "slot"):
-            evs[prio][i][0].record(stream)
-            moe.moe_layer_forward(cfgs[prio], x, wr, b, packed, wd, out, wss[prio])
-            evs[prio][i][1].record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        torch.cuda._sleep(1_000_000)
+        for i in range(args.steps):
+            for prio in ("token", "slot"):
+                evs[prio][i][0].record(stream)
+                moe.moe_layer_forward(cfgs[prio], x, wr, b, packed, wd, out, wss[prio])
+                evs[prio][i][1].record(stream)
+        torch.cuda.synchronize()
+    res["clocks"] = clk.summary()
     for prio in ("token", "slot"):
         ms = float(np.mean([a.elapsed_time(z) for a, z in evs[prio]]))
         res[f"{prio}_priority_forward"] = dict(ms=round(ms, 4),
