@@ -7,7 +7,8 @@ and 1e-4 * max|ref| for fp32 layers (the forward's fp32 rule).
 Routing is exact on the dyadic input variant, so both sides differentiate the same
 selection. The shapes span several M / N / K tiles with ragged tails (H and I not
 multiples of 64 or 128), capacity drops, slot-major priority, mask-and-sum mode, a
-single token, experts that receive no rows, and a 256-row expert segment boundary.
+single token, experts that receive no rows, segments of more than 256 and of more
+than 512 rows, and more tiles than the GPU runs at once (persistent tile loops).
 """
 import numpy as np
 import pytest
@@ -30,6 +31,11 @@ SHAPES = [
     S("b_sparse", N=20, H=128, I=64, E=32, top_k=2, ep_size=8),     # most experts get no rows
     S("b_one", N=1, H=64, I=64, E=4, top_k=2, ep_size=2),
     S("b_long_seg", N=1200, H=192, I=320, E=4, top_k=1, ep_size=2),  # segments > 256 rows
+    # segments of ~1150 rows: several 256-token tiles per expert
+    S("b_multi_tile", N=2300, H=128, I=96, E=2, top_k=1, ep_size=2),
+    # more tiles than clusters of two SMs in all four GEMMs: each cluster runs several
+    # tiles, the ring and both accumulators cycle through several phases
+    S("b_persistent", N=2048, H=512, I=256, E=64, top_k=8, ep_size=8),
     # fp32 layers (FFMA kernels): ragged tiles, drops, the PR1 configuration
     S("f_ragged", N=333, H=96, I=72, E=8, top_k=2, ep_size=4, dtype="fp32", bias=True),
     S("f_cap", N=500, H=64, I=136, E=4, top_k=2, ep_size=2, capacity_factor=0.6, dtype="fp32"),
