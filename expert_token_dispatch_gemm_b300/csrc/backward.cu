@@ -135,6 +135,89 @@ router_wgrad_reduce_kernel(const float *__restrict__ partial, const float *__res
         }
 }
 
+// The expert-grouped rows of a token matrix, transposed into the K-major operand of the
+// weight-gradient GEMMs: dstT[h][64 pk_e + j] = src[perm[eo_e + j] / k][h] for the j-th
+// row of expert e's segment (pk_e = the 64-row blocks of the experts before e), zero for
+// j in [seg_e, 64 ceil(seg_e / 64)), so that every K block of an expert is whole. One
+// block per 64 columns of dstT (64 rows of one expert), looping over the hidden
+// dimension 128 at a time through a shared-memory tile. The blocks also zero rows
+// [A, A + 64) (A = the kept rows) of two [rows, cols] buffers, which the same GEMMs read
+// as their other operand in an expert's last K block.
+__global__ void __launch_bounds__(256)
+transpose_rows_kernel(const __nv_bfloat16 *__restrict__ src, int H, int k,
+                      const int32_t *__restrict__ eoff, int E, const int32_t *__restrict__ perm,
+                      __nv_bfloat16 *__restrict__ dstT, int64_t ldt, __nv_bfloat16 *z0, int z0_cols,
+                      __nv_bfloat16 *z1, int z1_cols, int rows) {
+    __shared__ int eo[kMaxExperts + 1], pk[kMaxExperts + 1];
+    __shared__ int tok_s[64];
+    // [row j][column h]; the 16-byte chunk of columns 8c .. 8c + 7 of row j is stored at
+    // chunk c ^ (j / 8 % 8), so that the column reads below spread over the banks
+    __shared__ __align__(16) __nv_bfloat16 tile[64][128];
+    grid_dep_wait();
+    grid_dep_trigger();
+    const int tid = threadIdx.x;
+    if (tid < 32) build_tile_tables(eoff, 0, E, 64, eo, pk);
+    __syncthreads();
+    // zero the rows past the kept rows (16-byte chunks spread over the whole grid)
+    {
+        const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+        const int A = eo[E];
+        const int64_t n0 = 64LL * (z0_cols / 8), n1 = 64LL * (z1_cols / 8);
+        for (int64_t g = (int64_t)blockIdx.x * blockDim.x + tid; g < n0 + n1; g += nthreads) {
+            __nv_bfloat16 *z = g < n0 ? z0 : z1;
+            const int cols = g < n0 ? z0_cols : z1_cols;
+            const int64_t c = g < n0 ? g : g - n0;
+            const int r = A + (int)(c / (cols / 8));
+            if (z != nullptr && r < rows)
+                *reinterpret_cast<uint4 *>(z + (size_t)r * cols + (c % (cols / 8)) * 8) =
+                    make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    const int cb = blockIdx.x;
+    if (cb >= pk[E]) return;   // past the last expert's blocks
+    int e, blk, unused;
+    decode_tile(cb, pk, E, 1, e, blk, unused);
+    const int seg = eo[e + 1] - eo[e];
+    if (tid < 64) tok_s[tid] = blk * 64 + tid < seg ? perm[eo[e] + blk * 64 + tid] / k : -1;
+    __syncthreads();
+    for (int h0 = 0; h0 < H; h0 += 128) {
+        // 64 rows x 128 columns of the source in 16-byte chunks; rows past the segment
+        // are zero
+        uint4 v[4];
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int c = tid + 256 * it;
+            const int j = c >> 4, hc = (c & 15) * 8;
+            const int tok = tok_s[j];
+            v[it] = make_uint4(0u, 0u, 0u, 0u);
+            if (tok >= 0 && h0 + hc < H)
+                v[it] = __ldg(reinterpret_cast<const uint4 *>(src + (size_t)tok * H + h0 + hc));
+        }
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int c = tid + 256 * it;
+            const int j = c >> 4;
+            *reinterpret_cast<uint4 *>(&tile[j][((c & 15) ^ ((j >> 3) & 7)) * 8]) = v[it];
+        }
+        __syncthreads();
+        // 128 rows of dstT (columns h0 ..), each 64 columns = eight 16-byte chunks
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int c = tid + 256 * it;
+            const int hh = c >> 3, jc = (c & 7) * 8;
+            if (h0 + hh < H) {
+                __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    o[q] = tile[jc + q][(((hh >> 3) ^ ((jc >> 3) & 7)) << 3) | (hh & 7)];
+                *reinterpret_cast<uint4 *>(dstT + (size_t)(h0 + hh) * ldt + (size_t)cb * 64 + jc) =
+                    *reinterpret_cast<const uint4 *>(o);
+            }
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 int router_wgrad_splits(const LayerDims &d) {
@@ -148,6 +231,14 @@ cudaError_t launch_router_dl(const LayerDims &d, const float *dweight_part, int 
                              cudaStream_t s) {
     return launch_pdl(router_dl_kernel, dim3(ceil_div(d.N, 256)), dim3(256), 0, s, d.N, d.k, m_tiles,
                       d.N * d.k, dweight_part, slot_pos, topk_w, dl);
+}
+
+cudaError_t launch_transpose_rows(const LayerDims &d, const void *src, const int32_t *eoff,
+                                  const int32_t *perm, void *dstT, int64_t ldt, void *z0, int z0_cols,
+                                  void *z1, int z1_cols, cudaStream_t s) {
+    return launch_pdl(transpose_rows_kernel, dim3((unsigned)(ldt / 64)), dim3(256), 0, s, (const __nv_bfloat16 *)src,
+                      d.H, d.k, eoff, d.E, perm, (__nv_bfloat16 *)dstT, ldt,
+                      (__nv_bfloat16 *)z0, z0_cols, (__nv_bfloat16 *)z1, z1_cols, d.N * d.k);
 }
 
 cudaError_t launch_dx_combine(const LayerDims &d, const void *dx_slots, const int32_t *slot_pos,

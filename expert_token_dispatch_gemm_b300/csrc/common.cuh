@@ -163,19 +163,29 @@ constexpr int kStatsBlocks = 256;
 
 // Backward: grouped GEMMs (tensor cores for bf16, FFMA for fp32), then the router /
 // combine kernels.
+// The weight-gradient GEMMs' K-major operands are transposed copies of token rows in the
+// send layout, [features][the 64-row blocks of every expert in turn] with this many
+// columns (zero past each segment).
+int64_t wgrad_t_cols(const LayerDims &d);
+// dgrad-down writes dgu rows and (w a)^T in that transposed layout.
 cudaError_t launch_tc_dgrad_down(const LayerDims &d, const void *dout_send, const int32_t *eoff,
                                  const void *w_down, const void *gu, const int32_t *perm,
-                                 const float *topk_w, void *dgu, void *wa, float *dweight_part,
+                                 const float *topk_w, void *dgu, void *waT, float *dweight_part,
                                  int32_t *status, cudaStream_t s);
 cudaError_t launch_tc_dgrad_gate_up(const LayerDims &d, const void *dgu, const int32_t *eoff,
                                     const void *packed, const int32_t *perm, void *dx_slots,
                                     int32_t *status, cudaStream_t s);
-cudaError_t launch_tc_wgrad_gate_up(const LayerDims &d, const void *dgu, const void *send,
+cudaError_t launch_tc_wgrad_gate_up(const LayerDims &d, const void *dgu, const void *xT,
                                     const int32_t *eoff, void *dw_gate, void *dw_up,
                                     int32_t *status, cudaStream_t s);
-cudaError_t launch_tc_wgrad_down(const LayerDims &d, const void *dout_send, const void *wa,
+cudaError_t launch_tc_wgrad_down(const LayerDims &d, const void *dout_send, const void *waT,
                                  const int32_t *eoff, void *dw_down, int32_t *status,
                                  cudaStream_t s);
+// x^T in the weight-gradient layout (ldt = wgrad_t_cols) from x [N, H] and perm; also zeroes
+// rows [A, A + 64) of z0 [N*k, z0_cols] and z1 [N*k, z1_cols] (A = the kept rows).
+cudaError_t launch_transpose_rows(const LayerDims &d, const void *src, const int32_t *eoff,
+                                  const int32_t *perm, void *dstT, int64_t ldt, void *z0, int z0_cols,
+                                  void *z1, int z1_cols, cudaStream_t s);
 cudaError_t launch_simt_dgrad_down(const LayerDims &d, const float *dout_send, const int32_t *eoff,
                                    const float *w_down, const float *gu, const int32_t *perm,
                                    const float *topk_w, float *dgu, float *wa, float *dweight_part,

@@ -1,37 +1,29 @@
-// Backward of the local experts as grouped GEMMs on the tensor cores. The chain rule
+// Backward of the local experts, the dgrad GEMMs on the tensor cores. The chain rule
 // through y = W_d (silu(g) * u), g = W_g x, u = W_u x of every kept (token, expert) pair
-// (Ultralytics glossary "Expert Parallelism", step 3; an expert's weight gradient sums
-// over every row it received -- Hugging Face "Expert parallelism" docs, "How the sizes
-// combine"). Per send row r (pair of token t, weight w) with upstream gradient dout_t:
+// (Ultralytics glossary "Expert Parallelism", step 3). Per send row r (pair of token t,
+// weight w) with upstream gradient dout_t:
 //   dgrad_down : da_u[i, r] = sum_h W_d[h, i] dout_t[h]       (tokens on N, K = H)
 //                epilogue: a = silu(g) u, dweight_r += da_u . a (the routing weight's
-//                gradient), dg = w da_u u silu'(g), du = w da_u silu(g), wa = w a
+//                gradient), dg = w da_u u silu'(g), du = w da_u silu(g) into the dgu
+//                rows, and (w a)^T in the transposed layout of the weight-gradient GEMMs
+//                (grouped_gemm_wgrad.cu)
 //   dgrad_gu   : dx_r[h] = sum_f W_gu[f, h] dgu_r[f]           (tokens on N, K = 2 Ipad)
-//   wgrad      : dW_gu[f, h] = sum_r dgu_r[f] x_r[h]           (K = the expert's rows)
-//                dW_d[h, i]  = sum_r dout_t[h] wa_r[i]
-// The weights stay in their forward layouts: the dgrad GEMMs read them as MN-major A
-// operands (M = the weight's column index), and the weight-gradient GEMMs read both
-// token-major activations as MN-major operands (K = token rows), so nothing is
-// transposed in memory.
+// The weights stay in their forward layouts: the GEMMs read them as MN-major A operands
+// (M = the weight's column index), so nothing is transposed in memory.
 //
-// One CTA per SM (192 threads, persistent over its tiles), tcgen05.mma cta_group::1,
+// One CTA per SM (320 threads, persistent over its tiles), tcgen05.mma cta_group::1,
 // M = 128 TMEM lanes, N <= 256:
 //   warp 0      TMA producer, 4-stage ring (A: 128 x 64, B: up to 256 x 64; 128-byte
 //               swizzle). MN-major tiles are 64-element boxes: one 128-byte row per K.
-//   warp 1      TMEM (two 128 x 256 fp32 accumulators); lane 0 issues the MMAs. In the
-//               weight-gradient GEMMs the warp first zeroes the rows of the last K block
-//               that lie past the expert's segment, in both operands (they hold another
-//               expert's rows, or unwritten memory past the kept rows).
-//   warps 2..9  epilogue, two warps per TMEM lane quarter: in the weight-gradient GEMMs
-//               each takes 128 of the tile's 256 columns (one TMEM load, two 64-column
-//               TMA stores); in the dgrad GEMMs alternate 16-token chunks, each half
-//               with its own named barrier.
+//   warp 1      TMEM (two 128 x 256 fp32 accumulators); lane 0 issues the MMAs.
+//   warps 2..9  epilogue, two warps per TMEM lane quarter taking alternate 16-token
+//               chunks, each half with its own named barrier.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
 // MOE_DEV_TIMEOUT in the status word, stops issuing work, waits (bounded) for its own
 // copies and MMAs, frees TMEM and returns.
 #include <mutex>
 
-#include "sm100.cuh"
+#include "tc_bwd.cuh"
 
 namespace moe {
 namespace {
@@ -48,42 +40,12 @@ template <int KIND> constexpr int num_threads() { return 320; }
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int CHUNK = 32;
 
-enum { BWD_DGRAD_DOWN = 0, BWD_DGRAD_GU = 1, BWD_WGRAD = 2 };
-
-// Shared-memory descriptor of an MN-major tile written by TMA in 64-element boxes with
-// 128-byte swizzle: one 128-byte row per K index, 8-row groups 1024 bytes apart (stride
-// byte offset), 64-element groups along M / N `lbo` bytes apart (leading byte offset).
-// Advancing K by 16 adds 16 rows = 2048 bytes to the start address.
-__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(src), "r"(x), "r"(y), "r"(z)
-        : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void tma_store_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void tma_store_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
+enum { BWD_DGRAD_DOWN = 0, BWD_DGRAD_GU = 1 };
 
 // Token maps with box heights 32, 64, 128 and 256 rows (K-major B of the dgrad GEMMs).
 struct BwdMaps {
     CUtensorMap a;       // MN-major A: box 64 x 64
-    CUtensorMap b[4];    // dgrad: token rows (K-major); wgrad: b[0] MN-major box 64 x 64
-    CUtensorMap out[2];  // wgrad: [E][rows][cols] outputs, box 64 x 32 (TMA stores)
+    CUtensorMap b[4];    // token rows (K-major)
 };
 __host__ __device__ constexpr int box_index(int rows) {
     return rows <= 32 ? 0 : rows <= 64 ? 1 : rows <= 128 ? 2 : 3;
@@ -93,129 +55,61 @@ struct BwdParams {
     const int32_t *expert_offsets;
     int ne;                  // experts (all of the layer)
     int num_kb;              // dgrad: K blocks of BK
-    int m_tiles, n_tiles;    // M tiles of BM; wgrad: N tiles of BN
+    int m_tiles;             // M tiles of BM
     int a_rows_per_expert;   // dgrad: rows between experts in A's map (K rows)
     uint32_t lbo, sbo;       // MN-major descriptor strides
     int I, Ipad, H;
     // dgrad_down
     const __nv_bfloat16 *gu;      // [rows, 2 Ipad] saved gate / up pre-activations
     __nv_bfloat16 *dgu;           // [rows, 2 Ipad] out
-    __nv_bfloat16 *wa;            // [rows, Ipad] out: w * silu(g) * u
+    __nv_bfloat16 *waT;           // [Ipad, ldt] out: (w * silu(g) * u)^T, the 64-row
+    int64_t ldt;                  // blocks of every expert in turn, zero past each segment
     float *dweight_part;          // [m_tiles, rows] out
     int rows;                     // send rows of the buffers (N * k)
     // dgrad_down / dgrad_gu
     const int32_t *perm;
     const float *topk_w;
     __nv_bfloat16 *dx_slots;      // dgrad_gu: [N*k, H] out (row = pair id)
-    int wgrad_gu;                 // wgrad: 1 = M is packed gate/up rows (outputs dW_gate,
-                                  // dW_up), 0 = M is down rows (output dW_down)
     int32_t *status;
 };
 
-// 4-stage ring. The dgrad GEMMs add a 16 KB staging block, the token tile's pair ids and
-// weights and two tile tables; the weight-gradient GEMMs 32 KB of TMA-store staging (8
-// warps x one 4 KB buffer) and the expert offsets only.
+// 4-stage ring, a 16 KB staging block, the token tile's pair ids and weights and the
+// tile tables (dgrad-down also the 64-row block prefix of (w a)^T's columns).
 template <int KIND>
 struct Smem {
-    static constexpr bool WG = KIND == BWD_WGRAD;
     static constexpr int STAGES = 4;
     static constexpr uint32_t a_off = 0;
     static constexpr uint32_t b_off = STAGES * A_BYTES;
     static constexpr uint32_t epi_off = b_off + STAGES * B_BYTES;
-    static constexpr uint32_t epi_bytes = WG ? 8 * 4096 : CHUNK * BM * 4;
+    static constexpr uint32_t epi_bytes = CHUNK * BM * 4;
     static constexpr uint32_t pairs_off = epi_off + epi_bytes;       // [BN] int + [BN] float
-    static constexpr uint32_t bar_off = pairs_off + (WG ? 0 : 2 * BN * 4);
+    static constexpr uint32_t bar_off = pairs_off + 2 * BN * 4;
     static constexpr uint32_t misc_off = bar_off + 24 * 8;
     static constexpr uint32_t tables_off = misc_off + 16;
-    static constexpr uint32_t end = tables_off + (WG ? 1 : 2) * (kMaxExperts + 1) * 4;
+    static constexpr uint32_t end = tables_off + 4 * (kMaxExperts + 1) * 4;
     static constexpr uint32_t alloc = end + 1024;
 };
-static_assert(Smem<BWD_WGRAD>::alloc <= 227 * 1024 && Smem<BWD_DGRAD_DOWN>::alloc <= 227 * 1024,
-              "shared memory per CTA");
+static_assert(Smem<BWD_DGRAD_DOWN>::alloc <= 227 * 1024, "shared memory per CTA");
 
-// Tile of a dgrad GEMM: expert i, M tile f, token tile m; tokens fastest.
+// Tile of a dgrad GEMM: expert i, M tile f, token tile m; tokens fastest. The MMA's N is
+// the tile's tokens rounded up to 32, to 64 in dgrad-down, whose epilogue then writes
+// every column of the expert's last 64-row block of (w a)^T (zeros past the segment).
 struct DTile {
     int i, f, m, tok0, ntok, nmma;
 };
+template <int KIND>
 __device__ __forceinline__ DTile dtile_at(int t, const int *mtp, const int *eo, int ne, int m_tiles) {
     DTile r;
     decode_tile(t, mtp, ne, m_tiles, r.i, r.m, r.f);
     const int seg = eo[r.i + 1] - eo[r.i];
     r.tok0 = eo[r.i] + r.m * BN;
     r.ntok = min(BN, seg - r.m * BN);
-    r.nmma = (r.ntok + 31) & ~31;
+    r.nmma = KIND == BWD_DGRAD_DOWN ? (r.ntok + 63) & ~63 : (r.ntok + 31) & ~31;
     return r;
 }
-// Tile of a weight-gradient GEMM: expert e, M tile mt, N tile nt; K = the expert's rows.
-struct WTile {
-    int e, mt, nt, row0, nrows, nkb;
-};
-__device__ __forceinline__ WTile wtile_at(int t, const int *eo, int m_tiles, int n_tiles) {
-    WTile r;
-    const int per = m_tiles * n_tiles;
-    r.e = t / per;
-    const int l = t - r.e * per;
-    r.mt = l / n_tiles;          // N fastest: concurrent tiles share the A rows in L2
-    r.nt = l - r.mt * n_tiles;
-    r.row0 = eo[r.e];
-    r.nrows = eo[r.e + 1] - r.row0;
-    r.nkb = (r.nrows + BK - 1) / BK;
-    return r;
-}
-
-// 128 consecutive fp32 accumulator columns of this thread's TMEM lane (one load, one wait).
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float *v) {
-    uint32_t r[128];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 16 consecutive fp32 accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Named barriers of the 8 dgrad epilogue warps: id 1 + half for one half (128 threads),
-// id 3 for all 256 (also a vote: returns whether `ok` holds in every thread).
-__device__ __forceinline__ void half_sync(int half) {
-    asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory");
-}
-__device__ __forceinline__ void epi8_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
-__device__ __forceinline__ bool epi8_all(bool ok) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 3, 256, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)ok)
-        : "memory");
-    return r != 0;
-}
-
 template <int KIND>
 __global__ void __launch_bounds__(num_threads<KIND>(), 1)
 grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p) {
-    constexpr bool WG = KIND == BWD_WGRAD;
     using L = Smem<KIND>;
     constexpr int STAGES = L::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -231,6 +125,8 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     volatile int *abort_s = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
     int *eo = reinterpret_cast<int *>(smem + L::tables_off);
     int *mtp = eo + (kMaxExperts + 1);
+    int *eo2 = mtp + (kMaxExperts + 1);
+    int *pk = eo2 + (kMaxExperts + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0) {
@@ -257,11 +153,10 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     grid_dep_wait();
     grid_dep_trigger();
     if (warp == 0) {
-        if (WG) {
-            for (int e = lane; e <= p.ne; e += 32) eo[e] = p.expert_offsets[e];
-        } else {
-            build_tile_tables(p.expert_offsets, 0, p.ne, BN, eo, mtp);
-        }
+        build_tile_tables(p.expert_offsets, 0, p.ne, BN, eo, mtp);
+        // dgrad-down: the 64-row blocks of the experts before e, the column of expert e's
+        // first row in (w a)^T (eo2 is the same expert-offset table again)
+        if (KIND == BWD_DGRAD_DOWN) build_tile_tables(p.expert_offsets, 0, p.ne, 64, eo2, pk);
     }
     fence_before();
     __syncthreads();
@@ -270,8 +165,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     // One CTA per tile, persistent over the tiles t = blockIdx.x + j * gridDim.x.
     const int tile0 = (int)blockIdx.x;
     const int tstride = (int)gridDim.x;
-    const int total = WG ? p.ne * p.m_tiles * p.n_tiles : mtp[p.ne] * p.m_tiles;
-    auto wtile = [&](int t) { return wtile_at(t, eo, p.m_tiles, p.n_tiles); };
+    const int total = mtp[p.ne] * p.m_tiles;
 
     if (warp == 0) {
         if (lane == 0) {   // ------------------------------------------ TMA producer
@@ -279,27 +173,12 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             uint32_t phase = 0, armed = 0, armed_parity = 0;
             bool ok = true;
             for (int t = tile0; ok && t < total; t += tstride) {
-                int nkb, a_x, a_y0, b_x, b_y0, bsel;
-                uint32_t tx;
-                if (WG) {
-                    const WTile tl = wtile(t);
-                    nkb = tl.nkb;
-                    a_x = tl.mt * BM;
-                    b_x = tl.nt * BN;
-                    a_y0 = b_y0 = tl.row0;
-                    bsel = 0;
-                    tx = A_BYTES + B_BYTES;
-                } else {
-                    const DTile tl = dtile_at(t, mtp, eo, p.ne, p.m_tiles);
-                    nkb = p.num_kb;
-                    a_x = tl.f * BM;
-                    a_y0 = tl.i * p.a_rows_per_expert;
-                    b_y0 = tl.tok0;
-                    bsel = box_index(tl.nmma);
-                    b_x = 0;
-                    tx = A_BYTES + (uint32_t)(32 << bsel) * BK * 2;
-                }
-                for (int kb = 0; kb < nkb; ++kb) {
+                const DTile tl = dtile_at<KIND>(t, mtp, eo, p.ne, p.m_tiles);
+                const int a_x = tl.f * BM;
+                const int a_y0 = tl.i * p.a_rows_per_expert;
+                const int bsel = box_index(tl.nmma);
+                const uint32_t tx = A_BYTES + (uint32_t)(32 << bsel) * BK * 2;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_s, p.status)) {
                         ok = false;
                         break;
@@ -310,14 +189,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     const uint32_t b_dst = smem_u32(smem + L::b_off + stage * B_BYTES);
                     tma_load_2d(a_dst, &maps.a, fb, a_x, a_y0 + kb * BK);
                     tma_load_2d(a_dst + MN_BOX, &maps.a, fb, a_x + 64, a_y0 + kb * BK);
-                    if (WG) {   // the B tile: four 64-column MN-major boxes
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            tma_load_2d(b_dst + q * MN_BOX, &maps.b[0], fb, b_x + 64 * q,
-                                        b_y0 + kb * BK);
-                    } else {
-                        tma_load_2d(b_dst, &maps.b[bsel], fb, kb * BK, b_y0);
-                    }
+                    tma_load_2d(b_dst, &maps.b[bsel], fb, kb * BK, tl.tok0);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -338,60 +210,25 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        const uint32_t idesc_mn = (1u << 15) | (WG ? (1u << 16) : 0u);
         for (int t = tile0; ok && t < total; t += tstride) {
-            int nkb, nmma, tail;
-            if (WG) {
-                const WTile tl = wtile(t);
-                nkb = tl.nkb;
-                nmma = BN;
-                tail = tl.nrows - (tl.nkb - 1) * BK;   // valid rows of the last K block
-            } else {
-                const DTile tl = dtile_at(t, mtp, eo, p.ne, p.m_tiles);
-                nkb = p.num_kb;
-                nmma = tl.nmma;
-                tail = BK;
-            }
-            const uint32_t idesc = make_idesc(BM, nmma) | idesc_mn;
+            const DTile tl = dtile_at<KIND>(t, mtp, eo, p.ne, p.m_tiles);
+            const uint32_t idesc = make_idesc(BM, tl.nmma) | (1u << 15);   // A MN-major
             if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_s, p.status))) break;
             fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int kb = 0; kb < nkb; ++kb) {
+            for (int kb = 0; kb < p.num_kb; ++kb) {
                 if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_s, p.status))) {
                     ok = false;
                     break;
                 }
-                uint8_t *a_tile = smem + L::a_off + stage * A_BYTES;
-                uint8_t *b_tile = smem + L::b_off + stage * B_BYTES;
-                // the last K block of a weight-gradient tile: only its 16-row slices
-                // that hold rows of the segment are multiplied, and the rows past the
-                // segment inside the last of them read as zero (both operands)
-                int kslices = BK / 16;
-                if (WG && kb == nkb - 1 && tail < BK) {
-                    kslices = (tail + 15) / 16;
-                    const int zr = kslices * 16 - tail;
-                    if (zr > 0) {
-                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                        for (int c = lane; c < 6 * zr * 8; c += 32) {
-                            const int box = c / (zr * 8), rem = c - box * zr * 8;
-                            const int row = tail + rem / 8, ch = rem % 8;
-                            uint8_t *base = box < 2 ? a_tile + box * MN_BOX : b_tile + (box - 2) * MN_BOX;
-                            *reinterpret_cast<uint4 *>(base + row * 128 + ch * 16) = z;
-                        }
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    }
-                    __syncwarp();
-                }
                 if (lane == 0) {
                     fence_after();
-                    const uint32_t a_addr = smem_u32(a_tile);
-                    const uint32_t b_addr = smem_u32(b_tile);
-                    for (int kk = 0; kk < kslices; ++kk) {
-                        const uint64_t ad = smem_desc_mn_sw128(a_addr + kk * 2048, p.lbo, p.sbo);
-                        const uint64_t bd = WG ? smem_desc_mn_sw128(b_addr + kk * 2048, p.lbo, p.sbo)
-                                               : smem_desc_sw128(b_addr + kk * 32);
-                        mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
-                    }
+                    const uint32_t a_addr = smem_u32(smem + L::a_off + stage * A_BYTES);
+                    const uint32_t b_addr = smem_u32(smem + L::b_off + stage * B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_bf16(d_tmem, smem_desc_mn_sw128(a_addr + kk * 2048, p.lbo, p.sbo),
+                                 smem_desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
                     commit(&empty[stage]);
                 }
                 __syncwarp();
@@ -424,17 +261,12 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         uint32_t acc_phase = 0;
         for (int t = tile0; t < total; t += tstride) {
             DTile dt = {};
-            WTile wt = {};
-            if (WG) {
-                wt = wtile(t);
-            } else {
-                dt = dtile_at(t, mtp, eo, p.ne, p.m_tiles);
-                for (int j = etid; j < dt.nmma; j += 256) {
-                    const bool tv = j < dt.ntok;
-                    const int pr = tv ? p.perm[dt.tok0 + j] : -1;
-                    pair_s[j] = pr;
-                    wgt_s[j] = tv && p.topk_w != nullptr ? p.topk_w[pr] : 1.f;
-                }
+            dt = dtile_at<KIND>(t, mtp, eo, p.ne, p.m_tiles);
+            for (int j = etid; j < dt.nmma; j += 256) {
+                const bool tv = j < dt.ntok;
+                const int pr = tv ? p.perm[dt.tok0 + j] : -1;
+                pair_s[j] = pr;
+                wgt_s[j] = tv && p.topk_w != nullptr ? p.topk_w[pr] : 1.f;
             }
             const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_s, p.status);
             // tcgen05.ld is warp-collective and the epilogue warps share named barriers:
@@ -442,56 +274,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             if (!epi8_all(ok)) break;
             fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            if (WG) {
-                // The warp's 32 accumulator rows are 32 consecutive rows of one output;
-                // half h of the 8 epilogue warps takes accumulator columns 128 h ..
-                // 128 h + 127 in one TMEM load and stores them as two 64-column chunks,
-                // each through the warp's 128-byte-swizzled staging block [32 rows][128
-                // bytes] into a TMA store (rows past I / H and columns past the output's
-                // width are clipped by the 3-D map).
-                const int half = (warp - 2) >> 2;
-                const int m0 = wt.mt * BM + q * 32;
-                int sel = 0, r0 = m0, ncols = p.I;
-                if (p.wgrad_gu) {
-                    sel = q >= 2 ? 1 : 0;                  // gate rows, then up rows
-                    r0 = wt.mt * 64 + (q & 1) * 32;
-                    ncols = p.H;
-                }
-                const bool live = r0 < (p.wgrad_gu ? p.I : p.H);
-                uint8_t *buf = smem + L::epi_off + (warp - 2) * 4096;
-                const int c2 = 128 * half;
-                const bool cols_live = wt.nt * BN + c2 < ncols;   // uniform over the warp
-                float v[128];
-                if (cols_live) {
-                    if (wt.nkb > 0) {
-                        tmem_ld128(taddr + c2, v);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 128; ++j) v[j] = 0.f;   // an expert with no rows
-                    }
-                }
-                // the warp's accumulator columns are read: hand them back
-                fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc]);
-                if (live && cols_live) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int col0 = wt.nt * BN + c2 + 64 * h;
-                        if (col0 >= ncols) break;
-                        // the store that last read the staging block is done
-                        if (lane == 0) tma_store_wait_read();
-                        __syncwarp();
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<uint4 *>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
-                                pack8_bf16(v + 64 * h + 8 * j);
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        __syncwarp();
-                        if (lane == 0) tma_store_3d(&maps.out[sel], smem_u32(buf), col0, r0, wt.e);
-                    }
-                }
-            } else {
+            {
                 // dgrad: half h of the 8 epilogue warps takes the 16-token chunks
                 // c = 16h, 16h + 32, ...; each half stages its chunk [16 tokens][128
                 // features] in its own half of the staging block
@@ -515,7 +298,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                         // 16 tokens x 16 groups of 8 features: two items per thread, their
                         // gate / up vectors loaded first so the latencies overlap
                         const __nv_bfloat16 *__restrict__ gu = p.gu;
-                        uint4 graw[2], uraw[2];
+                        uint4 graw[2], uraw[2], wa_v[2];
 #pragma unroll
                         for (int s2 = 0; s2 < 2; ++s2) {
                             const int item = htid + 128 * s2;
@@ -536,10 +319,11 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                             const int i = dt.f * BM + f8;             // intermediate feature
                             const bool tv = c + j < dt.ntok;
                             float part = 0.f;
+                            wa_v[s2] = make_uint4(0u, 0u, 0u, 0u);   // zero past the tile's tokens
                             if (tv) {
                                 const size_t r = (size_t)dt.tok0 + c + j;
                                 const int gcol = (i / 64) * 128 + (i % 64);   // packed column
-                                uint4 dg_v = make_uint4(0u, 0u, 0u, 0u), du_v = dg_v, wa_v = dg_v;
+                                uint4 dg_v = make_uint4(0u, 0u, 0u, 0u), du_v = dg_v;
                                 if (i < p.I) {
                                     const float w = wgt_s[c + j];
                                     float g[8], u[8], dg[8], du[8], wa[8];
@@ -561,17 +345,38 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                                     }
                                     dg_v = pack8_bf16(dg);
                                     du_v = pack8_bf16(du);
-                                    wa_v = pack8_bf16(wa);
+                                    wa_v[s2] = pack8_bf16(wa);
                                 }
                                 *reinterpret_cast<uint4 *>(p.dgu + r * 2 * p.Ipad + gcol) = dg_v;
                                 *reinterpret_cast<uint4 *>(p.dgu + r * 2 * p.Ipad + gcol + 64) = du_v;
-                                *reinterpret_cast<uint4 *>(p.wa + r * p.Ipad + i) = wa_v;
                             }
                             // the 16 items of token j are 16 consecutive lanes
 #pragma unroll
                             for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
                             if (tv && (item & 15) == 0)
                                 p.dweight_part[(size_t)dt.f * p.rows + dt.tok0 + c + j] = part;
+                        }
+                        half_sync(half);   // the chunk's da values are read
+                        // (w a)^T: the chunk [16 tokens][128 features] through this half's
+                        // staging block, then 16 bytes (8 tokens) of a feature row per item,
+                        // the two items of a feature in adjacent lanes
+                        __nv_bfloat16 *swa = reinterpret_cast<__nv_bfloat16 *>(sf);
+#pragma unroll
+                        for (int s2 = 0; s2 < 2; ++s2) {
+                            const int item = htid + 128 * s2;
+                            *reinterpret_cast<uint4 *>(swa + (item >> 4) * BM + (item & 15) * 8) = wa_v[s2];
+                        }
+                        half_sync(half);
+                        const int64_t colT = 64LL * pk[dt.i] + (int64_t)dt.m * BN + c;
+#pragma unroll
+                        for (int s2 = 0; s2 < 2; ++s2) {
+                            const int item = htid + 128 * s2;
+                            const int ff = item >> 1, jg = (item & 1) * 8;
+                            __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+                            for (int x = 0; x < 8; ++x) o[x] = swa[(jg + x) * BM + ff];
+                            *reinterpret_cast<uint4 *>(p.waT + (size_t)(dt.f * BM + ff) * p.ldt + colT + jg) =
+                                *reinterpret_cast<const uint4 *>(o);
                         }
                         half_sync(half);
                     } else {   // BWD_DGRAD_GU: dx of the pair, unweighted, into its slot
@@ -600,7 +405,6 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         }
     }
 
-    if (WG && warp >= 2 && lane == 0) tma_store_wait_all();   // stores done, staging free
     fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -654,7 +458,7 @@ cudaError_t token_maps(BwdMaps *m, const void *t, uint64_t rows, uint64_t cols, 
 
 cudaError_t launch_tc_dgrad_down(const LayerDims &d, const void *dout_send, const int32_t *eoff,
                                  const void *w_down, const void *gu, const int32_t *perm,
-                                 const float *topk_w, void *dgu, void *wa, float *dweight_part,
+                                 const float *topk_w, void *dgu, void *waT, float *dweight_part,
                                  int32_t *status, cudaStream_t s) {
     const int64_t rows = (int64_t)d.N * d.k;
     BwdMaps maps;
@@ -673,7 +477,8 @@ cudaError_t launch_tc_dgrad_down(const LayerDims &d, const void *dout_send, cons
     prm.H = d.H;
     prm.gu = (const __nv_bfloat16 *)gu;
     prm.dgu = (__nv_bfloat16 *)dgu;
-    prm.wa = (__nv_bfloat16 *)wa;
+    prm.waT = (__nv_bfloat16 *)waT;
+    prm.ldt = wgrad_t_cols(d);
     prm.dweight_part = dweight_part;
     prm.rows = (int)rows;
     prm.perm = perm;
@@ -706,56 +511,6 @@ cudaError_t launch_tc_dgrad_gate_up(const LayerDims &d, const void *dgu, const i
     prm.dx_slots = (__nv_bfloat16 *)dx_slots;
     prm.status = status;
     return launch_bwd<BWD_DGRAD_GU>(maps, prm, (ceil_div64(rows, BN) + d.E) * prm.m_tiles, s);
-}
-
-cudaError_t launch_tc_wgrad_gate_up(const LayerDims &d, const void *dgu, const void *send,
-                                    const int32_t *eoff, void *dw_gate, void *dw_up,
-                                    int32_t *status, cudaStream_t s) {
-    const int64_t rows = (int64_t)d.N * d.k;
-    BwdMaps maps = {};
-    cudaError_t e = make_map(&maps.a, dgu, rows, 2 * d.Ipad, 2 * d.Ipad, 64);
-    if (e == cudaSuccess) e = make_map(&maps.b[0], send, rows, d.H, d.H, 64);
-    for (int b = 1; b < 4 && e == cudaSuccess; ++b) maps.b[b] = maps.b[0];
-    if (e == cudaSuccess) e = make_store_map_3d(&maps.out[0], dw_gate, d.H, d.I, d.E, 64, 32);
-    if (e == cudaSuccess) e = make_store_map_3d(&maps.out[1], dw_up, d.H, d.I, d.E, 64, 32);
-    if (e != cudaSuccess) return e;
-    BwdParams prm = {};
-    prm.expert_offsets = eoff;
-    prm.ne = d.E;
-    prm.m_tiles = 2 * d.Ipad / BM;
-    prm.n_tiles = ceil_div(d.H, BN);
-    prm.I = d.I;
-    prm.Ipad = d.Ipad;
-    prm.H = d.H;
-    prm.rows = (int)rows;
-    prm.wgrad_gu = 1;
-    prm.status = status;
-    return launch_bwd<BWD_WGRAD>(maps, prm, (int64_t)d.E * prm.m_tiles * prm.n_tiles, s);
-}
-
-cudaError_t launch_tc_wgrad_down(const LayerDims &d, const void *dout_send, const void *wa,
-                                 const int32_t *eoff, void *dw_down, int32_t *status,
-                                 cudaStream_t s) {
-    const int64_t rows = (int64_t)d.N * d.k;
-    BwdMaps maps = {};
-    cudaError_t e = make_map(&maps.a, dout_send, rows, d.H, d.H, 64);
-    if (e == cudaSuccess) e = make_map(&maps.b[0], wa, rows, d.Ipad, d.Ipad, 64);
-    for (int b = 1; b < 4 && e == cudaSuccess; ++b) maps.b[b] = maps.b[0];
-    if (e == cudaSuccess) e = make_store_map_3d(&maps.out[0], dw_down, d.I, d.H, d.E, 64, 32);
-    if (e == cudaSuccess) maps.out[1] = maps.out[0];
-    if (e != cudaSuccess) return e;
-    BwdParams prm = {};
-    prm.expert_offsets = eoff;
-    prm.ne = d.E;
-    prm.m_tiles = ceil_div(d.H, BM);
-    prm.n_tiles = ceil_div(d.I, BN);
-    prm.I = d.I;
-    prm.Ipad = d.Ipad;
-    prm.H = d.H;
-    prm.rows = (int)rows;
-    prm.wgrad_gu = 0;
-    prm.status = status;
-    return launch_bwd<BWD_WGRAD>(maps, prm, (int64_t)d.E * prm.m_tiles * prm.n_tiles, s);
 }
 
 }  // namespace moe

@@ -137,6 +137,8 @@ struct Workspace {
     void *dgu;             // [N*k, 2 Ipad]
     float *dweight_part;   // [Ipad / 128, N*k]
     float *dl;             // [N*k]
+    void *xT;              // bf16: [H, wgrad_t_cols] x rows transposed per expert
+    void *waT;             // bf16: [Ipad, wgrad_t_cols] (w a) rows transposed per expert
     int32_t *routed_all, *counts_all, *eoff_all, *poff_all, *slot_all, *perm_all;
     float *rw_partial;     // [Z, E, H]
     float *rw_partial_db;  // [Z, E]
@@ -175,6 +177,10 @@ Workspace carve(const LayerDims &d, int mode, void *base) {
         w.dgu = take(pairs * 2 * d.Ipad * esize(d));
         w.dweight_part = (float *)take((size_t)(d.Ipad / 64) * pairs * sizeof(float));
         w.dl = (float *)take(pairs * sizeof(float));
+        if (d.dtype == MOE_DTYPE_BF16) {
+            w.xT = take((size_t)d.H * wgrad_t_cols(d) * esize(d));
+            w.waT = take((size_t)d.Ipad * wgrad_t_cols(d) * esize(d));
+        }
         w.routed_all = (int32_t *)take(d.E * sizeof(int32_t));
         w.counts_all = (int32_t *)take(d.E * sizeof(int32_t));
         w.eoff_all = (int32_t *)take((d.E + 1) * sizeof(int32_t));
@@ -695,15 +701,20 @@ moe_status_t moe_layer_backward(const moe_config *cfg, const void *x, const void
     int dw_tiles;   // M tiles of the dweight partials
     if (d.dtype == MOE_DTYPE_BF16) {
         dw_tiles = d.Ipad / 128;
+        // the weight-gradient GEMMs' K-major operands: x^T here, (w a)^T from dgrad-down;
+        // the rows past the kept rows of their other operands (dgu, dout) are zeroed here
+        MOE_CUDA(launch_transpose_rows(d, x, w.eoff, w.perm, w.xT, wgrad_t_cols(d), w.dgu,
+                                       2 * d.Ipad, w.dout_send, d.H, s),
+                 "transpose kernel");
         MOE_CUDA(launch_tc_dgrad_down(d, w.dout_send, w.eoff, w_down, w.gu, w.perm, w.topk_w,
-                                      w.dgu, w.h, w.dweight_part, w.status, s),
+                                      w.dgu, w.waT, w.dweight_part, w.status, s),
                  "tensor-core dgrad-down kernel");
         MOE_CUDA(launch_tc_dgrad_gate_up(d, w.dgu, w.eoff, w_gate_up_packed, w.perm, w.slots,
                                          w.status, s),
                  "tensor-core dgrad-gate/up kernel");
-        MOE_CUDA(launch_tc_wgrad_gate_up(d, w.dgu, w.send, w.eoff, dw_gate, dw_up, w.status, s),
+        MOE_CUDA(launch_tc_wgrad_gate_up(d, w.dgu, w.xT, w.eoff, dw_gate, dw_up, w.status, s),
                  "tensor-core wgrad-gate/up kernel");
-        MOE_CUDA(launch_tc_wgrad_down(d, w.dout_send, w.h, w.eoff, dw_down, w.status, s),
+        MOE_CUDA(launch_tc_wgrad_down(d, w.dout_send, w.waT, w.eoff, dw_down, w.status, s),
                  "tensor-core wgrad-down kernel");
     } else {
         dw_tiles = d.Ipad / 64;
