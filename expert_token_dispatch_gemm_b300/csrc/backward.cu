@@ -139,8 +139,8 @@ router_wgrad_reduce_kernel(const float *__restrict__ partial, const float *__res
 // weight-gradient GEMMs: dstT[h][64 pk_e + j] = src[perm[eo_e + j] / k][h] for the j-th
 // row of expert e's segment (pk_e = the 64-row blocks of the experts before e), zero for
 // j in [seg_e, 64 ceil(seg_e / 64)), so that every K block of an expert is whole. One
-// block per 64 columns of dstT (64 rows of one expert), looping over the hidden
-// dimension 128 at a time through a shared-memory tile. The blocks also zero rows
+// block per 64 columns of dstT (64 rows of one expert) and 512 of the hidden dimension,
+// 128 at a time through a shared-memory tile. The blocks also zero rows
 // [A, A + 64) (A = the kept rows) of two [rows, cols] buffers, which the same GEMMs read
 // as their other operand in an expert's last K block.
 __global__ void __launch_bounds__(256)
@@ -160,10 +160,11 @@ transpose_rows_kernel(const __nv_bfloat16 *__restrict__ src, int H, int k,
     __syncthreads();
     // zero the rows past the kept rows (16-byte chunks spread over the whole grid)
     {
-        const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+        const int64_t nthreads = (int64_t)gridDim.x * gridDim.y * blockDim.x;
         const int A = eo[E];
         const int64_t n0 = 64LL * (z0_cols / 8), n1 = 64LL * (z1_cols / 8);
-        for (int64_t g = (int64_t)blockIdx.x * blockDim.x + tid; g < n0 + n1; g += nthreads) {
+        for (int64_t g = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + tid;
+             g < n0 + n1; g += nthreads) {
             __nv_bfloat16 *z = g < n0 ? z0 : z1;
             const int cols = g < n0 ? z0_cols : z1_cols;
             const int64_t c = g < n0 ? g : g - n0;
@@ -180,7 +181,7 @@ transpose_rows_kernel(const __nv_bfloat16 *__restrict__ src, int H, int k,
     const int seg = eo[e + 1] - eo[e];
     if (tid < 64) tok_s[tid] = blk * 64 + tid < seg ? perm[eo[e] + blk * 64 + tid] / k : -1;
     __syncthreads();
-    for (int h0 = 0; h0 < H; h0 += 128) {
+    for (int h0 = blockIdx.y * 512; h0 < min(H, (int)blockIdx.y * 512 + 512); h0 += 128) {
         // 64 rows x 128 columns of the source in 16-byte chunks; rows past the segment
         // are zero
         uint4 v[4];
@@ -236,7 +237,8 @@ cudaError_t launch_router_dl(const LayerDims &d, const float *dweight_part, int 
 cudaError_t launch_transpose_rows(const LayerDims &d, const void *src, const int32_t *eoff,
                                   const int32_t *perm, void *dstT, int64_t ldt, void *z0, int z0_cols,
                                   void *z1, int z1_cols, cudaStream_t s) {
-    return launch_pdl(transpose_rows_kernel, dim3((unsigned)(ldt / 64)), dim3(256), 0, s, (const __nv_bfloat16 *)src,
+    return launch_pdl(transpose_rows_kernel, dim3((unsigned)(ldt / 64), (unsigned)ceil_div(d.H, 512)),
+                      dim3(256), 0, s, (const __nv_bfloat16 *)src,
                       d.H, d.k, eoff, d.E, perm, (__nv_bfloat16 *)dstT, ldt,
                       (__nv_bfloat16 *)z0, z0_cols, (__nv_bfloat16 *)z1, z1_cols, d.N * d.k);
 }
