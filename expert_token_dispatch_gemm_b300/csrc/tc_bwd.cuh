@@ -33,6 +33,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
 __device__ __forceinline__ void tma_store_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// Arrival on an mbarrier of either CTA of the cluster without release semantics: for
+// handing a TMEM accumulator back after tcgen05.wait::ld, whose loads are complete before
+// the arrive issues. A release arrive would also wait for the thread's earlier global
+// stores, which the waiter does not need.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
 // All but the most recent bulk store have finished reading shared memory.
 __device__ __forceinline__ void tma_store_wait_read1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
