@@ -57,24 +57,48 @@ dx_combine_kernel(const T *__restrict__ dx_slots, const int32_t *__restrict__ sl
     const int my_e = lane < k ? topk_idx[(size_t)t * k + lane] : 0;
     const float my_dl = lane < k ? dl[(size_t)t * k + lane] : 0.f;
     const int nvec = H / V;
+    // the vectors of four slots (then four router rows) are loaded before any is added,
+    // so that their latencies overlap; the sums keep the slot order
     for (int v = lane; v < nvec; v += 32) {
         float acc[V] = {};
-        for (int j = 0; j < k; ++j) {
-            const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-            if (slot < 0) continue;
-            float f[V];
-            Vec16<T>::to_float(
-                __ldg(reinterpret_cast<const uint4 *>(dx_slots + ((size_t)t * k + j) * H) + v), f);
+        for (int j0 = 0; j0 < k; j0 += 4) {
+            uint4 r[4];
+            bool live[4];
 #pragma unroll
-            for (int c = 0; c < V; ++c) acc[c] += f[c];
+            for (int u = 0; u < 4; ++u) {
+                const int slot = __shfl_sync(0xffffffffu, my_slot, (j0 + u) & 31);
+                live[u] = j0 + u < k && slot >= 0;
+                r[u] = live[u] ? __ldg(reinterpret_cast<const uint4 *>(
+                                           dx_slots + ((size_t)t * k + j0 + u) * H) + v)
+                               : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (live[u]) {
+                    float f[V];
+                    Vec16<T>::to_float(r[u], f);
+#pragma unroll
+                    for (int c = 0; c < V; ++c) acc[c] += f[c];
+                }
         }
-        for (int j = 0; j < k; ++j) {
-            const int e = __shfl_sync(0xffffffffu, my_e, j);
-            const float c0 = __shfl_sync(0xffffffffu, my_dl, j);
-            float f[V];
-            Vec16<T>::to_float(__ldg(reinterpret_cast<const uint4 *>(w_router + (size_t)e * H) + v), f);
+        for (int j0 = 0; j0 < k; j0 += 4) {
+            uint4 r[4];
+            float c0[4];
 #pragma unroll
-            for (int c = 0; c < V; ++c) acc[c] = fmaf(c0, f[c], acc[c]);
+            for (int u = 0; u < 4; ++u) {
+                const int e = __shfl_sync(0xffffffffu, my_e, (j0 + u) & 31);
+                c0[u] = __shfl_sync(0xffffffffu, my_dl, (j0 + u) & 31);
+                r[u] = j0 + u < k ? __ldg(reinterpret_cast<const uint4 *>(w_router + (size_t)e * H) + v)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j0 + u < k) {
+                    float f[V];
+                    Vec16<T>::to_float(r[u], f);
+#pragma unroll
+                    for (int c = 0; c < V; ++c) acc[c] = fmaf(c0[u], f[c], acc[c]);
+                }
         }
         reinterpret_cast<uint4 *>(dx + (size_t)t * H)[v] = Vec16<T>::from_float(acc);
     }
