@@ -123,8 +123,14 @@ __device__ __forceinline__ DTile dtile_at(int t, const int *mtp, const int *eo, 
     DTile r;
     decode_tile(t, mtp, ne, m_tiles, r.i, r.m, r.f);
     const int seg = eo[r.i + 1] - eo[r.i];
-    r.tok0 = eo[r.i] + r.m * BN;
-    r.ntok = min(BN, seg - r.m * BN);
+    // dgrad-down splits an expert's rows evenly over its ceil(rows / 256) token tiles (a
+    // multiple of 64 each but the last), so that no tile is a short remainder: the tiles
+    // of an expert then take about as long, and the adjacent CTAs running them stay
+    // together and share the weight strip in L2
+    const int ntiles = mtp[r.i + 1] - mtp[r.i];
+    const int base = KIND == BWD_DGRAD_DOWN ? ((seg + ntiles - 1) / ntiles + 63) & ~63 : BN;
+    r.tok0 = eo[r.i] + r.m * base;
+    r.ntok = min(base, seg - r.m * base);
     r.nmma = KIND == BWD_DGRAD_DOWN ? (r.ntok + 63) & ~63 : (r.ntok + 31) & ~31;
     return r;
 }
@@ -442,7 +448,8 @@ grouped_gemm_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                             *reinterpret_cast<uint4 *>(swa + (item >> 4) * BM + (item & 15) * 8) = wa_v[s2];
                         }
                         half_sync(half);
-                        const int64_t colT = 64LL * pk[dt.i] + (int64_t)dt.m * BN + c;
+                        // the tile's first column: its first row's place in the expert's block
+                        const int64_t colT = 64LL * pk[dt.i] + (dt.tok0 - eo[dt.i]) + c;
 #pragma unroll
                         for (int s2 = 0; s2 < 2 && blk_live; ++s2) {
                             const int item = htid + 128 * s2;
