@@ -231,6 +231,23 @@ def test_training_grows_the_workspace(moe):
     assert status_of(moe, c)[0] == 1
 
 
+def test_bf16_training_workspace_holds_the_transposed_operands(moe):
+    """A bf16 training workspace also holds x^T [H, T] and (w a)^T [Ipad, T], the
+    weight-gradient GEMMs' K-major operands (T = N*k rounded up to 64, plus 64 E: every
+    expert's rows in whole 64-row blocks), on top of what the fp32 backward needs."""
+    N, H, I, E, k = 64, 64, 32, 8, 2
+    Ipad = 128
+    T = (N * k + 63) // 64 * 64 + 64 * E
+    sizes = {}
+    for dtype, es in (("bf16", 2), ("fp32", 4)):
+        c = cfg(moe, dtype=dtype)
+        _, base = status_of(moe, c)
+        c.training = 1
+        _, grown = status_of(moe, c)
+        sizes[dtype] = (grown - base) / es   # elements
+    assert sizes["bf16"] - sizes["fp32"] >= (H + Ipad) * T
+
+
 def test_backward_needs_a_training_config(moe):
     c = cfg(moe)
     st = moe.lib.moe_layer_backward(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
