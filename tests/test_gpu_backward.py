@@ -36,6 +36,9 @@ SHAPES = [
     # more tiles than clusters of two SMs in all four GEMMs: each cluster runs several
     # tiles, the ring and both accumulators cycle through several phases
     S("b_persistent", N=2048, H=512, I=256, E=64, top_k=8, ep_size=8),
+    # the most experts the tile tables hold (256), ~16 rows each: most segments end
+    # inside their only 64-row block of the transposed operands
+    S("b_max_experts", N=512, H=128, I=64, E=256, top_k=8, ep_size=8),
     # fp32 layers (FFMA kernels): ragged tiles, drops, the PR1 configuration
     S("f_ragged", N=333, H=96, I=72, E=8, top_k=2, ep_size=4, dtype="fp32", bias=True),
     S("f_cap", N=500, H=64, I=136, E=4, top_k=2, ep_size=2, capacity_factor=0.6, dtype="fp32"),
