@@ -1,8 +1,8 @@
 """The benchmark's host arithmetic, on CPU: algorithmic work per stage (closed forms of
 each stage's byte and flop counts on a hand-checked shape), the roofline's choice of
 bound and fraction, the traffic record's guard on the GEMM sources, whole-job
-throughput, the load summary, and the CPU legs (one-thread pinning, token sample,
-the same config in both arms)."""
+throughput, the load summary, the CPU legs (one-thread pinning, token sample, the same
+config in both arms), and the reference arm's line (run on a small workload)."""
 import json
 import math
 
@@ -134,3 +134,56 @@ def test_both_arms_share_one_config():
     c2 = bench.run_config(workloads.GPTOSS, "dispatch", 1)
     assert c1 == c2 and c1["workload"] == workloads.GPTOSS.name
     assert c1["mode"] == "dispatch" and "parallelism" in c1
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` on a small workload: one JSON line whose metric,
+    config and timing fields match the GPU arm's, with the oracle's one-thread CPU
+    baseline and an end-to-end figure that moves no bytes between host and device."""
+    import os
+    import subprocess
+    import sys
+    shape = workloads.PR1_FP32
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                        shape.name, "--steps", "1", "--warmup", "3"], cwd=root,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["higher_is_better"] is True and d["n_gpus"] == 1
+    assert d["steps"] == 1 and d["warmup"] == 3
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"] == bench.run_config(shape, "dispatch", 1)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"]
+    assert isinstance(cb["sample"], str) and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun the reference arm runs on rank 0 alone; another rank exits 0
+    without output, and rank 0's line counts the launch's GPUs."""
+    import os
+    import subprocess
+    import sys
+    shape = workloads.PR1_FP32
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", shape.name,
+           "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    for rank in (1, 0):
+        env = dict(os.environ, RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE="2")
+        r = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+        if rank:
+            assert lines == []
+        else:
+            assert len(lines) == 1
+            d = json.loads(lines[0])
+            assert d["n_gpus"] == 2 and d["config"] == bench.run_config(shape, "dispatch", 2)
