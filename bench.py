@@ -462,7 +462,10 @@ def load_summary(shape, routed, kept):
                 routed_pairs=int(routed.sum()), dropped_pairs=int(routed.sum() - kept.sum()))
 
 
-BACKWARD_LAUNCHES = 11   # permute, 4 GEMMs, logit grads, dx combine, histogram, scan, 2 router
+def backward_launches(dtype):
+    """Kernels of one moe_layer_backward call: permute, (bf16: the transposed copy of x,)
+    the 4 expert GEMMs, logit gradients, dx combine, histogram, scan, 2 router-gradient."""
+    return 12 if dtype == "bf16" else 11
 
 
 def time_backward(moe, args, shape, inp, packed, dist, dev, stream, mode=None):
@@ -528,7 +531,8 @@ def time_backward(moe, args, shape, inp, packed, dist, dev, stream, mode=None):
                               peak=peak, frac=round(ach / peak, 4) if peak else None,
                               source=psrc,
                               note="whole backward time against the expert GEMMs' flops"),
-                gpu_launches=(6 + BACKWARD_LAUNCHES) * args.steps, clocks=clk.summary())
+                gpu_launches=(FORWARD_LAUNCHES + backward_launches(shape.dtype)) * args.steps,
+                clocks=clk.summary())
 
 
 def _event_ms(stream, fn, steps):
