@@ -587,7 +587,7 @@ def time_variants(moe, args, shape, inp, packed, dev, stream):
         ms = float(np.mean([a.elapsed_time(z) for a, z in evs[prio]]))
         res[f"{prio}_priority_forward"] = dict(ms=round(ms, 4),
                                                tokens_per_s=round(shape.N / (ms * 1e-3), 1),
-                                               gpu_launches_per_step=6 if prio == "token" else 7)
+                                               gpu_launches_per_step=FORWARD_LAUNCHES + (prio == "slot"))
     cfg, ws = cfgs["slot"], wss["slot"]
     logits = torch.empty(shape.N, shape.E, device=dev)
     routed = torch.empty(shape.E, dtype=torch.int32, device=dev)
@@ -600,13 +600,13 @@ def time_variants(moe, args, shape, inp, packed, dev, stream):
     nbytes = shape.N * shape.E * 4 + shape.E * 12
     res["balance_stats"] = dict(ms=round(ms, 4), bound="hbm", achieved=round(nbytes / ms / 1e6, 1),
                                 peak=bw, unit="GB/s", frac=round(nbytes / ms / 1e6 / bw, 4),
-                                gpu_launches_per_step=2)
+                                gpu_launches_per_step=STATS_LAUNCHES)
     padded = torch.zeros(2, shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
     ms = _event_ms(stream, lambda: moe.moe_tp_reduce(cfg, 2, padded, out), args.steps)
     nbytes = 3 * shape.N * shape.H * s
     res["tp_reduce_tp2"] = dict(ms=round(ms, 4), bound="hbm", achieved=round(nbytes / ms / 1e6, 1),
                                 peak=bw, unit="GB/s", frac=round(nbytes / ms / 1e6 / bw, 4),
-                                gpu_launches_per_step=1,
+                                gpu_launches_per_step=TP_REDUCE_LAUNCHES,
                                 note="inputs below L2 size at small workloads: fractions above "
                                      "1 are L2 hits")
     res["peak_source"] = source
@@ -656,6 +656,8 @@ class Layer:
 
 
 FORWARD_LAUNCHES = 6   # route, scan/assign, permute, gate_up, down, combine
+STATS_LAUNCHES = 2     # moe_balance_stats: per-block partial sums, their ordered total
+TP_REDUCE_LAUNCHES = 1
 
 
 def time_forward(moe, L, steps, warmup, dist, dev, stream, clocks=True):

@@ -30,16 +30,20 @@ def library_kernels(fn):
             if e.device_type == torch.autograd.DeviceType.CUDA and "moe::" in e.name]
 
 
-def small_layer(dtype, mode="dispatch"):
+def small_layer(dtype, mode="dispatch", capacity_priority="token"):
     shape = workloads.LayerShape("launches_" + dtype, N=700, H=128, I=96, E=8, top_k=2,
                                  ep_size=4, capacity_factor=1.0, dtype=dtype, bias=True)
-    return shape, Layer(shape, workloads.layer_inputs(shape, seed=5, variant="perf"), mode=mode)
+    return shape, Layer(shape, workloads.layer_inputs(shape, seed=5, variant="perf"), mode=mode,
+                        capacity_priority=capacity_priority)
 
 
-@pytest.mark.parametrize("dtype,mode", [("bf16", "dispatch"), ("bf16", "mask_sum"),
-                                        ("fp32", "dispatch")])
-def test_forward_launches_what_the_bench_counts(dtype, mode):
-    shape, layer = small_layer(dtype, mode)
+@pytest.mark.parametrize("dtype,mode,prio", [("bf16", "dispatch", "token"),
+                                             ("bf16", "mask_sum", "token"),
+                                             ("fp32", "dispatch", "token"),
+                                             ("bf16", "dispatch", "slot")])
+def test_forward_launches_what_the_bench_counts(dtype, mode, prio):
+    """6 kernels per forward; slot-major capacity priority adds its histogram kernel."""
+    shape, layer = small_layer(dtype, mode, prio)
     out = torch.empty(shape.N, shape.H, dtype=shape.torch_dtype, device="cuda")
 
     def fwd():
@@ -48,7 +52,34 @@ def test_forward_launches_what_the_bench_counts(dtype, mode):
     fwd()                                   # kernel set-up outside the profile
     torch.cuda.synchronize()
     kernels = library_kernels(fwd)
-    assert len(kernels) == bench.FORWARD_LAUNCHES, kernels
+    assert len(kernels) == bench.FORWARD_LAUNCHES + (prio == "slot"), kernels
+
+
+def test_stats_and_tp_reduce_launch_what_the_bench_counts():
+    """moe_balance_stats: partial sums and their ordered total (2 kernels); moe_tp_reduce
+    for two slices: one kernel."""
+    shape, layer = small_layer("bf16")
+    dev = layer.x.device
+    out = torch.empty(shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
+    logits = torch.empty(shape.N, shape.E, device=dev)
+    routed = torch.empty(shape.E, dtype=torch.int32, device=dev)
+    moe.moe_layer_forward(layer.cfg, layer.x, layer.w_router, layer.b_router, layer.packed,
+                          layer.w_down, out, layer.ws,
+                          dict(router_logits=logits, routed_counts=routed))
+    load = torch.empty(shape.E, device=dev)
+    prob = torch.empty(shape.E, device=dev)
+    padded = torch.zeros(2, shape.N, shape.H, dtype=shape.torch_dtype, device=dev)
+
+    def stats():
+        moe.moe_balance_stats(layer.cfg, logits, routed, load, prob, layer.ws)
+
+    def reduce():
+        moe.moe_tp_reduce(layer.cfg, 2, padded, out)
+    stats()
+    reduce()
+    torch.cuda.synchronize()
+    assert len(library_kernels(stats)) == bench.STATS_LAUNCHES
+    assert len(library_kernels(reduce)) == bench.TP_REDUCE_LAUNCHES
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
