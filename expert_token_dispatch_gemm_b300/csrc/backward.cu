@@ -48,14 +48,21 @@ dx_combine_kernel(const T *__restrict__ dx_slots, const int32_t *__restrict__ sl
                   const int32_t *__restrict__ topk_idx, const float *__restrict__ dl,
                   const T *__restrict__ w_router, int N, int H, int k, T *__restrict__ dx) {
     constexpr int V = Vec16<T>::N;
+    // the token's slots, experts and logit gradients, shared by the warp's lanes (a lane
+    // past the last vector of a row takes no part in the loop below)
+    __shared__ int slot_s[8][32], e_s[8][32];
+    __shared__ float dl_s[8][32];
     grid_dep_wait();
     grid_dep_trigger();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int t = blockIdx.x * 8 + warp;
     if (t >= N) return;
-    const int my_slot = lane < k ? slot_pos[(size_t)t * k + lane] : -1;
-    const int my_e = lane < k ? topk_idx[(size_t)t * k + lane] : 0;
-    const float my_dl = lane < k ? dl[(size_t)t * k + lane] : 0.f;
+    if (lane < k) {
+        slot_s[warp][lane] = slot_pos[(size_t)t * k + lane];
+        e_s[warp][lane] = topk_idx[(size_t)t * k + lane];
+        dl_s[warp][lane] = dl[(size_t)t * k + lane];
+    }
+    __syncwarp();
     const int nvec = H / V;
     // the vectors of four slots (then four router rows) are loaded before any is added,
     // so that their latencies overlap; the sums keep the slot order
@@ -66,8 +73,8 @@ dx_combine_kernel(const T *__restrict__ dx_slots, const int32_t *__restrict__ sl
             bool live[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int slot = __shfl_sync(0xffffffffu, my_slot, (j0 + u) & 31);
-                live[u] = j0 + u < k && slot >= 0;
+                const int slot = j0 + u < k ? slot_s[warp][j0 + u] : -1;
+                live[u] = slot >= 0;
                 r[u] = live[u] ? __ldg(reinterpret_cast<const uint4 *>(
                                            dx_slots + ((size_t)t * k + j0 + u) * H) + v)
                                : make_uint4(0u, 0u, 0u, 0u);
@@ -86,10 +93,10 @@ dx_combine_kernel(const T *__restrict__ dx_slots, const int32_t *__restrict__ sl
             float c0[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int e = __shfl_sync(0xffffffffu, my_e, (j0 + u) & 31);
-                c0[u] = __shfl_sync(0xffffffffu, my_dl, (j0 + u) & 31);
-                r[u] = j0 + u < k ? __ldg(reinterpret_cast<const uint4 *>(w_router + (size_t)e * H) + v)
-                                  : make_uint4(0u, 0u, 0u, 0u);
+                const bool in = j0 + u < k;
+                c0[u] = in ? dl_s[warp][j0 + u] : 0.f;
+                r[u] = in ? __ldg(reinterpret_cast<const uint4 *>(w_router + (size_t)e_s[warp][j0 + u] * H) + v)
+                          : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u)

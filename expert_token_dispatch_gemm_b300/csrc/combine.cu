@@ -153,12 +153,15 @@ mask_sum_small_kernel(const T *__restrict__ slots, const int32_t *__restrict__ i
     }
 }
 
-// k > 8: the same sums, with each partition's slots found per vector.
+// k > 8: the same sums. The (partition, slot) order is found once per token, with every
+// lane of the warp in the ballots and shuffles, and kept in shared memory (up to 32
+// entries); then each vector runs the same fixed sequence of adds as the small kernels.
 template <typename T>
 __global__ void __launch_bounds__(256)
 mask_sum_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
                 const int32_t *__restrict__ slot_pos, int N, int k, int H, int E, int P,
                 T *__restrict__ out) {
+    __shared__ int order_s[8][32];
     grid_dep_wait();
     grid_dep_trigger();
     using V = Vec16<T>;
@@ -171,33 +174,41 @@ mask_sum_kernel(const T *__restrict__ slots, const int32_t *__restrict__ idx,
     const int nvec = H / V::N;
     const uint4 *src = reinterpret_cast<const uint4 *>(slots + (size_t)t * k * H);
     uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)t * H);
+    unsigned todo = __ballot_sync(0xffffffffu, owner >= 0) & ((k < 32) ? ((1u << k) - 1u) : ~0u);
+    uint32_t ends = 0;
+    int nk = 0;
+    while (todo) {
+        // lowest partition among the remaining slots, its slots in slot order
+        int pmin = 0x7fffffff;
+        for (unsigned m = todo; m; m &= m - 1) {
+            const int o = __shfl_sync(0xffffffffu, owner, __ffs(m) - 1);
+            pmin = o < pmin ? o : pmin;
+        }
+        const unsigned mine = __ballot_sync(0xffffffffu, owner == pmin) & todo;
+        for (unsigned m = mine; m; m &= m - 1) {
+            if (lane == 0) order_s[warp][nk] = __ffs(m) - 1;
+            ++nk;
+        }
+        ends |= 1u << (nk - 1);
+        todo &= ~mine;
+    }
+    __syncwarp();
     for (int v = lane; v < nvec; v += 32) {
-        float acc[V::N];
+        float acc[V::N], part[V::N];
 #pragma unroll
-        for (int i = 0; i < V::N; ++i) acc[i] = 0.f;
-        int p = -1;
-        unsigned todo = __ballot_sync(0xffffffffu, owner >= 0) & ((k < 32) ? ((1u << k) - 1u) : ~0u);
-        while (todo) {
-            // lowest partition among the remaining slots
-            int pmin = 0x7fffffff;
-            for (unsigned m = todo; m; m &= m - 1) {
-                const int o = __shfl_sync(0xffffffffu, owner, __ffs(m) - 1);
-                pmin = o < pmin ? o : pmin;
+        for (int i = 0; i < V::N; ++i) acc[i] = part[i] = 0.f;
+        for (int s = 0; s < nk; ++s) {
+            float f[V::N];
+            V::to_float(__ldg(src + (size_t)order_s[warp][s] * nvec + v), f);
+#pragma unroll
+            for (int i = 0; i < V::N; ++i) part[i] += f[i];
+            if ((ends >> s) & 1u) {
+#pragma unroll
+                for (int i = 0; i < V::N; ++i) {
+                    acc[i] += part[i];
+                    part[i] = 0.f;
+                }
             }
-            p = pmin;
-            const unsigned mine = __ballot_sync(0xffffffffu, owner == p);
-            float part[V::N];
-#pragma unroll
-            for (int i = 0; i < V::N; ++i) part[i] = 0.f;
-            for (unsigned m = mine; m; m &= m - 1) {
-                float f[V::N];
-                V::to_float(__ldg(src + (size_t)(__ffs(m) - 1) * nvec + v), f);
-#pragma unroll
-                for (int i = 0; i < V::N; ++i) part[i] += f[i];
-            }
-#pragma unroll
-            for (int i = 0; i < V::N; ++i) acc[i] += part[i];
-            todo &= ~mine;
         }
         dst[v] = V::from_float(acc);
     }

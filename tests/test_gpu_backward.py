@@ -39,6 +39,11 @@ SHAPES = [
     # the most experts the tile tables hold (256), ~16 rows each: most segments end
     # inside their only 64-row block of the transposed operands
     S("b_max_experts", N=512, H=128, I=64, E=256, top_k=8, ep_size=8),
+    # the smallest hidden and intermediate sizes (8): one K block and one weight tile,
+    # mostly outside the tensors
+    S("b_min_sizes", N=300, H=8, I=8, E=4, top_k=2, ep_size=2, bias=True),
+    # 33 vectors per row: the last pass of dx combine has one active lane for 4 slots
+    S("b_ragged_rows", N=300, H=264, I=64, E=16, top_k=4, ep_size=4),
     # fp32 layers (FFMA kernels): ragged tiles, drops, the PR1 configuration
     S("f_ragged", N=333, H=96, I=72, E=8, top_k=2, ep_size=4, dtype="fp32", bias=True),
     S("f_cap", N=500, H=64, I=136, E=4, top_k=2, ep_size=2, capacity_factor=0.6, dtype="fp32"),

@@ -113,6 +113,10 @@ EDGE = [
     S("capacity_one", N=300, H=64, I=32, E=8, top_k=2, ep_size=4, capacity_factor=1e-4),
     S("ragged_segments", N=65, H=136, I=24, E=3, top_k=2, ep_size=1),
     S("fp32_one_token", N=1, H=32, I=16, E=2, top_k=1, ep_size=2, dtype="fp32"),
+    # the smallest sizes the boundary accepts (multiples of 8): every copy box is wider
+    # than the tensor it reads
+    S("min_sizes_bf16", N=300, H=8, I=8, E=4, top_k=2, ep_size=2, bias=True),
+    S("min_sizes_fp32", N=300, H=8, I=8, E=4, top_k=2, ep_size=2, dtype="fp32", bias=True),
 ]
 
 
@@ -122,6 +126,25 @@ def test_edge_cases(shape):
     ref = oracle_layer(shape, inp)
     layer = Layer(shape, inp)
     out, diag = layer.forward()
+    assert_routing_and_layout_exact(diag, ref, shape)
+    assert_close(out, ref["out"], tol_for(shape))
+
+
+# A row of H values is nvec = H / (8 bf16 or 4 fp32) 16-byte vectors, one per lane, 32 at
+# a time: with H = 264 (bf16) or 136 (fp32) the last pass over a row has 1 or 2 active
+# lanes, fewer than the k = 12 slots whose owners the warp must still see together.
+RAGGED_ROWS = [
+    S("k12_ragged_rows_bf16", N=300, H=264, I=64, E=32, top_k=12, ep_size=4, bias=True),
+    S("k12_ragged_rows_fp32", N=300, H=136, I=32, E=32, top_k=12, ep_size=4, dtype="fp32"),
+]
+
+
+@pytest.mark.parametrize("mode", ["dispatch", "mask_sum"])
+@pytest.mark.parametrize("shape", RAGGED_ROWS, ids=lambda s: s.name)
+def test_many_slots_with_a_ragged_last_row_pass(shape, mode):
+    inp = _inputs(shape, seed=12)
+    ref = oracle_layer(shape, inp, mode=mode)
+    out, diag = Layer(shape, inp, mode=mode).forward()
     assert_routing_and_layout_exact(diag, ref, shape)
     assert_close(out, ref["out"], tol_for(shape))
 
