@@ -120,11 +120,12 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("mode", ["dispatch", "mask_sum"])
 @pytest.mark.parametrize("shape", EDGE, ids=lambda s: s.name)
-def test_edge_cases(shape):
+def test_edge_cases(shape, mode):
     inp = _inputs(shape, seed=8)
-    ref = oracle_layer(shape, inp)
-    layer = Layer(shape, inp)
+    ref = oracle_layer(shape, inp, mode)
+    layer = Layer(shape, inp, mode)
     out, diag = layer.forward()
     assert_routing_and_layout_exact(diag, ref, shape)
     assert_close(out, ref["out"], tol_for(shape))
