@@ -34,6 +34,10 @@ PRIORITY_SHAPES = [
     S("p_fp32_cap", N=613, H=96, I=72, E=8, top_k=2, ep_size=4, capacity_factor=0.6,
       dtype="fp32", bias=True),
     S("p_one_token", N=1, H=64, I=32, E=4, top_k=2, ep_size=2, capacity_factor=0.5),
+    # more slots per token than the register-list combine kernels take (k > 8), and the
+    # most (k = 32): spans of 64k tokens, k segments each
+    S("p_bf16_k12_cap", N=1500, H=136, I=32, E=32, top_k=12, ep_size=4, capacity_factor=0.9),
+    S("p_bf16_k32_cap", N=300, H=64, I=32, E=64, top_k=32, ep_size=8, capacity_factor=1.1),
 ]
 
 
