@@ -44,6 +44,9 @@ SHAPES = [
     S("b_min_sizes", N=300, H=8, I=8, E=4, top_k=2, ep_size=2, bias=True),
     # 33 vectors per row: the last pass of dx combine has one active lane for 4 slots
     S("b_ragged_rows", N=300, H=264, I=64, E=16, top_k=4, ep_size=4),
+    # more slots per token than 8 (with drops), and the most (32)
+    S("b_k12_cap", N=500, H=136, I=64, E=32, top_k=12, ep_size=4, capacity_factor=0.9),
+    S("b_k32", N=200, H=64, I=32, E=64, top_k=32, ep_size=8),
     # fp32 layers (FFMA kernels): ragged tiles, drops, the PR1 configuration
     S("f_ragged", N=333, H=96, I=72, E=8, top_k=2, ep_size=4, dtype="fp32", bias=True),
     S("f_cap", N=500, H=64, I=136, E=4, top_k=2, ep_size=2, capacity_factor=0.6, dtype="fp32"),
