@@ -10,10 +10,12 @@ intermediate 2880, 8 logical EP partitions). Its 6.4 GB of expert weights are ~5
 L2, so no L2 flush is needed between steps.
 
 The line also carries, for the same workload, the per-stage rooflines, the training
-step, the routing variants and an end-to-end figure with host copies, and (one GPU
-only) a `workloads` object: the other forward rule on the same inputs and the PR1,
-8-expert, skewed + capacity and decode workloads, each with its stage rooflines,
-clocks and training step.
+step, the routing variants, an end-to-end figure with host copies and a `sustained`
+figure (100 back-to-back forwards, long enough for the board's power cap to act; the
+headline's 20-step region ends before it does), and (one GPU only) a `workloads`
+object: the other forward rule on the same inputs and the PR1, 8-expert, skewed +
+capacity and decode workloads, each with its stage rooflines, clocks and training
+step.
 
 Under torchrun (N > 1) every rank runs the same layer on its own batch (different
 seed): the expert-parallel partitions live inside one GPU, so ranks share no data and
@@ -740,6 +742,27 @@ def dominant_roofline(shape, stage_ms, counts, with_traffic=True):
                 traffic=measured_traffic(shape.name, dom) if with_traffic else None)
 
 
+SUSTAINED_STEPS = 100
+
+
+def time_sustained(moe, L, dev, stream, steps=SUSTAINED_STEPS):
+    """Back-to-back forwards for ~0.2 s (device time), with their own clock record: the
+    rate once the board's power management has reacted. The headline's timed region
+    (20 steps by default) ends before it does; this is reported beside it, not in it."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index or 0) as clk:
+        torch.cuda._sleep(2_000_000)
+        a.record(stream)
+        for _ in range(steps):
+            L.forward(moe)
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return dict(steps=steps, ms_per_step=round(ms, 4),
+                tokens_per_s=round(L.shape.N / (ms * 1e-3), 1), clocks=clk.summary())
+
+
 def time_e2e(moe, L, steps, dist, dev, stream):
     """End to end through the C ABI: every step copies its input from pinned host memory
     to the device and reads its output back. Copies run on their own streams, double
@@ -830,6 +853,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-sustained", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other workloads and the mask-and-sum line")
     args = ap.parse_args()
@@ -868,6 +892,8 @@ def main():
     if not args.no_backward:
         backward = time_backward(moe, args, shape, L.inp, L.packed, dist, dev, stream)
     e2e = None if args.no_e2e else time_e2e(moe, L, args.steps, dist, dev, stream)
+    # last on this workload: its stretch at the power cap would slow what follows
+    sustained = None if args.no_sustained else time_sustained(moe, L, dev, stream)
 
     roof = dominant_roofline(shape, r["stage_ms"], counts)
     per_stage = stage_rooflines(shape, r["stage_ms"], counts, moe.binding.STAGE_NAMES)
@@ -906,7 +932,8 @@ def main():
                     cpu_baseline=cpu, e2e=e2e,
                     gpu_launches=FORWARD_LAUNCHES * args.steps, clocks=r["clocks"],
                     kept_pairs=int(counts.sum()), load=load_summary(shape, r["routed"], counts),
-                    backward=backward, variants=variants, workloads=others, impl="b300")
+                    sustained=sustained, backward=backward, variants=variants,
+                    workloads=others, impl="b300")
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

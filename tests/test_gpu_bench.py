@@ -140,6 +140,9 @@ def test_bench_line_carries_its_contract():
     assert d["gpu_launches"] == bench.FORWARD_LAUNCHES * steps
     clk = d["clocks"]
     assert clk["sm_mhz"] > 0 and clk["sm_max_mhz"] > 0 and isinstance(clk["reasons"], list)
+    sus = d["sustained"]
+    assert sus["steps"] == bench.SUSTAINED_STEPS and sus["ms_per_step"] > 0
+    assert abs(sus["tokens_per_s"] - shape.N / (sus["ms_per_step"] * 1e-3)) <= 1e-3 * sus["tokens_per_s"]
     bwd = d["backward"]
     assert bwd["backward_ms"] > 0 and bwd["roofline"]["frac"] > 0
     assert bwd["gpu_launches"] == (bench.FORWARD_LAUNCHES + bench.backward_launches("bf16")) * steps
