@@ -47,6 +47,8 @@ SHAPES = [
     # more slots per token than 8 (with drops), and the most (32)
     S("b_k12_cap", N=500, H=136, I=64, E=32, top_k=12, ep_size=4, capacity_factor=0.9),
     S("b_k32", N=200, H=64, I=32, E=64, top_k=32, ep_size=8),
+    S("f_k12_cap", N=400, H=72, I=40, E=32, top_k=12, ep_size=4, capacity_factor=0.9,
+      dtype="fp32", bias=True),
     # fp32 layers (FFMA kernels): ragged tiles, drops, the PR1 configuration
     S("f_ragged", N=333, H=96, I=72, E=8, top_k=2, ep_size=4, dtype="fp32", bias=True),
     S("f_cap", N=500, H=64, I=136, E=4, top_k=2, ep_size=2, capacity_factor=0.6, dtype="fp32"),

@@ -117,6 +117,8 @@ EDGE = [
     # than the tensor it reads
     S("min_sizes_bf16", N=300, H=8, I=8, E=4, top_k=2, ep_size=2, bias=True),
     S("min_sizes_fp32", N=300, H=8, I=8, E=4, top_k=2, ep_size=2, dtype="fp32", bias=True),
+    # the FFMA router and experts at the most experts and slots
+    S("fp32_max_experts_max_k", N=130, H=64, I=32, E=256, top_k=32, ep_size=8, dtype="fp32"),
 ]
 
 
